@@ -1,0 +1,384 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* hand-derived worked examples under tests/golden/ (full plans);
+* the pages' invariants on seeded inputs of every workload shape (plan_checks);
+* closed forms: maxvio, the moved-route lower bound, combine(dispatch(x)) =
+  K*x, constant-fill gradient reduce;
+* special cases that reduce to library routines: a perfectly balanced routing
+  is a stable sort by expert (numpy argsort), dispatch is a fancy-indexed
+  scatter, prefetch is a row copy, bf16 rounding is torch's conversion;
+* error bounds: combine within one bf16 ulp of the exact (fp64) K-sum,
+  gradient reduce within the fp32 accumulation bound of the exact sum.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from combine_moonep_plan_gb300 import workloads as wl
+from tests.plan_checks import check_plan, decode
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _cfg(sh):
+    return dict(R=sh.R, E=sh.E, K=sh.K, S=sh.S, B=sh.B, tp=sh.tp)
+
+
+def _plan(oracle, cfg, topk, tpe=None, dup=True):
+    st, p = oracle.plan(cfg["R"], cfg["E"], cfg["K"], cfg["S"], cfg["B"], cfg["tp"],
+                        topk, tpe, dup_records=dup)
+    return st, p
+
+
+# --------------------------------------------------------------- goldens
+
+@pytest.mark.parametrize("name", ["plan_two_ranks_dup.json",
+                                  "plan_chain_donor_turns_receiver.json"])
+def test_golden_plan(oracle_mod, name):
+    g = json.load(open(os.path.join(GOLDEN, name)))
+    cfg = g["config"]
+    topk = np.array(g["topk"], np.int32)
+    st, p = _plan(oracle_mod, cfg, topk)
+    assert st == 0
+    assert p["NvS"] == g["NvS"]
+    for f in ("dst", "experts_to_copy", "cu_seqlens", "zero_fill_ranges",
+              "remote_stats", "dup_counts"):
+        assert np.array_equal(p[f], np.array(g[f], np.int32)), f
+    for j in range(cfg["R"]):
+        ng = len(g["dup_groups_valid"][j])
+        assert np.array_equal(p["dup_groups"][j, :ng], np.array(g["dup_groups_valid"][j], np.int32).reshape(ng, 3))
+        assert np.all(p["dup_groups"][j, ng:] == -1)
+        nd = len(g["dup_loffs_valid"][j])
+        assert np.array_equal(p["dup_loffs"][j, :nd], np.array(g["dup_loffs_valid"][j], np.int32))
+    check_plan(cfg, topk, p)
+
+
+# ------------------------------------------------------------ invariants
+
+def _small_shapes():
+    yield "tiny", wl.SHAPES["tiny"]
+    # the large shapes scaled down in S only (same R, E, K, B, tp ratios)
+    for n in ("mixtral", "deepseek_v3", "kimi_k2", "qwen3_decode"):
+        sh = wl.SHAPES[n]
+        yield n, wl.Shape(n + "_s64", R=sh.R, E=sh.E, K=sh.K, S=64, H=64, Hp=8,
+                          B=sh.B, tp=sh.tp, weights=sh.weights)
+
+
+@pytest.mark.parametrize("name,sh", list(_small_shapes()), ids=[n for n, _ in _small_shapes()])
+@pytest.mark.parametrize("kind", ["exact0", "uniform", "zipf1", "zipf3", "hot"])
+def test_oracle_plan_invariants(oracle_mod, name, sh, kind):
+    if kind == "exact0":
+        topk, _ = wl.routing(sh, "exact0", seed=3)
+    elif kind == "uniform":
+        topk, _ = wl.routing(sh, "uniform", seed=4)
+    elif kind == "zipf1":
+        topk, _ = wl.routing(sh, "zipf", zipf_s=1.0, seed=5)
+    elif kind == "zipf3":
+        topk, _ = wl.routing(sh, "zipf", zipf_s=3.0, seed=6)
+    else:
+        topk, _ = wl.routing(sh, "hot", hot_share=0.3, seed=7)
+    cfg = _cfg(sh)
+    st, p = _plan(oracle_mod, cfg, topk, wl.tokens_per_expert(topk, sh.E))
+    assert st == 0
+    info = check_plan(cfg, topk, p)
+    # closed form: routes that must leave home >= sum of overloads
+    assert info["moved"] >= info["lower_bound"]
+
+
+def test_oracle_full_size_plan_invariants(oracle_mod):
+    sh = wl.SHAPES["deepseek_v3"]
+    topk, info = wl.routing(sh, "zipf", zipf_s=1.1, seed=11)
+    cfg = _cfg(sh)
+    st, p = _plan(oracle_mod, cfg, topk, wl.tokens_per_expert(topk, sh.E))
+    assert st == 0
+    res = check_plan(cfg, topk, p, max_records=256)
+    assert res["moved"] >= res["lower_bound"]
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_oracle_random_tiny_configs(oracle_mod, seed):
+    """Random small configurations, duplicates allowed within a token (as when
+    invalid ids are mapped to expert 0)."""
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, 5))
+    L = int(rng.integers(1, 4))
+    E = R * L
+    K = int(rng.integers(1, 4))
+    S = int(rng.integers(0, 7))
+    B = L + int(rng.integers(0, 2))
+    tp = int(rng.integers(1, 5))
+    skew = rng.random(E) ** 3
+    topk = rng.choice(E, size=(R, S, K), p=skew / skew.sum()).astype(np.int32)
+    cfg = dict(R=R, E=E, K=K, S=S, B=B, tp=tp)
+    st, p = _plan(oracle_mod, cfg, topk)
+    assert st == 0
+    if S:
+        info = check_plan(cfg, topk, p)
+        assert info["moved"] >= info["lower_bound"]
+
+
+def test_moved_equals_lower_bound_when_no_donor_receives(oracle_mod):
+    """With a single overloaded group the chain never turns a donor into a
+    receiver, so exactly the overload moves."""
+    sh = wl.SHAPES["tiny"]
+    R, E, K, S = sh.R, sh.E, sh.K, sh.S
+    rng = np.random.default_rng(0)
+    # rank-group 0 gets 70% of the routes
+    p = np.array([0.7 / 4] * 4 + [0.3 / 4] * 4)
+    topk = np.stack([np.stack([rng.choice(E, K, replace=False, p=p) for _ in range(S)]) for _ in range(R)]).astype(np.int32)
+    st, pl = _plan(oracle_mod, _cfg(sh), topk)
+    assert st == 0
+    info = check_plan(_cfg(sh), topk, pl)
+    assert info["moved"] == info["lower_bound"]
+
+
+# ----------------------------------------------- balanced = stable sort
+
+@pytest.mark.parametrize("name", ["tiny", "deepseek_v3", "qwen3_decode"])
+def test_balanced_routing_is_a_stable_sort(oracle_mod, name):
+    """When every home group already holds S*K routes nothing moves, and the
+    plan is the stable sort of each rank's home routes by expert id, padded per
+    expert (numpy argsort, kind='stable')."""
+    sh = wl.SHAPES[name]
+    if name != "tiny":
+        sh = wl.Shape(name, R=sh.R, E=sh.E, K=sh.K, S=min(sh.S, 256), H=8, Hp=8,
+                      B=sh.B, tp=sh.tp, weights=sh.weights)
+    topk, info = wl.routing(sh, "exact0", seed=1)
+    assert abs(info["maxvio"]) < 1e-12
+    R, E, K, S, tp, L, C = sh.R, sh.E, sh.K, sh.S, sh.tp, sh.L, sh.C
+    st, p = _plan(oracle_mod, _cfg(sh), topk)
+    assert st == 0
+    NvS = p["NvS"]
+    flat = topk.reshape(-1).astype(np.int64)
+    expect_g = np.zeros(R * C, np.int64)
+    for j in range(R):
+        mine = np.nonzero(flat // L == j)[0]            # route ids in (r,s,k) order
+        order = mine[np.argsort(flat[mine], kind="stable")]
+        counts = np.bincount(flat[order] - j * L, minlength=L)
+        padded = -(-counts // tp) * tp
+        start = np.concatenate([[0], np.cumsum(padded)[:-1]])
+        first = np.concatenate([[0], np.cumsum(counts)[:-1]])
+        e_loc = flat[order] - j * L
+        rows = start[e_loc] + (np.arange(len(order)) - first[e_loc])
+        expect_g[order] = j * NvS + rows
+        assert np.array_equal(p["cu_seqlens"][j, :E][j * L:(j + 1) * L], np.cumsum(padded))
+    assert np.array_equal(decode(p["dst"]).reshape(-1), expect_g)
+    assert np.all(p["experts_to_copy"] == -1)
+    assert np.all(p["remote_stats"] == 0)
+
+
+# ------------------------------------------------------------- errors
+
+def test_bad_expert_and_hist_mismatch(oracle_mod):
+    sh = wl.SHAPES["tiny"]
+    topk, _ = wl.routing(sh, "zipf", zipf_s=1.2, seed=2)
+    tpe = wl.tokens_per_expert(topk, sh.E)
+    bad = topk.copy()
+    bad[1, 5, 1] = sh.E
+    assert _plan(oracle_mod, _cfg(sh), bad)[0] == oracle_mod.ERR_BAD_EXPERT
+    bad[1, 5, 1] = -1
+    assert _plan(oracle_mod, _cfg(sh), bad)[0] == oracle_mod.ERR_BAD_EXPERT
+    tpe2 = tpe.copy()
+    tpe2[0, 0] += 1
+    assert _plan(oracle_mod, _cfg(sh), topk, tpe2)[0] == oracle_mod.ERR_HIST_MISMATCH
+    assert _plan(oracle_mod, _cfg(sh), topk, tpe)[0] == 0
+
+
+def test_slots_error_when_b_below_group_size(oracle_mod):
+    """B < E/R: a receiver whose run spans two experts needs two slots."""
+    cfg = dict(R=2, E=4, K=1, S=4, B=1, tp=1)
+    # rank 0's group holds all 8 routes, Q_0 = six of e0 then two of e1, so
+    # rank 1 receives Q_0[4,8) = two routes of e0 and two of e1 -> 2 slots > B
+    topk = np.array([[[0], [0], [0], [0]], [[0], [0], [1], [1]]], np.int32)
+    st, _ = _plan(oracle_mod, cfg, topk)
+    assert st == oracle_mod.ERR_SLOTS
+    cfg["B"] = 2
+    st, p = _plan(oracle_mod, cfg, topk)
+    assert st == 0 and list(p["experts_to_copy"][1]) == [0, 1]
+
+
+def test_empty_tokens(oracle_mod):
+    cfg = dict(R=2, E=4, K=2, S=0, B=2, tp=4)
+    st, p = _plan(oracle_mod, cfg, np.zeros((2, 0, 2), np.int32))
+    assert st == 0 and np.all(p["cu_seqlens"] == 0) and np.all(p["experts_to_copy"] == -1)
+
+
+# ---------------------------------------------------------------- bf16
+
+def test_bf16_rounding_matches_torch(oracle_mod):
+    import torch
+    rng = np.random.default_rng(0)
+    vals = [rng.standard_normal(20000).astype(np.float32),
+            (rng.standard_normal(2000) * 1e-39).astype(np.float32),        # subnormals
+            (rng.standard_normal(2000) * 3e38).astype(np.float32),
+            np.array([0.0, -0.0, np.inf, -np.inf, 3.3961e38, -3.3961e38,
+                      np.finfo(np.float32).max, np.finfo(np.float32).tiny], np.float32)]
+    # exact ties: low 16 bits = 0x8000 with odd and even upper halves
+    u = rng.integers(0, 0x7f7f, 4000).astype(np.uint32) << 16 | 0x8000
+    vals.append(u.view(np.float32))
+    u = rng.integers(0, 0xffff, 4000).astype(np.uint32) << 16 | rng.integers(0x7ff0, 0x8010, 4000).astype(np.uint32)
+    u = u[((u >> 23) & 0xff) != 0xff]
+    vals.append(u.view(np.float32))
+    v = np.concatenate(vals)
+    ours = oracle_mod.f32_to_bf16(v)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    nan = oracle_mod.f32_to_bf16(np.array([np.nan], np.float32))[0]
+    assert (nan & 0x7f80) == 0x7f80 and (nan & 0x7f) != 0
+
+
+# ------------------------------------------------ dispatch / combine
+
+def _tiny_case(oracle_mod, seed=0):
+    sh = wl.SHAPES["tiny"]
+    topk, _ = wl.routing(sh, "zipf", zipf_s=1.2, seed=seed)
+    st, p = _plan(oracle_mod, _cfg(sh), topk)
+    assert st == 0
+    x = wl.hidden_bf16(sh, seed)
+    w = wl.route_weights(sh, seed)
+    return sh, topk, p, x, w
+
+
+def test_dispatch_is_a_scatter(oracle_mod):
+    sh, topk, p, x, w = _tiny_case(oracle_mod)
+    NvS, H = p["NvS"], sh.H
+    out = np.full((sh.R * NvS, H), 0x7fc1, np.uint16)   # NaN poison
+    wout = np.full(sh.R * NvS, np.nan, np.float32)
+    oracle_mod.dispatch(sh.R, sh.S, sh.K, sh.E, sh.B, NvS, H, p["dst"], p["zero_fill_ranges"],
+                        x, w, out, wout)
+    g = decode(p["dst"]).reshape(-1)
+    tok = np.repeat(np.arange(sh.R * sh.S), sh.K)
+    assert np.array_equal(out[g], x[tok])
+    assert np.array_equal(wout[g], w.reshape(-1))
+    zfr = p["zero_fill_ranges"]
+    pad = [j * NvS + r for j in range(sh.R) for a, b in zfr[j] for r in range(a, b)]
+    assert np.all(out[pad] == 0) and np.all(wout[pad] == 0) and not np.signbit(wout[pad]).any()
+    # tail rows untouched
+    touched = np.zeros(sh.R * NvS, bool)
+    touched[g] = True
+    touched[pad] = True
+    assert np.all(out[~touched] == 0x7fc1)
+
+
+def test_identity_expert_combine_is_k_times_x(oracle_mod):
+    """With y = the dispatched rows, combine returns K*x exactly (K a power of
+    two: the fp32 sum of K equal bf16 values is exact, and scaling by a power
+    of two keeps a bf16 value representable)."""
+    sh, topk, p, x, w = _tiny_case(oracle_mod, 1)
+    NvS, H = p["NvS"], sh.H
+    y = oracle_mod.dispatch(sh.R, sh.S, sh.K, sh.E, sh.B, NvS, H, p["dst"], p["zero_fill_ranges"], x)
+    out, wout = oracle_mod.combine(sh.R, sh.S, sh.K, NvS, H, p["dst"], y)
+    xf = oracle_mod.bf16_to_f32(x)
+    assert np.array_equal(oracle_mod.bf16_to_f32(out), xf * sh.K)
+
+
+def test_combine_within_one_ulp_of_exact_sum(oracle_mod):
+    sh, topk, p, x, w = _tiny_case(oracle_mod, 2)
+    NvS, H = p["NvS"], sh.H
+    rng = np.random.default_rng(5)
+    y = wl.bf16_bits_from_f32(rng.standard_normal((sh.R * NvS, H)).astype(np.float32))
+    wn = rng.standard_normal(sh.R * NvS).astype(np.float32)
+    out, wout = oracle_mod.combine(sh.R, sh.S, sh.K, NvS, H, p["dst"], y, wn)
+    g = decode(p["dst"]).reshape(sh.R * sh.S, sh.K)
+    yf = oracle_mod.bf16_to_f32(y).astype(np.float64)
+    exact = yf[g].sum(axis=1)
+    got = oracle_mod.bf16_to_f32(out).astype(np.float64)
+    ulp = np.maximum(np.abs(exact), 1e-30)
+    ulp = 2.0 ** (np.floor(np.log2(ulp)) - 7)
+    # fp32 accumulation error is far below one bf16 ulp except near
+    # cancellation; allow one ulp of the result's magnitude plus the fp32 bound
+    bound = ulp + (sh.K - 1) * 2.0 ** -24 * np.abs(yf[g]).sum(axis=1)
+    assert np.all(np.abs(got - exact) <= bound)
+    assert np.array_equal(wout, wn[g])
+
+
+def test_combine_token_subset_and_columns(oracle_mod):
+    sh, topk, p, x, w = _tiny_case(oracle_mod, 3)
+    NvS, H = p["NvS"], sh.H
+    rng = np.random.default_rng(9)
+    y = wl.bf16_bits_from_f32(rng.standard_normal((sh.R * NvS, H)).astype(np.float32))
+    full, _ = oracle_mod.combine(sh.R, sh.S, sh.K, NvS, H, p["dst"], y)
+    toks = np.array([0, 5, 77, 127])
+    part, _ = oracle_mod.combine(sh.R, sh.S, sh.K, NvS, H, p["dst"], y, tokens=toks, c0=16, c1=48)
+    assert np.array_equal(part[:, 16:48], full[toks, 16:48])
+    assert np.all(part[:, :16] == 0)
+
+
+# ------------------------------------------------ prefetch / reduce
+
+def test_prefetch_copies_home_rows(oracle_mod):
+    sh, topk, p, x, w = _tiny_case(oracle_mod, 4)
+    HHp = sh.H * sh.Hp
+    etc = p["experts_to_copy"]
+    rng = np.random.default_rng(1)
+    W = rng.integers(0, 65535, (sh.E + sh.R * sh.B, HHp)).astype(np.uint16)
+    W0 = W.copy()
+    oracle_mod.prefetch(sh.R, sh.E, sh.B, etc, W, HHp)
+    for j in range(sh.R):
+        for b in range(sh.B):
+            row = sh.E + j * sh.B + b
+            src = etc[j, b]
+            assert np.array_equal(W[row], W0[src] if src >= 0 else W0[row])
+    assert np.array_equal(W[:sh.E], W0[:sh.E])
+
+
+def test_reduce_constant_fill_counts_copies(oracle_mod):
+    sh, topk, p, x, w = _tiny_case(oracle_mod, 5)
+    etc = p["experts_to_copy"].reshape(-1)
+    assert (etc >= 0).any()
+    HHp = 64
+    Gh = np.zeros((sh.E, HHp), np.float32)
+    Gs = np.ones((sh.R * sh.B, HHp), np.float32)
+    oracle_mod.reduce(sh.R, sh.E, sh.B, etc, Gh, Gs, HHp)
+    copies = np.bincount(etc[etc >= 0], minlength=sh.E)
+    assert np.array_equal(Gh, np.repeat(copies[:, None].astype(np.float32), HHp, 1))
+    assert np.all(Gs[etc >= 0] == 0) and np.all(Gs[etc < 0] == 1)
+
+
+def test_reduce_random_within_fp32_bound(oracle_mod):
+    cfg = dict(R=4, E=4, K=1, S=10, B=1, tp=4)
+    g = json.load(open(os.path.join(GOLDEN, "plan_chain_donor_turns_receiver.json")))
+    etc = np.array(g["experts_to_copy"], np.int32).reshape(-1)   # e0 in two slots
+    HHp = 257
+    rng = np.random.default_rng(3)
+    Gh = rng.standard_normal((cfg["E"], HHp)).astype(np.float32)
+    Gs = rng.standard_normal((cfg["R"] * cfg["B"], HHp)).astype(np.float32)
+    Gh0, Gs0 = Gh.copy(), Gs.copy()
+    oracle_mod.reduce(cfg["R"], cfg["E"], cfg["B"], etc, Gh, Gs, HHp)
+    for e in range(cfg["E"]):
+        sl = np.nonzero(etc == e)[0]
+        if not len(sl):
+            assert np.array_equal(Gh[e], Gh0[e])
+            continue
+        exact = Gh0[e].astype(np.float64) + Gs0[sl].astype(np.float64).sum(0)
+        mag = np.abs(Gh0[e]).astype(np.float64) + np.abs(Gs0[sl]).astype(np.float64).sum(0)
+        assert np.all(np.abs(Gh[e] - exact) <= len(sl) * 2.0 ** -24 * mag + 1e-45)
+    assert np.all(Gs[etc >= 0] == 0)
+    assert np.array_equal(Gs[etc < 0], Gs0[etc < 0])
+
+
+def test_reduce_integer_values_exact(oracle_mod):
+    """Small integers add exactly in fp32: the result equals numpy's integer sum."""
+    g = json.load(open(os.path.join(GOLDEN, "plan_chain_donor_turns_receiver.json")))
+    etc = np.array(g["experts_to_copy"], np.int32).reshape(-1)
+    rng = np.random.default_rng(4)
+    Gh_i = rng.integers(-1000, 1000, (4, 33))
+    Gs_i = rng.integers(-1000, 1000, (4, 33))
+    Gh, Gs = Gh_i.astype(np.float32), Gs_i.astype(np.float32)
+    oracle_mod.reduce(4, 4, 1, etc, Gh, Gs, 33)
+    want = Gh_i.copy()
+    for i, e in enumerate(etc):
+        if e >= 0:
+            want[e] += Gs_i[i]
+    assert np.array_equal(Gh, want.astype(np.float32))
+
+
+def test_maxvio_closed_form():
+    sh = wl.SHAPES["deepseek_v3"]
+    sh = wl.Shape("d", R=sh.R, E=sh.E, K=sh.K, S=128, H=8, Hp=8, B=sh.B, tp=sh.tp, weights="sigmoid")
+    topk, info = wl.routing(sh, "zipf", target_maxvio=2.0, seed=1)
+    T = np.bincount(topk.reshape(-1), minlength=sh.E)
+    assert abs(info["maxvio"] - (T.max() / (sh.N / sh.E) - 1)) < 1e-12
+    assert abs(info["maxvio"] - 2.0) <= 0.02
