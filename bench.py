@@ -1,0 +1,583 @@
+#!/usr/bin/env python
+"""Benchmark of the balanced expert-parallel hot path on one GB300 per process.
+
+One step = one pass of every hot-path row over one batch of synthetic input:
+plan -> dispatch (hidden + route weights) -> weight prefetch -> combine (the
+dispatched rows stand in for the expert outputs) -> plan-reuse dispatch of an
+[R, S, H] gradient -> redundant-expert gradient reduce (one projection).
+Tokens per step = R*S.  Prints one JSON line.
+
+  python bench.py [--gpus N --steps K --warmup W] [--config mixtral]
+                  [--maxvio 1.0] [--impl ours|reference]
+
+With N > 1 (torchrun), every process runs the same workload on its own GPU
+(the R emulated ranks are independent batches: weak scaling, no data-path
+collective); a gloo group carries only the barrier and the max of the timings.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "plan+dispatch+combine tokens/s and effective HBM GB/s vs ~8 TB/s, per maxvio"
+SWEEPS = {"tiny": [1.0], "mixtral": [0.0, 0.5, 1.0, 2.0, 3.0],
+          "deepseek_v3": [0.0, 1.0, 2.0, 4.0], "kimi_k2": ["hot30", "hot9"],
+          "qwen3_decode": ["uniform", "zipf1"]}
+HEADLINE = {"tiny": 1.0, "mixtral": 1.0, "deepseek_v3": 1.0, "kimi_k2": "hot30",
+            "qwen3_decode": "zipf1"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="mixtral")
+    ap.add_argument("--maxvio", default=None, help="headline routing point")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--profile-op", default=None,
+                    help="comma list of ops (plan,dispatch,combine,prefetch,reduce): "
+                         "allocate only what they need and run each --steps times "
+                         "(a small, self-contained case for profilers; prints timings)")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- routing
+
+def make_routing(sh, point, seed):
+    from combine_moonep_plan_gb300 import workloads as wl
+    if point == "hot30":
+        return wl.routing(sh, "hot", hot_share=0.30, seed=seed)
+    if point == "hot9":
+        return wl.routing(sh, "hot", hot_share=0.09375, seed=seed)
+    if point == "uniform":
+        return wl.routing(sh, "uniform", seed=seed)
+    if point == "zipf1":
+        return wl.routing(sh, "zipf", zipf_s=1.0, seed=seed)
+    mv = float(point)
+    if mv == 0.0 and (sh.N % sh.E == 0):
+        return wl.routing(sh, "exact0", seed=seed)
+    return wl.routing(sh, "zipf", target_maxvio=mv, seed=seed)
+
+
+def point_label(p):
+    return p if isinstance(p, str) else float(p)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, with host times."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        used = inside
+        if not used and self.samples:
+            # timed region shorter than the sampling period: nearest samples
+            used = [min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[1]]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        sm = [num(p[0]) for p in used if num(p[0]) is not None]
+        mx = [num(p[1]) for p in used if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in used for n, v in zip(names, p[4:8]) if v == "Active"})
+        pw = [num(p[2]) for p in used if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(inside)}
+
+
+# ------------------------------------------------------------- our arm
+
+class Step:
+    """Device-resident inputs and outputs of one hot-path step."""
+
+    def __init__(self, buf, sh, topk_np, seed, torch):
+        from combine_moonep_plan_gb300 import workloads as wl
+        dev = "cuda"
+        R, S, K, E, H, Hp, B = sh.R, sh.S, sh.K, sh.E, sh.H, sh.Hp, sh.B
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.sh = sh
+        self.buf = buf
+        self.topk = torch.from_numpy(topk_np).to(dev)
+        self.tpe = torch.from_numpy(wl.tokens_per_expert(topk_np, E)).to(dev)
+        self.hidden = torch.randn((R, S, H), generator=g, device=dev).to(torch.bfloat16)
+        self.w_sk = torch.from_numpy(wl.route_weights(sh, seed)).to(dev)
+        self.grad = torch.randn((R, S, H), generator=g, device=dev).to(torch.bfloat16)
+        NvS = buf.NvS
+        self.hid_nvsh = torch.empty((R * NvS, H), dtype=torch.bfloat16, device=dev)
+        self.w_nvs = torch.empty((R * NvS,), dtype=torch.float32, device=dev)
+        self.grad_nvsh = torch.empty((R * NvS, H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((R, S, H), dtype=torch.bfloat16, device=dev)
+        self.w_back = torch.empty((R, S, K), dtype=torch.float32, device=dev)
+        self.W = torch.randn((E + R * B, H, Hp), generator=g, device=dev).to(torch.bfloat16)
+        self.Gh = torch.randn((E, H, Hp), generator=g, device=dev)
+        self.Gs = torch.randn((R, B, H, Hp), generator=g, device=dev)
+        self.plan = buf.new_plan()
+
+    def run(self, events=None):
+        b = self.buf
+        rec = (lambda i: events[i].record()) if events else (lambda i: None)
+        rec(0)
+        b.plan(self.topk, self.tpe, plan=self.plan)
+        rec(1)
+        b.dispatch(self.hidden, self.w_sk, plan=self.plan, out=self.hid_nvsh,
+                   weights_out=self.w_nvs)
+        rec(2)
+        b.prefetch_weight(self.plan, self.W)
+        rec(3)
+        b.combine(self.plan, self.hid_nvsh, self.w_nvs, out=self.out, weights_out=self.w_back)
+        rec(4)
+        b.dispatch(self.grad, plan=self.plan, out=self.grad_nvsh)
+        rec(5)
+        b.reduce_grad(self.plan, [self.Gh], [self.Gs])
+        rec(6)
+
+    LAUNCHES_PER_STEP = 8  # plan: 3 kernels; dispatch, prefetch, combine, dispatch, reduce
+
+    def algorithmic_bytes(self):
+        """Bytes each op must move (reads + writes), per launch."""
+        sh = self.sh
+        R, S, K, E, H, B, Hp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.Hp
+        N = R * S * K
+        p = self.plan
+        zfr = p.zero_fill_ranges.cpu().numpy().astype(np.int64)
+        P = int((zfr[..., 1] - zfr[..., 0]).sum())
+        etc = p.experts_to_copy.cpu().numpy()
+        U = int((etc >= 0).sum())
+        D = len(np.unique(etc[etc >= 0]))
+        HHp = H * Hp
+        return {
+            "plan": N * 4 + R * E * 4 + N * 4 + R * (E + B) * 16,
+            "dispatch": R * S * H * 2 + N * 8 + (N + P) * (H * 2 + 4),
+            "prefetch": 2 * U * HHp * 2,
+            "combine": N * H * 2 + N * 8 + R * S * H * 2 + N * 4,
+            "grad_dispatch": R * S * H * 2 + N * 4 + (N + P) * H * 2,
+            "reduce": (2 * D + 2 * U) * HHp * 4,
+        }, {"P": P, "U": U, "D": D}
+
+
+OPS = ["plan", "dispatch", "prefetch", "combine", "grad_dispatch", "reduce"]
+
+
+def timed_steps(step, steps, torch, dist=None):
+    """Run `steps` steps with per-op events; returns (total_ms, per-op ms list)."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record()
+    for i in range(steps):
+        step.run(evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    total = start.elapsed_time(end)
+    per_op = {op: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)]
+              for j, op in enumerate(OPS)}
+    return total, per_op, (t0, t1)
+
+
+def max_over_ranks(x, dist):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
+    """Same step through the public API, inputs from pinned host memory and
+    the combined result read back, copies inside the timed region."""
+    from combine_moonep_plan_gb300 import workloads as wl
+    R, S, K, E, H = sh.R, sh.S, sh.K, sh.E, sh.H
+    pin = dict(pin_memory=True)
+    h_topk = torch.from_numpy(topk_np).pin_memory()
+    h_tpe = torch.from_numpy(wl.tokens_per_expert(topk_np, E)).pin_memory()
+    g = torch.Generator().manual_seed(seed)
+    h_hidden = torch.randn((R, S, H), generator=g).to(torch.bfloat16).pin_memory()
+    h_w = torch.from_numpy(wl.route_weights(sh, seed)).pin_memory()
+    h_grad = torch.randn((R, S, H), generator=g).to(torch.bfloat16).pin_memory()
+    h_out = torch.empty((R, S, H), dtype=torch.bfloat16, **pin)
+    h_wout = torch.empty((R, S, K), dtype=torch.float32, **pin)
+    st = Step(buf, sh, topk_np, seed, torch)
+    bi = sum(t.numel() * t.element_size() for t in (h_topk, h_tpe, h_hidden, h_w, h_grad))
+    bo = h_out.numel() * h_out.element_size() + h_wout.numel() * h_wout.element_size()
+
+    def one():
+        st.topk.copy_(h_topk, non_blocking=True)
+        st.tpe.copy_(h_tpe, non_blocking=True)
+        st.hidden.copy_(h_hidden, non_blocking=True)
+        st.w_sk.copy_(h_w, non_blocking=True)
+        st.grad.copy_(h_grad, non_blocking=True)
+        st.run()
+        h_out.copy_(st.out, non_blocking=True)
+        h_wout.copy_(st.w_back, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    start.record()
+    for _ in range(steps):
+        one()
+    end.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end), dist)
+    del st
+    return ms / steps, bi, bo
+
+
+def cpu_baseline(sh, topk_np, seed, cols=None, hh_cols=None, repeats=1):
+    """The oracle, single-threaded on the host, over all tokens and a column
+    sample of every row; times scaled to full rows."""
+    import oracle
+    from combine_moonep_plan_gb300 import workloads as wl
+    R, S, K, E, H, B, Hp, tp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.Hp, sh.tp
+    Hs = min(H, cols or 256)
+    HHp = H * Hp
+    HHs = min(HHp, hh_cols or (1 << 16))
+    x = wl.hidden_bf16(sh, seed, rows=R * S, cols=Hs)
+    w = wl.route_weights(sh, seed)
+    gr = wl.hidden_bf16(sh, seed + 1, rows=R * S, cols=Hs)
+    tpe = wl.tokens_per_expert(topk_np, E)
+    rng = np.random.default_rng(seed)
+    W = rng.integers(0, 65535, (E + R * B, HHs), dtype=np.uint16)
+    Gh = rng.standard_normal((E, HHs), dtype=np.float32)
+    Gs = rng.standard_normal((R * B, HHs), dtype=np.float32)
+    t = {op: 0.0 for op in OPS}
+    for _ in range(repeats):
+        a = time.perf_counter()
+        st, p = oracle.plan(R, E, K, S, B, tp, topk_np, tpe, dup_records=False)
+        b = time.perf_counter()
+        NvS = p["NvS"]
+        hid = np.zeros((R * NvS, Hs), np.uint16)
+        wn = np.zeros(R * NvS, np.float32)
+        oracle.dispatch(R, S, K, E, B, NvS, Hs, p["dst"], p["zero_fill_ranges"], x, w, hid, wn)
+        c = time.perf_counter()
+        oracle.prefetch(R, E, B, p["experts_to_copy"], W, HHs)
+        d = time.perf_counter()
+        oracle.combine(R, S, K, NvS, Hs, p["dst"], hid, wn)
+        e = time.perf_counter()
+        gh = np.zeros((R * NvS, Hs), np.uint16)
+        oracle.dispatch(R, S, K, E, B, NvS, Hs, p["dst"], p["zero_fill_ranges"], gr, None, gh)
+        f = time.perf_counter()
+        oracle.reduce(R, E, B, p["experts_to_copy"], Gh, Gs, HHs)
+        g = time.perf_counter()
+        t["plan"] += b - a
+        t["dispatch"] += (c - b) * H / Hs
+        t["prefetch"] += (d - c) * HHp / HHs
+        t["combine"] += (e - d) * H / Hs
+        t["grad_dispatch"] += (f - e) * H / Hs
+        t["reduce"] += (g - f) * HHp / HHs
+    for op in t:
+        t[op] /= repeats
+    step_s = sum(t.values())
+    sample = (f"all {R * S} tokens and the full plan; hidden columns [0,{Hs}) of {H}; "
+              f"weight/grad columns [0,{HHs}) of {HHp}; times scaled to full rows")
+    return R * S / step_s, step_s, t, sample
+
+
+def reference_arm(args, sh, point, topk_np, seed, dist):
+    """The oracle as the reference arm: each step a column sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    steps, warm = args.steps, args.warmup
+    # size the per-step column sample so the whole run stays near 3 minutes
+    cols, hh = 64, 1 << 16
+    a = time.perf_counter()
+    cpu_baseline(sh, topk_np, seed, cols, hh)
+    est = (time.perf_counter() - a) * (steps + warm)
+    if est > 180.0:
+        scale = max(180.0 / est, 1.0 / 8)
+        cols, hh = max(8, int(cols * scale)), max(1 << 12, int(hh * scale))
+    for _ in range(warm):
+        cpu_baseline(sh, topk_np, seed, cols, hh)
+    a = time.perf_counter()
+    tot = 0.0
+    for _ in range(steps):
+        v, step_s, per, sample = cpu_baseline(sh, topk_np, seed, cols, hh)
+        tot += step_s
+    wall = time.perf_counter() - a
+    value = R_S(sh) * steps / tot
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * tot / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "impl": "reference",
+            "config": workload_config(sh, point),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample, "wall_s": wall},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def R_S(sh):
+    return sh.R * sh.S
+
+
+def workload_config(sh, point):
+    return {"workload": f"{sh.name}-shaped: R={sh.R} E={sh.E} K={sh.K} S={sh.S} H={sh.H} "
+                        f"H'={sh.Hp} B={sh.B} token_padding={sh.tp}, routing maxvio point "
+                        f"{point_label(point)}",
+            "R": sh.R, "E": sh.E, "K": sh.K, "S": sh.S, "H": sh.H, "H_prime": sh.Hp, "B": sh.B,
+            "token_padding": sh.tp, "maxvio_point": point_label(point), "n_proj": 1,
+            "step": "plan -> dispatch(+weights) -> prefetch -> combine(+weights) -> "
+                    "plan-reuse grad dispatch -> grad reduce",
+            "l2": "inputs larger than L2 (no flush): every step moves several GB",
+            "dup_records": False, "global_batch": sh.R * sh.S}
+
+
+def profile_ops(args, sh, point, seed):
+    """Run only the named ops with minimal allocations (profiling case)."""
+    import torch
+    from combine_moonep_plan_gb300 import workloads as wl
+    from combine_moonep_plan_gb300.api import Buffer
+    from combine_moonep_plan_gb300.build import build
+    build()
+    ops = args.profile_op.split(",")
+    R, S, K, E, H, B, Hp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.Hp
+    topk_np, info = make_routing(sh, point, seed)
+    buf = Buffer(S=S, H=H, K=K, E=E, num_ep_ranks=R, B=B, token_padding=sh.tp,
+                 zero_copy_views=False)
+    dev = "cuda"
+    topk = torch.from_numpy(topk_np).to(dev)
+    plan = buf.plan(topk)
+    x = torch.randn((R, S, H), device=dev).to(torch.bfloat16)
+    w = torch.from_numpy(wl.route_weights(sh, seed)).to(dev)
+    y = torch.empty((R * buf.NvS, H), dtype=torch.bfloat16, device=dev)
+    wn = torch.empty((R * buf.NvS,), dtype=torch.float32, device=dev)
+    buf.dispatch(x, w, plan=plan, out=y, weights_out=wn)
+    W = Gh = Gs = None
+    if "prefetch" in ops:
+        W = torch.randn((E + R * B, H, Hp), device=dev).to(torch.bfloat16)
+    if "reduce" in ops:
+        Gh = torch.randn((E, H, Hp), device=dev)
+        Gs = torch.randn((R, B, H, Hp), device=dev)
+    out = torch.empty((R, S, H), dtype=torch.bfloat16, device=dev)
+    wb = torch.empty((R, S, K), dtype=torch.float32, device=dev)
+    run = {"plan": lambda: buf.plan(topk, plan=plan),
+           "dispatch": lambda: buf.dispatch(x, w, plan=plan, out=y, weights_out=wn),
+           "combine": lambda: buf.combine(plan, y, wn, out=out, weights_out=wb),
+           "prefetch": lambda: buf.prefetch_weight(plan, W),
+           "reduce": lambda: buf.reduce_grad(plan, [Gh], [Gs])}
+    res = {}
+    for op in ops:
+        for _ in range(2):
+            run[op]()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            run[op]()
+        b.record()
+        torch.cuda.synchronize()
+        res[op] = a.elapsed_time(b) / args.steps
+    print(json.dumps({"profile_case": sh.name, "maxvio": info["maxvio"], "ms": res,
+                      "status": buf.get_status()}), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from combine_moonep_plan_gb300 import workloads as wl
+    sh = wl.SHAPES[args.config]
+    point = args.maxvio if args.maxvio is not None else HEADLINE[args.config]
+    try:
+        point = float(point)
+    except (TypeError, ValueError):
+        pass
+    seed = wl.seed_for(sh.name, 0)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("gloo")
+        dist = dist_mod
+
+    if args.profile_op:
+        profile_ops(args, sh, point, seed)
+        return
+
+    if args.impl == "reference":
+        topk_np, _ = make_routing(sh, point, seed)
+        line = reference_arm(args, sh, point, topk_np, seed, dist)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    from combine_moonep_plan_gb300.build import build
+    build()
+    from combine_moonep_plan_gb300.api import Buffer
+
+    topk_np, rinfo = make_routing(sh, point, seed)
+    buf = Buffer(S=sh.S, H=sh.H, K=sh.K, E=sh.E, num_ep_ranks=sh.R, B=sh.B,
+                 token_padding=sh.tp, zero_copy_views=False)
+    step = Step(buf, sh, topk_np, seed, torch)
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+    status = buf.get_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} during warm-up")
+
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    total_ms, per_op, (t0, t1) = timed_steps(step, args.steps, torch, dist)
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    total_ms = max_over_ranks(total_ms, dist)
+    ms_per_step = total_ms / args.steps
+    alg, counts = step.algorithmic_bytes()
+    op_ms = {op: statistics.mean(v) for op, v in per_op.items()}
+    tokens = R_S(sh) * world
+    value = tokens / (ms_per_step / 1e3)
+    pdc_ms = op_ms["plan"] + op_ms["dispatch"] + op_ms["combine"]
+
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) if os.path.exists(
+            os.path.join(ROOT, "MEASURED_PEAKS.json")) else open(os.devnull) as f:
+        try:
+            peaks = json.load(f)
+        except Exception:
+            peaks = {}
+    peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    dom = max((o for o in OPS if o != "plan"), key=lambda o: op_ms[o])
+    achieved = alg[dom] / (op_ms[dom] / 1e3) / 1e9
+    ops = {o: {"ms": round(op_ms[o], 5), "GB": round(alg[o] / 1e9, 4),
+               "GBps": round(alg[o] / (op_ms[o] / 1e3) / 1e9, 1) if op_ms[o] > 0 else None,
+               "frac_of_peak": round(alg[o] / (op_ms[o] / 1e3) / 1e9 / peak, 4)
+               if op_ms[o] > 0 else None} for o in OPS}
+    step_bytes = sum(alg.values())
+
+    sweep = []
+    if not args.no_sweep:
+        for p in SWEEPS[args.config]:
+            tk, info = make_routing(sh, p, seed + 1 + len(sweep))
+            s2 = Step(buf, sh, tk, seed, torch)
+            for _ in range(3):
+                s2.run()
+            tot2, po2, _ = timed_steps(s2, args.sweep_steps, torch, None)
+            a2, c2 = s2.algorithmic_bytes()
+            m2 = {o: statistics.mean(v) for o, v in po2.items()}
+            pdc2 = m2["plan"] + m2["dispatch"] + m2["combine"]
+            sweep.append({
+                "maxvio_point": point_label(p), "maxvio": round(info["maxvio"], 4),
+                "step_tokens_per_s": R_S(sh) / (tot2 / args.sweep_steps / 1e3),
+                "plan_dispatch_combine_tokens_per_s": R_S(sh) / (pdc2 / 1e3),
+                "plan_us": round(1e3 * m2["plan"], 2),
+                "dispatch_GBps": round(a2["dispatch"] / (m2["dispatch"] / 1e3) / 1e9, 1),
+                "combine_GBps": round(a2["combine"] / (m2["combine"] / 1e3) / 1e9, 1),
+                "plan_frac_of_dispatch": round(m2["plan"] / m2["dispatch"], 4),
+                "padding_rows": c2["P"], "slots_used": c2["U"]})
+            del s2
+        torch.cuda.synchronize()
+
+    e2e = None
+    if not args.no_e2e:
+        ms_e2e, bi, bo = run_e2e(buf, sh, topk_np, seed, args.e2e_steps, torch, dist)
+        e2e = {"value": tokens / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": args.e2e_steps}
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        v, step_s, per, sample = cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+               "step_s": step_s}
+
+    status = buf.get_status()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(sh, point),
+        "routing": {k: v for k, v in rinfo.items() if k != "hot"},
+        "plan_dispatch_combine_tokens_per_s": R_S(sh) * world / (pdc_ms / 1e3),
+        "plan_frac_of_dispatch": op_ms["plan"] / op_ms["dispatch"],
+        "step_hbm_GBps": step_bytes / (ms_per_step / 1e3) / 1e9,
+        "ops": ops, "plan_counts": counts,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": peak_src, "traffic": None},
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks, "sweep": sweep, "device_status": status,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

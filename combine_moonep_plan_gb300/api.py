@@ -1,0 +1,296 @@
+"""PyTorch-facing wrapper over the C ABI, shaped like the MoonEP Python API.
+
+"MoonEP Public API Visual Guide": Buffer(...), Buffer.dispatch(...),
+Buffer.prefetch_weight(...), Buffer.combine(...), Buffer.reduce_grad(...),
+the two buffer views, Buffer.destroy() and MoonEPCommPlan.clone().
+
+The R expert-parallel ranks live on one GPU, so every tensor carries a
+leading rank axis: hidden_sh is [R, S, H], topk [R, S, K], and dispatched rows
+are [R*NvS, H] (rank j's window starts at row j*NvS).  Everything is issued on
+torch's current CUDA stream; PyTorch provides memory and streams only, and
+every step runs in libmoonep's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import MoonepCommPlan, MoonepConfig, check
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+class _DeviceArray:
+    """Zero-copy, non-owning view of library-owned device memory."""
+
+    def __init__(self, ptr: int, shape, typestr: str, owner):
+        self._owner = owner
+        self.__cuda_array_interface__ = {
+            "shape": tuple(int(s) for s in shape), "typestr": typestr,
+            "data": (int(ptr), False), "version": 3, "strides": None, "stream": None}
+
+
+def _view(ptr, shape, owner, dtype=torch.int32):
+    typestr = {torch.int32: "<i4", torch.float32: "<f4", torch.bfloat16: "<u2"}[dtype]
+    n = 1
+    for s in shape:
+        n *= int(s)
+    if not ptr or n == 0:
+        return torch.empty(shape, dtype=dtype, device="cuda")
+    t = torch.as_tensor(_DeviceArray(ptr, shape, typestr, owner), device="cuda")
+    if dtype == torch.bfloat16:
+        t = t.view(torch.bfloat16)
+    return t
+
+
+def _check_tensor(t, name, dtype, shape):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+class CommPlan:
+    """A communication plan [MoonEPCommPlan]: device arrays owned by libmoonep."""
+
+    def __init__(self, buffer: "Buffer", flags: int = 0):
+        self._buffer = buffer
+        self._st = MoonepCommPlan()
+        check(_lib.load().moonep_plan_create(buffer._ctx, flags, ctypes.byref(self._st)),
+              "moonep_plan_create")
+        st = self._st
+        R, E, B, K, S, NvS = st.R, st.E, st.B, st.K, st.S, st.NvS
+        self.R, self.E, self.B, self.K, self.S, self.NvS, self.N = R, E, B, K, S, NvS, st.N
+        self.flags = flags
+        self.dst = _view(st.dst, (R, S * K), self)
+        self.experts_to_copy = _view(st.experts_to_copy, (R, B), self)
+        self.cu_seqlens = _view(st.cu_seqlens, (R, E + B), self)
+        self.zero_fill_ranges = _view(st.zero_fill_ranges, (R, E + B, 2), self)
+        self.remote_stats = _view(st.remote_stats, (R, 2), self)
+        self.dup_counts = _view(st.dup_counts, (R, 2), self)
+        if flags & _lib.PLAN_DUP_RECORDS:
+            self.dup_groups = _view(st.dup_groups, (R, NvS, 3), self)
+            self.dup_loffs = _view(st.dup_loffs, (R, NvS), self)
+        else:
+            self.dup_groups = self.dup_loffs = None
+
+    @property
+    def struct(self):
+        return ctypes.byref(self._st)
+
+    def clone(self) -> "CommPlan":
+        """Deep copy of every array and scalar [MoonEPCommPlan.clone()]."""
+        other = CommPlan(self._buffer, self.flags)
+        check(_lib.load().moonep_plan_clone(self.struct, other.struct, _stream()),
+              "moonep_plan_clone")
+        return other
+
+    def destroy(self):
+        if getattr(self, "_st", None) is not None and self._st.internal:
+            _lib.load().moonep_plan_destroy(ctypes.byref(self._st))
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+class Buffer:
+    """Persistent resources of the balanced EP hot path [Buffer(...)].
+
+    S tokens per rank, H hidden, K routes per token, E experts, R ranks
+    (num_ep_ranks), B prefetch slots per rank (default E // R), token_padding
+    rows of alignment per non-empty segment, num_sms SM cap (None: all)."""
+
+    def __init__(self, S: int, H: int, K: int, E: int, num_ep_ranks: int, B: int | None = None,
+                 token_padding: int = 128, num_sms: int | None = None,
+                 zero_copy_views: bool = True, dup_records: bool = False):
+        lib = _lib.load()
+        R = num_ep_ranks
+        B = E // R if B is None else B
+        self.cfg = MoonepConfig(R=R, E=E, K=K, S=S, H=H, B=B, token_padding=token_padding,
+                                num_sms=0 if num_sms is None else num_sms)
+        self.R, self.E, self.K, self.S, self.H, self.B = R, E, K, S, H, B
+        self.token_padding = token_padding
+        nvs, nvsp = ctypes.c_int(), ctypes.c_int()
+        check(lib.moonep_query_sizes(ctypes.byref(self.cfg), ctypes.byref(nvs),
+                                     ctypes.byref(nvsp), None), "moonep_query_sizes")
+        self.NvS, self.NvS_padded = nvs.value, nvsp.value
+        torch.cuda.current_device()  # make sure the primary context exists
+        h = ctypes.c_void_p()
+        check(lib.moonep_ctx_create(ctypes.byref(self.cfg), int(zero_copy_views),
+                                    ctypes.byref(h)), "moonep_ctx_create")
+        self._ctx = h
+        self._plan_flags = _lib.PLAN_DUP_RECORDS if dup_records else 0
+        self._views = zero_copy_views
+
+    # ----------------------------------------------------------- lifecycle
+    @property
+    def destroyed(self) -> bool:
+        return self._ctx is None or bool(_lib.load().moonep_ctx_destroyed(self._ctx))
+
+    def destroy(self) -> None:
+        """Synchronise and release everything [Buffer.destroy()]; idempotent."""
+        if self._ctx is not None:
+            _lib.load().moonep_ctx_destroy(self._ctx)
+
+    def __del__(self):
+        try:
+            if self._ctx is not None:
+                _lib.load().moonep_ctx_free(self._ctx)
+                self._ctx = None
+        except Exception:
+            pass
+
+    @property
+    def num_sms(self) -> int:
+        return _lib.load().moonep_num_sms(self._ctx)
+
+    # ------------------------------------------------------------- views
+    def hidden_nvsh_buffer_view(self, rank: int | None = None) -> torch.Tensor:
+        """Writable [NvS, H] bf16 window of rank `rank` (all ranks, [R*NvS, H],
+        when rank is None) of the persistent hidden buffer."""
+        lib = _lib.load()
+        if rank is None:
+            p = lib.moonep_hidden_view(self._ctx, 0)
+            return _view(p, (self.R * self.NvS, self.H), self, torch.bfloat16)
+        return _view(lib.moonep_hidden_view(self._ctx, rank), (self.NvS, self.H), self,
+                     torch.bfloat16)
+
+    def router_weight_buffer_view(self, rank: int | None = None) -> torch.Tensor:
+        lib = _lib.load()
+        if rank is None:
+            return _view(lib.moonep_weight_view(self._ctx, 0), (self.R * self.NvS,), self,
+                         torch.float32)
+        return _view(lib.moonep_weight_view(self._ctx, rank), (self.NvS,), self, torch.float32)
+
+    # -------------------------------------------------------------- plan
+    def new_plan(self) -> CommPlan:
+        return CommPlan(self, self._plan_flags)
+
+    def plan(self, topk_experts_sk: torch.Tensor, tokens_per_expert: torch.Tensor | None = None,
+             plan: CommPlan | None = None) -> CommPlan:
+        """Run the online planner into `plan` (a new plan when None)."""
+        R, S, K, E = self.R, self.S, self.K, self.E
+        tk = _check_tensor(topk_experts_sk, "topk_experts_sk", torch.int32, (R, S, K))
+        tp = None
+        if tokens_per_expert is not None:
+            tp = _check_tensor(tokens_per_expert, "tokens_per_expert", torch.int32, (R, E))
+        plan = self.new_plan() if plan is None else plan
+        check(_lib.load().moonep_plan(self._ctx, tk, tp, plan.struct, _stream()), "moonep_plan")
+        return plan
+
+    # ---------------------------------------------------------- dispatch
+    def dispatch(self, hidden_sh: torch.Tensor, route_weights_sk: torch.Tensor | None = None,
+                 topk_experts_sk: torch.Tensor | None = None,
+                 tokens_per_expert: torch.Tensor | None = None, plan: CommPlan | None = None,
+                 zero_copy: bool = False, router_weights_zero_copy: bool = False,
+                 out: torch.Tensor | None = None, weights_out: torch.Tensor | None = None):
+        """Fresh dispatch (plan is None) or plan-reuse dispatch [Buffer.dispatch].
+
+        Returns (hidden_nvsh [R*NvS, H] bf16, route_weights_nvs [R*NvS] fp32 or
+        None, cu_seqlens [R, E+B] int32 (None on plan reuse), plan)."""
+        R, S, H, K, NvS = self.R, self.S, self.H, self.K, self.NvS
+        hp = _check_tensor(hidden_sh, "hidden_sh", torch.bfloat16, (R, S, H))
+        fresh = plan is None
+        if fresh:
+            if topk_experts_sk is None:
+                raise ValueError("a fresh dispatch needs topk_experts_sk")
+            plan = self.plan(topk_experts_sk, tokens_per_expert)
+        if out is None:
+            out = self.hidden_nvsh_buffer_view() if zero_copy else torch.empty(
+                (R * NvS, H), dtype=torch.bfloat16, device=hidden_sh.device)
+        op = _check_tensor(out, "hidden_nvsh", torch.bfloat16, (R * NvS, H))
+        wp = wop = None
+        w_out = None
+        if route_weights_sk is not None:
+            wp = _check_tensor(route_weights_sk, "route_weights_sk", torch.float32, (R, S, K))
+            if weights_out is None:
+                weights_out = self.router_weight_buffer_view() if router_weights_zero_copy \
+                    else torch.empty((R * NvS,), dtype=torch.float32, device=hidden_sh.device)
+            wop = _check_tensor(weights_out, "route_weights_nvs", torch.float32, (R * NvS,))
+            w_out = weights_out
+        check(_lib.load().moonep_dispatch(self._ctx, plan.struct, hp, wp, op, wop, _stream()),
+              "moonep_dispatch")
+        return out, w_out, (plan.cu_seqlens if fresh else None), plan
+
+    # ----------------------------------------------------------- combine
+    def combine(self, plan: CommPlan, hidden_nvsh: torch.Tensor,
+                route_weights_nvs: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                weights_out: torch.Tensor | None = None):
+        """Gather and K-sum back to token-major [Buffer.combine].
+        Returns (hidden_sh [R, S, H] bf16, route_weights_sk [R, S, K] or None)."""
+        R, S, H, K, NvS = self.R, self.S, self.H, self.K, self.NvS
+        yp = _check_tensor(hidden_nvsh, "hidden_nvsh", torch.bfloat16, (R * NvS, H))
+        if out is None:
+            out = torch.empty((R, S, H), dtype=torch.bfloat16, device=hidden_nvsh.device)
+        op = _check_tensor(out, "hidden_sh", torch.bfloat16, (R, S, H))
+        wp = wop = None
+        if route_weights_nvs is not None:
+            wp = _check_tensor(route_weights_nvs, "route_weights_nvs", torch.float32, (R * NvS,))
+            if weights_out is None:
+                weights_out = torch.empty((R, S, K), dtype=torch.float32,
+                                          device=hidden_nvsh.device)
+            wop = _check_tensor(weights_out, "route_weights_sk", torch.float32, (R, S, K))
+        else:
+            weights_out = None
+        check(_lib.load().moonep_combine(self._ctx, plan.struct, yp, wp, op, wop, _stream()),
+              "moonep_combine")
+        return out, weights_out
+
+    # --------------------------------------------------- weights / grads
+    def prefetch_weight(self, plan: CommPlan, *weights: torch.Tensor) -> None:
+        """Fill the prefetch slots of every [E + R*B, H, H'] bf16 tensor given
+        (gate, up, down, ...; at most 4) [Buffer.prefetch_weight]."""
+        if not weights or len(weights) > 4:
+            raise ValueError("prefetch_weight takes 1 to 4 weight tensors")
+        rows = self.E + self.R * self.B
+        HHp = None
+        ptrs = []
+        for i, w in enumerate(weights):
+            hh = w[0].numel() if w.dim() > 1 else 0
+            HHp = hh if HHp is None else HHp
+            if hh != HHp:
+                raise ValueError("all weight tensors must share H*H'")
+            ptrs.append(_check_tensor(w, f"weight[{i}]", torch.bfloat16, (rows, *w.shape[1:])))
+        check(_lib.load().moonep_prefetch_weight(self._ctx, plan.struct, len(ptrs),
+                                                  _lib.ptr_array(ptrs), HHp, _stream()),
+              "moonep_prefetch_weight")
+
+    def reduce_grad(self, plan: CommPlan, grads, reduce_buffers) -> None:
+        """Add the slot gradients into their home experts and clear the used
+        slots [Buffer.reduce_grad].  grads: [E, H, H'] fp32 tensors;
+        reduce_buffers: matching [R, B, H, H'] fp32 tensors."""
+        grads, reduce_buffers = list(grads), list(reduce_buffers)
+        if not grads or len(grads) != len(reduce_buffers) or len(grads) > 4:
+            raise ValueError("reduce_grad takes 1 to 4 (grad, reduce_buffer) pairs")
+        HHp = grads[0][0].numel()
+        gp, sp = [], []
+        for i, (g, s) in enumerate(zip(grads, reduce_buffers)):
+            gp.append(_check_tensor(g, f"grad[{i}]", torch.float32, (self.E, *g.shape[1:])))
+            sp.append(_check_tensor(s, f"reduce_buffer[{i}]", torch.float32,
+                                    (self.R, self.B, *g.shape[1:])))
+            if g[0].numel() != HHp:
+                raise ValueError("all gradients must share H*H'")
+        check(_lib.load().moonep_reduce_redundant_grad(
+            self._ctx, plan.struct, len(gp), _lib.ptr_array(gp), _lib.ptr_array(sp), HHp,
+            _stream()), "moonep_reduce_redundant_grad")
+
+    # ------------------------------------------------------------ status
+    def get_status(self) -> int:
+        """Synchronise the current stream and return (and clear) the first
+        error a kernel latched since the last call (0 when none)."""
+        v = ctypes.c_int()
+        check(_lib.load().moonep_get_status(self._ctx, ctypes.byref(v), _stream()),
+              "moonep_get_status")
+        return v.value

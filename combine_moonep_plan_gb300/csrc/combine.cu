@@ -1,0 +1,171 @@
+// Combine: the reverse data movement of dispatch.
+//
+// "MoonEP Public API Visual Guide", Buffer.combine(...): follow plan.dst, read
+// the valid rows and perform the top-k reduction of every original token;
+// routing weights are gathered back through the same positive/negative
+// encoding.  The vLLM integration's finalize() fixes the reduction as an
+// unweighted K-sum (weights are applied inside the expert compute).
+//
+// out[t, :] = bf16_rne( y[|dst(t,0)|,:] + y[|dst(t,1)|,:] + ... ) with the adds
+// in fp32 in k order.  The page's version first folds duplicate rows into
+// their primaries (to save link bytes between GPUs); on one GPU every row is
+// read directly, so there is a single rounding at the end.
+// Units of (token, chunk of 32*U 16-byte vectors) are strided over the warps
+// of a persistent grid; each lane keeps K*U 16-byte loads in flight.
+// HBM bytes per call: read N*H*2 + N*4 (dst) [+ N*4 weights]; write
+// R*S*H*2 [+ N*4].
+#include "copy_common.cuh"
+#include "moonep_internal.cuh"
+
+namespace moonep {
+namespace {
+
+constexpr int kThreads = 256;
+
+struct Args {
+  const uint4 *y;
+  const float *w_nvs;
+  const int32_t *dst;
+  uint4 *out;
+  float *w_out;
+  int32_t *status;
+  int64_t ntok;
+  int64_t total_rows;
+  int K, H8, nchunk;
+};
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    acc[2 * i] += __uint_as_float(w[i] << 16);
+    acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ void set_bf16x8(float (&acc)[8], const uint4 &v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    acc[2 * i] = __uint_as_float(w[i] << 16);
+    acc[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i]));
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1]));
+    w[i] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// KT: compile-time K (0 = runtime K, up to 32).  U: vectors per lane per unit.
+template <int KT, int U>
+__global__ void __launch_bounds__(kThreads) combine_kernel(Args a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int K = KT > 0 ? KT : a.K;
+  const int64_t units = a.ntok * a.nchunk;
+  for (int64_t u = wid; u < units; u += nw) {
+    const int64_t t = u / a.nchunk;
+    const int c = (int)(u - t * a.nchunk);
+    int64_t g = 0;
+    if (lane < K) {
+      g = decode_row(__ldg(a.dst + t * K + lane));
+      if (g >= a.total_rows) {
+        set_status(a.status, MOONEP_ERR_PLAN);
+        g = 0;
+      }
+      if (c == 0 && a.w_out) a.w_out[t * K + lane] = __ldg(a.w_nvs + g);
+    }
+    const int v0 = c * 32 * U + lane;
+    float acc[U][8];
+    if (KT > 0) {
+      constexpr int KK = KT > 0 ? KT : 1;
+      uint4 x[KK][U];
+#pragma unroll
+      for (int k = 0; k < KK; k++) {
+        const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k) * a.H8;
+#pragma unroll
+        for (int i = 0; i < U; i++) {
+          const int v = v0 + 32 * i;
+          if (v < a.H8) x[k][i] = ld_stream(row + v);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < U; i++) {
+        set_bf16x8(acc[i], x[0][i]);
+#pragma unroll
+        for (int k = 1; k < KK; k++) add_bf16x8(acc[i], x[k][i]);
+      }
+    } else {
+      for (int k = 0; k < K; k++) {
+        const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k) * a.H8;
+#pragma unroll
+        for (int i = 0; i < U; i++) {
+          const int v = v0 + 32 * i;
+          uint4 xv = make_uint4(0, 0, 0, 0);
+          if (v < a.H8) xv = ld_stream(row + v);
+          if (k == 0) set_bf16x8(acc[i], xv); else add_bf16x8(acc[i], xv);
+        }
+      }
+    }
+    uint4 *op = a.out + t * a.H8;
+#pragma unroll
+    for (int i = 0; i < U; i++) {
+      const int v = v0 + 32 * i;
+      if (v < a.H8) st_global(op + v, pack_bf16x8(acc[i]));
+    }
+  }
+}
+
+template <int KT, int U>
+void launch(const Args &a, int grid, cudaStream_t st) {
+  combine_kernel<KT, U><<<grid, kThreads, 0, st>>>(a);
+}
+
+}  // namespace
+
+int occupancy_combine(int K) {
+  int n = 0;
+  void *f = K == 1 ? (void *)combine_kernel<1, 4> : K == 2 ? (void *)combine_kernel<2, 4>
+          : K == 4 ? (void *)combine_kernel<4, 4> : K == 8 ? (void *)combine_kernel<8, 2>
+          : (void *)combine_kernel<0, 2>;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess) n = 1;
+  return n > 0 ? n : 1;
+}
+
+int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *y,
+                   const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st) {
+  const moonep_config &c = ctx->cfg;
+  Args a;
+  a.y = reinterpret_cast<const uint4 *>(y);
+  a.w_nvs = w_nvs;
+  a.dst = plan->dst;
+  a.out = reinterpret_cast<uint4 *>(out);
+  a.w_out = w_out;
+  a.status = ctx->d_status;
+  a.ntok = (int64_t)c.R * c.S;
+  a.total_rows = (int64_t)c.R * ctx->NvS;
+  a.K = c.K;
+  a.H8 = c.H / 8;
+  const int U = (c.K == 1 || c.K == 2 || c.K == 4) ? 4 : 2;
+  a.nchunk = (a.H8 + 32 * U - 1) / (32 * U);
+  if (a.ntok == 0 || a.H8 == 0) return MOONEP_OK;
+  const int grid = ctx->sms * ctx->blocks_combine;
+  switch (c.K) {
+    case 1: launch<1, 4>(a, grid, st); break;
+    case 2: launch<2, 4>(a, grid, st); break;
+    case 4: launch<4, 4>(a, grid, st); break;
+    case 8: launch<8, 2>(a, grid, st); break;
+    default: launch<0, 2>(a, grid, st); break;
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moonep

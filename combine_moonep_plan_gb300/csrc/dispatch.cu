@@ -1,0 +1,175 @@
+// Fused-permute dispatch.
+//
+// "MoonEP Public API Visual Guide", Buffer.dispatch(...): decode route
+// i = s*K + k, copy the token's hidden row to its destination row, scatter
+// every routing weight, zero-fill padding, expand locally deduplicated routes.
+// "MoonshotAI/MoonEP" README item 3: tokens are written straight to their
+// expert-grouped positions (no permute in, no permute out).
+//
+// On one GPU every destination row is local HBM, so duplicates are expanded by
+// writing the row to every |dst| directly: each source row is read once and
+// written K times.  The work is cut into units of (token, 2 KB chunk of its
+// row) followed by (padding row, chunk), strided over every warp of a
+// persistent grid, so the tail is balanced whatever the token count.
+// HBM bytes per call: read R*S*H*2 + N*8 (dst, weights); write
+// (N + P)*(H*2 + 4), P = padding rows.
+#include "copy_common.cuh"
+#include "moonep_internal.cuh"
+
+namespace moonep {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kU = 4;                  // 16-byte vectors per lane per unit
+constexpr int kChunk = 32 * kU;        // vectors per unit (2 KB)
+
+struct Args {
+  const uint4 *hidden;
+  const float *w_sk;
+  const int32_t *dst;
+  uint4 *out;
+  float *w_out;
+  const int32_t *pad_prefix;
+  const int32_t *zfr;
+  const int32_t *meta;
+  int32_t *status;
+  int64_t ntok;       // R*S
+  int64_t total_rows; // R*NvS
+  int K, H8, nchunk, NvS, nseg, EB;
+};
+
+template <int KT>
+__global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int K = KT > 0 ? KT : a.K;
+  const int64_t tok_units = a.ntok * a.nchunk;
+  const int64_t P = a.meta[kMetaP];
+  const int64_t units = tok_units + P * a.nchunk;
+  for (int64_t u = wid; u < units; u += nw) {
+    if (u < tok_units) {
+      const int64_t t = u / a.nchunk;
+      const int c = (int)(u - t * a.nchunk);
+      int64_t g = -1;
+      if (lane < K) {
+        const int64_t gg = decode_row(__ldg(a.dst + t * K + lane));
+        if (gg < a.total_rows) {
+          g = gg;
+        } else {
+          set_status(a.status, MOONEP_ERR_PLAN);
+        }
+        if (c == 0 && g >= 0 && a.w_out) a.w_out[g] = __ldg(a.w_sk + t * K + lane);
+      }
+      const uint4 *src = a.hidden + t * a.H8;
+      const int v0 = c * kChunk + lane;
+      uint4 x[kU];
+#pragma unroll
+      for (int i = 0; i < kU; i++) {
+        const int v = v0 + 32 * i;
+        if (v < a.H8) x[i] = ld_stream(src + v);
+      }
+      if (KT > 0) {
+#pragma unroll
+        for (int k = 0; k < (KT > 0 ? KT : 1); k++) {
+          const int64_t gk = __shfl_sync(0xffffffffu, g, k);
+          if (gk < 0) continue;
+          uint4 *dp = a.out + gk * a.H8;
+#pragma unroll
+          for (int i = 0; i < kU; i++) {
+            const int v = v0 + 32 * i;
+            if (v < a.H8) st_global(dp + v, x[i]);
+          }
+        }
+      } else {
+        for (int k = 0; k < K; k++) {
+          const int64_t gk = __shfl_sync(0xffffffffu, g, k);
+          if (gk < 0) continue;
+          uint4 *dp = a.out + gk * a.H8;
+#pragma unroll
+          for (int i = 0; i < kU; i++) {
+            const int v = v0 + 32 * i;
+            if (v < a.H8) st_global(dp + v, x[i]);
+          }
+        }
+      }
+    } else {
+      // padding row q: segment = last s with pad_prefix[s] <= q
+      const int64_t pu = u - tok_units;
+      const int64_t q = pu / a.nchunk;
+      const int c = (int)(pu - q * a.nchunk);
+      int lo = 0, hi = a.nseg;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(a.pad_prefix + mid) <= q) lo = mid; else hi = mid;
+      }
+      const int j = lo / a.EB;
+      const int64_t row = __ldg(a.zfr + 2 * lo) + (q - __ldg(a.pad_prefix + lo));
+      const int64_t g = (int64_t)j * a.NvS + row;
+      if (g >= a.total_rows) {
+        set_status(a.status, MOONEP_ERR_PLAN);
+        continue;
+      }
+      uint4 *dp = a.out + g * a.H8;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int i = 0; i < kU; i++) {
+        const int v = c * kChunk + lane + 32 * i;
+        if (v < a.H8) st_global(dp + v, z);
+      }
+      if (c == 0 && lane == 0 && a.w_out) a.w_out[g] = 0.0f;
+    }
+  }
+}
+
+template <int KT>
+void *kernel_ptr() {
+  return (void *)dispatch_kernel<KT>;
+}
+
+}  // namespace
+
+int occupancy_dispatch(int K) {
+  int n = 0;
+  void *f = K == 1 ? kernel_ptr<1>() : K == 2 ? kernel_ptr<2>() : K == 4 ? kernel_ptr<4>()
+          : K == 8 ? kernel_ptr<8>() : kernel_ptr<0>();
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess) n = 1;
+  return n > 0 ? n : 1;
+}
+
+int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *hidden,
+                    const float *w_sk, uint16_t *out, float *w_out, cudaStream_t st) {
+  const moonep_config &c = ctx->cfg;
+  PlanLayout lay = PlanLayout::make(c.R, c.E, c.B, ctx->NvS,
+                                    (plan->flags & MOONEP_PLAN_DUP_RECORDS) != 0);
+  Args a;
+  a.hidden = reinterpret_cast<const uint4 *>(hidden);
+  a.w_sk = w_sk;
+  a.dst = plan->dst;
+  a.out = reinterpret_cast<uint4 *>(out);
+  a.w_out = w_out;
+  a.pad_prefix = plan->internal + lay.pad_prefix;
+  a.zfr = plan->zero_fill_ranges;
+  a.meta = plan->internal;
+  a.status = ctx->d_status;
+  a.ntok = (int64_t)c.R * c.S;
+  a.total_rows = (int64_t)c.R * ctx->NvS;
+  a.K = c.K;
+  a.H8 = c.H / 8;
+  a.nchunk = (a.H8 + kChunk - 1) / kChunk;
+  a.NvS = ctx->NvS;
+  a.nseg = c.R * ctx->EB;
+  a.EB = ctx->EB;
+  if (a.H8 == 0) return MOONEP_OK;
+  const int grid = ctx->sms * ctx->blocks_dispatch;
+  switch (c.K) {
+    case 1: dispatch_kernel<1><<<grid, kThreads, 0, st>>>(a); break;
+    case 2: dispatch_kernel<2><<<grid, kThreads, 0, st>>>(a); break;
+    case 4: dispatch_kernel<4><<<grid, kThreads, 0, st>>>(a); break;
+    case 8: dispatch_kernel<8><<<grid, kThreads, 0, st>>>(a); break;
+    default: dispatch_kernel<0><<<grid, kThreads, 0, st>>>(a); break;
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moonep

@@ -1,0 +1,111 @@
+// Internal declarations shared by the translation units of libmoonep.
+// Not part of the public ABI (include/moonep.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moonep.h"
+
+namespace moonep {
+
+// Routes handled by one planner tile: 8 warps x 32 lanes x 8 routes.
+constexpr int kPlanThreads = 256;
+constexpr int kPlanItems = 8;
+constexpr int kTile = kPlanThreads * kPlanItems;
+
+// Bits of the plan-local error word (meta[kMetaErr]).
+constexpr int kErrBadExpert = 1;
+constexpr int kErrHist = 2;
+constexpr int kErrSlots = 4;
+
+// Scalar words at the head of plan->internal.
+enum {
+  kMetaErr = 0,    // error bits found while planning
+  kMetaValid = 1,  // 1 when the plan's tables are usable
+  kMetaP = 2,      // padding rows over all ranks
+  kMetaU = 3,      // used prefetch slots over all ranks
+  kMetaD = 4,      // experts with at least one slot copy
+  kMetaWords = 16
+};
+
+// Word offsets of the tables inside plan->internal (see PlanLayout::make).
+struct PlanLayout {
+  int64_t qoff, T, home_rowbase, keep, piece_first, piece_count, piece_start,
+      piece_len, piece_recv, slot_rowbase, slot_b, nseg, pad_prefix, copy_slot,
+      copy_expert, red_expert, red_first, red_slot, dupflag, total;
+  static PlanLayout make(int R, int E, int B, int NvS, bool dup_records) {
+    PlanLayout l;
+    const int L = E / R, EB = E + B;
+    int64_t o = kMetaWords;
+    auto take = [&o](int64_t n) { int64_t at = o; o += (n + 3) / 4 * 4; return at; };
+    l.qoff = take(E);
+    l.T = take(E);
+    l.home_rowbase = take(E);
+    l.keep = take(R);
+    l.piece_first = take(R);
+    l.piece_count = take(R);
+    l.piece_start = take(R);
+    l.piece_len = take(R);
+    l.piece_recv = take(R);
+    l.slot_rowbase = take((int64_t)R * L);
+    l.slot_b = take((int64_t)R * L);
+    l.nseg = take((int64_t)R * EB);
+    l.pad_prefix = take((int64_t)R * EB + 1);
+    l.copy_slot = take((int64_t)R * B);
+    l.copy_expert = take((int64_t)R * B);
+    l.red_expert = take(E);
+    l.red_first = take(E + 1);
+    l.red_slot = take((int64_t)R * B);
+    l.dupflag = dup_records ? take((int64_t)R * NvS) : -1;
+    l.total = o;
+    return l;
+  }
+};
+
+}  // namespace moonep
+
+struct moonep_ctx {
+  moonep_config cfg;
+  int device;
+  int sms;         // SMs the copy kernels may use
+  int L, C, EB, NvS, TPR, G;  // E/R, S*K, E+B, rows per rank, tiles per rank, R*TPR
+  int destroyed;
+  int32_t *d_status;   // sticky first error
+  int32_t *d_hist;     // [E, G] tile histograms -> exclusive tile offsets
+  int32_t *d_ord;      // [R*C] ordinal of a route among its tile's routes to the same expert
+  uint16_t *d_hidden_view;  // optional [R*NvS, H] bf16
+  float *d_weight_view;     // optional [R*NvS] fp32
+  int blocks_dispatch, blocks_combine, blocks_copy;  // resident blocks per SM
+};
+
+namespace moonep {
+
+int check_ctx(const moonep_ctx *ctx);
+int check_plan(const moonep_ctx *ctx, const moonep_comm_plan *plan);
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+int cuda_status(cudaError_t e);
+
+// Launchers (one per translation unit).
+int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
+                moonep_comm_plan *plan, cudaStream_t st);
+int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *hidden,
+                    const float *w_sk, uint16_t *out, float *w_out, cudaStream_t st);
+int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *y,
+                   const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st);
+int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj,
+                    uint16_t *const *W, int64_t HHp, cudaStream_t st);
+int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, float *const *Gh,
+                  float *const *Gs, int64_t HHp, cudaStream_t st);
+// Opt the planner kernels into the dynamic shared memory E experts need.
+cudaError_t plan_configure(int R, int E);
+int occupancy_dispatch(int K);
+int occupancy_combine(int K);
+int occupancy_copy();
+
+// Latch the first error code into the status word.
+__device__ __forceinline__ void set_status(int32_t *status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+}  // namespace moonep

@@ -1,0 +1,187 @@
+// Redundant-expert weight prefetch and gradient reduce.
+//
+// "MoonEP Public API Visual Guide", Buffer.prefetch_weight(...): each used slot
+// of plan.experts_to_copy receives its source expert's [H, H'] weight; -1
+// slots are skipped.  Buffer.reduce_grad(...): every owned expert seeds an
+// accumulator with its own fp32 gradient, adds the matching slot gradients of
+// every rank, writes the sum back, and the consumed slots are cleared.
+// "MoonshotAI/MoonEP" README, "Weight buffer": the [E+B, H, H'] tensors and the
+// [R, B, H, H'] reduce buffer.
+//
+// One device holds every rank's slots: the weight tensor is [E + R*B, HHp]
+// (rank j's slot b is row E + j*B + b) and the slot gradients are [R*B, HHp].
+// The planner leaves compact lists on the device (used slots; experts with
+// copies and their slots in (rank, slot) order), so both kernels walk only the
+// rows that move.  Work units are 64 KB chunks of a row, strided over a
+// persistent grid.  Reduce reads each slot element once, adds it, and zeroes
+// it in the same thread, so no barrier separates the reduce and the clear.
+// HBM bytes: prefetch 2*U*HHp*2 per projection; reduce (2*D + 2*U)*HHp*4.
+#include "copy_common.cuh"
+#include "moonep_internal.cuh"
+
+namespace moonep {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxProj = 4;
+constexpr int kChunkVec = 4096;  // 16-byte vectors per unit (64 KB)
+constexpr int kPU = 4;           // vectors per thread per step
+
+struct PrefetchArgs {
+  uint4 *W[kMaxProj];
+  const int32_t *meta, *copy_slot, *copy_expert;
+  int n_proj, E;
+  int64_t vec_per_row;  // HHp / 8
+  int64_t nchunk;
+};
+
+__global__ void __launch_bounds__(kThreads) prefetch_kernel(PrefetchArgs a) {
+  const int64_t U = a.meta[kMetaU];
+  const int64_t per_proj = U * a.nchunk;
+  const int64_t units = per_proj * a.n_proj;
+  for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int p = (int)(unit / per_proj);
+    const int64_t rem = unit - p * per_proj;
+    const int64_t s = rem / a.nchunk;
+    const int64_t c = rem - s * a.nchunk;
+    const int slot = a.copy_slot[s];
+    const int e = a.copy_expert[s];
+    const uint4 *src = a.W[p] + (int64_t)e * a.vec_per_row;
+    uint4 *dst = a.W[p] + ((int64_t)a.E + slot) * a.vec_per_row;
+    const int64_t v_begin = c * kChunkVec;
+    const int64_t v_end = min(v_begin + kChunkVec, a.vec_per_row);
+    for (int64_t v = v_begin + threadIdx.x; v < v_end; v += kThreads * kPU) {
+      uint4 x[kPU];
+#pragma unroll
+      for (int i = 0; i < kPU; i++)
+        if (v + i * kThreads < v_end) x[i] = ld_stream(src + v + i * kThreads);
+#pragma unroll
+      for (int i = 0; i < kPU; i++)
+        if (v + i * kThreads < v_end) st_global(dst + v + i * kThreads, x[i]);
+    }
+  }
+}
+
+struct ReduceArgs {
+  float4 *Gh[kMaxProj];
+  float4 *Gs[kMaxProj];
+  const int32_t *meta, *red_expert, *red_first, *red_slot;
+  int n_proj;
+  int64_t vec_per_row;  // HHp / 4
+  int64_t nchunk;
+};
+
+__global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
+  const int64_t D = a.meta[kMetaD];
+  const int64_t per_proj = D * a.nchunk;
+  const int64_t units = per_proj * a.n_proj;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int p = (int)(unit / per_proj);
+    const int64_t rem = unit - p * per_proj;
+    const int64_t di = rem / a.nchunk;
+    const int64_t c = rem - di * a.nchunk;
+    const int e = a.red_expert[di];
+    const int f0 = a.red_first[di], f1 = a.red_first[di + 1];
+    float4 *home = a.Gh[p] + (int64_t)e * a.vec_per_row;
+    float4 *slots = a.Gs[p];
+    const int64_t v_begin = c * kChunkVec;
+    const int64_t v_end = min(v_begin + kChunkVec, a.vec_per_row);
+    // Two vectors per thread, up to four slot rows loaded before they are
+    // added, so several loads are in flight; adds stay in slot-list order.
+    for (int64_t v = v_begin + threadIdx.x; v < v_end; v += 2 * kThreads) {
+      float4 acc[2];
+      bool ok[2];
+#pragma unroll
+      for (int i = 0; i < 2; i++) {
+        ok[i] = v + i * kThreads < v_end;
+        if (ok[i]) acc[i] = ld_once_f4(home + v + i * kThreads);
+      }
+      for (int f = f0; f < f1; f += 4) {
+        float4 x[4][2];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          if (f + q >= f1) break;
+          const float4 *sp = slots + (int64_t)a.red_slot[f + q] * a.vec_per_row + v;
+#pragma unroll
+          for (int i = 0; i < 2; i++)
+            if (ok[i]) x[q][i] = ld_once_f4(sp + i * kThreads);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          if (f + q >= f1) break;
+          float4 *sp = slots + (int64_t)a.red_slot[f + q] * a.vec_per_row + v;
+#pragma unroll
+          for (int i = 0; i < 2; i++) {
+            if (!ok[i]) continue;
+            acc[i].x = acc[i].x + x[q][i].x;
+            acc[i].y = acc[i].y + x[q][i].y;
+            acc[i].z = acc[i].z + x[q][i].z;
+            acc[i].w = acc[i].w + x[q][i].w;
+            st_global_f4(sp + i * kThreads, zero);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 2; i++)
+        if (ok[i]) st_global_f4(home + v + i * kThreads, acc[i]);
+    }
+  }
+}
+
+}  // namespace
+
+int occupancy_copy() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefetch_kernel, kThreads, 0) !=
+      cudaSuccess)
+    n = 1;
+  return n > 0 ? n : 1;
+}
+
+int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, uint16_t *const *W,
+                    int64_t HHp, cudaStream_t st) {
+  const moonep_config &c = ctx->cfg;
+  if (n_proj < 1 || n_proj > kMaxProj) return MOONEP_ERR_INVALID_ARG;
+  PlanLayout lay = PlanLayout::make(c.R, c.E, c.B, ctx->NvS,
+                                    (plan->flags & MOONEP_PLAN_DUP_RECORDS) != 0);
+  PrefetchArgs a{};
+  for (int p = 0; p < n_proj; p++) a.W[p] = reinterpret_cast<uint4 *>(W[p]);
+  a.meta = plan->internal;
+  a.copy_slot = plan->internal + lay.copy_slot;
+  a.copy_expert = plan->internal + lay.copy_expert;
+  a.n_proj = n_proj;
+  a.E = c.E;
+  a.vec_per_row = HHp / 8;
+  a.nchunk = (a.vec_per_row + kChunkVec - 1) / kChunkVec;
+  if (a.vec_per_row == 0 || c.B == 0) return MOONEP_OK;
+  const int grid = ctx->sms * ctx->blocks_copy;
+  prefetch_kernel<<<grid, kThreads, 0, st>>>(a);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, float *const *Gh,
+                  float *const *Gs, int64_t HHp, cudaStream_t st) {
+  const moonep_config &c = ctx->cfg;
+  if (n_proj < 1 || n_proj > kMaxProj) return MOONEP_ERR_INVALID_ARG;
+  PlanLayout lay = PlanLayout::make(c.R, c.E, c.B, ctx->NvS,
+                                    (plan->flags & MOONEP_PLAN_DUP_RECORDS) != 0);
+  ReduceArgs a{};
+  for (int p = 0; p < n_proj; p++) {
+    a.Gh[p] = reinterpret_cast<float4 *>(Gh[p]);
+    a.Gs[p] = reinterpret_cast<float4 *>(Gs[p]);
+  }
+  a.meta = plan->internal;
+  a.red_expert = plan->internal + lay.red_expert;
+  a.red_first = plan->internal + lay.red_first;
+  a.red_slot = plan->internal + lay.red_slot;
+  a.n_proj = n_proj;
+  a.vec_per_row = HHp / 4;
+  a.nchunk = (a.vec_per_row + kChunkVec - 1) / kChunkVec;
+  if (a.vec_per_row == 0 || c.B == 0) return MOONEP_OK;
+  const int grid = ctx->sms * ctx->blocks_copy;
+  reduce_kernel<<<grid, kThreads, 0, st>>>(a);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace moonep

@@ -1,0 +1,233 @@
+/*
+ * moonep.h -- C ABI of the GB300 (sm_103a) balanced expert-parallel hot path.
+ *
+ * One process, one GPU.  The R expert-parallel ranks of the method are R
+ * logical partitions of this device's HBM: rank j's dispatched rows are rows
+ * [j*NvS, (j+1)*NvS) of one [R*NvS, H] buffer, so a "remote" write of the
+ * method is an ordinary scatter inside one allocation.
+ *
+ * Sources (page title, section):
+ *   [API]    "MoonEP Public API Visual Guide": Notation; Buffer(...);
+ *            Buffer.dispatch(...); Buffer.prefetch_weight(...);
+ *            Buffer.combine(...); Buffer.reduce_grad(...);
+ *            Buffer.hidden_nvsh_buffer_view; Buffer.router_weight_buffer_view;
+ *            Buffer.destroy(); MoonEPCommPlan and MoonEPCommPlan.clone().
+ *   [README] "MoonshotAI/MoonEP" README: items 1-3; "Weight buffer";
+ *            "How to set B".
+ *   [vLLM]   "vllm ... prepare_finalize.moonep": prepare() and finalize().
+ *
+ * Conventions shared by every entry point
+ *   - Arrays are dense, row-major, and live in device memory unless stated.
+ *     bf16 tensors travel as uint16_t bit patterns.
+ *   - Every device pointer must be 16-byte aligned; H % 8 == 0 and, for the
+ *     weight entry points, HHp % 8 == 0 (16-byte rows).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     is stream-ordered and asynchronous: nothing synchronises with the host
+ *     except moonep_get_status, moonep_ctx_destroy and moonep_plan_destroy
+ *     ("statically known shapes eliminate per-layer MoE host
+ *     synchronization" [README item 3]).
+ *   - Return value: MOONEP_OK (0) or a negative MOONEP_ERR_*.  Errors found on
+ *     the host (bad argument, destroyed context, CUDA launch failure) return
+ *     at once and launch nothing.  Errors found by a kernel (bad expert id,
+ *     histogram mismatch, too many slots, corrupted plan) are latched in the
+ *     context's device status word and read with moonep_get_status; outputs of
+ *     the failing call and of calls that use its plan are then unspecified but
+ *     every kernel stays inside the buffers it was given.
+ *   - The caller owns every tensor argument.  The library owns the context's
+ *     scratch and status word, the plan's arrays and the optional zero-copy
+ *     buffers behind moonep_hidden_view / moonep_weight_view.
+ */
+#ifndef MOONEP_H
+#define MOONEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOONEP_OK 0
+#define MOONEP_ERR_INVALID_ARG (-1)   /* bad argument or configuration (host) */
+#define MOONEP_ERR_BAD_EXPERT (-2)    /* a top-k id outside [0, E) (device) */
+#define MOONEP_ERR_HIST_MISMATCH (-3) /* tokens_per_expert != recount of topk (device) */
+#define MOONEP_ERR_SLOTS (-4)         /* a rank needs more than B slots (device) */
+#define MOONEP_ERR_CUDA (-5)          /* a CUDA call failed (host) */
+#define MOONEP_ERR_DESTROYED (-6)     /* context already destroyed (host) */
+#define MOONEP_ERR_PLAN (-7)          /* plan row outside [0, R*NvS) (device) */
+#define MOONEP_ERR_NOMEM (-8)         /* device allocation failed (host) */
+
+/* Constructor controls [API, Buffer(...)]: E % R == 0; B prefetch slots per
+ * rank (B = E/R is what training needs [README, How to set B]; smaller B is
+ * allowed and reported as MOONEP_ERR_SLOTS when a plan needs more);
+ * token_padding = row alignment of every non-empty segment; num_sms caps the
+ * SMs the copy kernels use (<= 0: every SM). */
+typedef struct moonep_config {
+  int R;             /* expert-parallel ranks (logical partitions), >= 1 */
+  int E;             /* experts, multiple of R */
+  int K;             /* routes per token, 1..32 */
+  int S;             /* tokens per rank, >= 0 */
+  int H;             /* hidden size, multiple of 8 */
+  int B;             /* prefetch slots per rank, >= 0 */
+  int token_padding; /* >= 1 */
+  int num_sms;       /* <= 0: all SMs */
+} moonep_config;
+
+typedef struct moonep_ctx moonep_ctx;
+
+/* Plan flags */
+#define MOONEP_PLAN_DUP_RECORDS 1 /* also build dup_groups / dup_loffs */
+
+/* A communication plan [API, MoonEPCommPlan].  All pointers are device
+ * arrays owned by the plan (moonep_plan_create / _clone / _destroy).
+ *   dst[R, S*K]              encoded global row of every route i = s*K + k of
+ *                            source rank r: g = j*NvS + w for the first route
+ *                            of the token that lands on rank j, -(g+1) for a
+ *                            later route of that token on the same rank
+ *                            [API, Buffer.combine: positive/negative encoding]
+ *   experts_to_copy[R, B]    expert held by each prefetch slot, -1 = unused
+ *   cu_seqlens[R, E+B]       inclusive padded end offset of every segment,
+ *                            rank-local rows, no leading 0 [API,
+ *                            Buffer.dispatch; vLLM prepare: diff(cu_seqlens)]
+ *   zero_fill_ranges[R,E+B,2] [start, end) padding rows of every segment
+ *   remote_stats[R, 2]       {routes received from a remote home group,
+ *                            prefetch slots used}
+ *   dup_counts[R, 2]         {local duplicate routes, duplicate groups}
+ *   dup_groups[R, NvS, 3]    (primary row, first index into dup_loffs, number
+ *                            of duplicates), ascending primary row; valid
+ *                            prefix dup_counts[j][1]; NULL unless the plan was
+ *                            created with MOONEP_PLAN_DUP_RECORDS
+ *   dup_loffs[R, NvS]        duplicate rows, grouped as dup_groups says; valid
+ *                            prefix dup_counts[j][0]
+ *   internal                 library-private tables (do not touch)
+ * Segments of rank j: x = e for its home experts e in [j*E/R, (j+1)*E/R),
+ * x = E + b for prefetch slot b; other segments are empty.  Rows
+ * [cu_seqlens[j][E+B-1], NvS) of a rank (the tail) are never written. */
+typedef struct moonep_comm_plan {
+  int32_t *dst;
+  int32_t *experts_to_copy;
+  int32_t *cu_seqlens;
+  int32_t *zero_fill_ranges;
+  int32_t *remote_stats;
+  int32_t *dup_counts;
+  int32_t *dup_groups;
+  int32_t *dup_loffs;
+  int32_t *internal;
+  int N;          /* routes per rank, S*K */
+  int R, E, B, K, S;
+  int NvS;        /* dispatched-row capacity per rank */
+  int NvS_padded; /* row stride between ranks (== NvS) */
+  int flags;
+  size_t internal_bytes;
+} moonep_comm_plan;
+
+/* Sizes for a configuration: NvS = roundup(S*K + (E/R + B)*(tp-1), tp) and the
+ * context's device scratch in bytes.  Any output pointer may be NULL. */
+int moonep_query_sizes(const moonep_config *cfg, int *NvS, int *NvS_padded,
+                       size_t *scratch_bytes);
+
+/* Create a context on the current CUDA device [API, Buffer(...)]: validates
+ * the configuration, allocates planner scratch and the status word, and, when
+ * alloc_views != 0, the persistent [R*NvS, H] bf16 hidden buffer and [R*NvS]
+ * fp32 weight buffer behind the zero-copy views.  *out is set on success. */
+int moonep_ctx_create(const moonep_config *cfg, int alloc_views,
+                      moonep_ctx **out);
+
+/* Synchronise the device, free everything the context owns, mark it
+ * destroyed [API, Buffer.destroy()].  Idempotent; NULL is accepted.  The
+ * handle itself stays allocated so that later calls on it return
+ * MOONEP_ERR_DESTROYED; moonep_ctx_free releases it. */
+int moonep_ctx_destroy(moonep_ctx *ctx);
+void moonep_ctx_free(moonep_ctx *ctx);
+/* 1 once moonep_ctx_destroy has completed [API, Buffer.destroyed]. */
+int moonep_ctx_destroyed(const moonep_ctx *ctx);
+
+/* Allocate a plan's device arrays for the context's configuration.  flags:
+ * MOONEP_PLAN_DUP_RECORDS. */
+int moonep_plan_create(moonep_ctx *ctx, int flags, moonep_comm_plan *plan);
+/* Free a plan's arrays (synchronises the device first); idempotent. */
+int moonep_plan_destroy(moonep_comm_plan *plan);
+/* Deep copy of every array and scalar [API, MoonEPCommPlan.clone()]: dst
+ * must be a plan created for the same configuration and flags. */
+int moonep_plan_clone(const moonep_comm_plan *src, moonep_comm_plan *dst, void *stream);
+
+/* Online planner [API, Buffer.dispatch: "planning converts the S * K logical
+ * routes into a compact dst map ..."; README items 1-2].
+ *   topk  [R, S, K] int32 expert ids, each in [0, E)
+ *   tpe   [R, E] int32 per-rank histogram, or NULL; when given it is checked
+ *         against a recount (MOONEP_ERR_HIST_MISMATCH)
+ * Fills every array of `plan`.  Deterministic: the same inputs give the same
+ * plan, bit for bit.  Every rank receives exactly S*K routes; the experts a
+ * rank prefetches come from one remote home group, at most B of them. */
+int moonep_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
+                moonep_comm_plan *plan, void *stream);
+
+/* Fused-permute dispatch [API, Buffer.dispatch; README item 3].
+ *   hidden      [R, S, H] bf16 source rows
+ *   w_sk        [R, S, K] fp32 route weights, or NULL
+ *   hidden_nvsh [R*NvS, H] bf16 out: row |dst| of every route = its token's
+ *               row; padding rows zero; tail rows untouched
+ *   w_nvs       [R*NvS] fp32 out, or NULL: route weight per row, 0 on padding
+ * Passing a saved plan again is the plan-reuse path (combine-backward
+ * dispatch of an [R, S, H] gradient, weights NULL) [API, Buffer.dispatch:
+ * "When an existing plan is passed, planning is skipped"]. */
+int moonep_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan,
+                    const uint16_t *hidden, const float *w_sk,
+                    uint16_t *hidden_nvsh, float *w_nvs, void *stream);
+
+/* Combine [API, Buffer.combine; vLLM finalize: the K-sum is unweighted].
+ *   y_nvsh   [R*NvS, H] bf16 expert outputs in dispatched order
+ *   w_nvs    [R*NvS] fp32 or NULL
+ *   out_sh   [R, S, H] bf16 out: out[r,s,:] = bf16_rne(fp32 sum over
+ *            k = 0..K-1, in k order, of y[|dst(r,s,k)|,:])
+ *   w_sk_out [R, S, K] fp32 out or NULL: w_nvs[|dst|] (bit copy)
+ * Reads only rows that dst names (never padding or tail rows). */
+int moonep_combine(moonep_ctx *ctx, const moonep_comm_plan *plan,
+                   const uint16_t *y_nvsh, const float *w_nvs,
+                   uint16_t *out_sh, float *w_sk_out, void *stream);
+
+/* Redundant-expert weight prefetch [API, Buffer.prefetch_weight; README,
+ * Weight buffer].  W[p] (p < n_proj <= 4) is a device pointer to one
+ * [E + R*B, HHp] bf16 tensor: rows [0, E) are the experts, rows E + j*B + b
+ * are rank j's slots.  For every slot with experts_to_copy[j][b] = e >= 0:
+ * row E + j*B + b = row e (bit copy).  Unused slots are not touched.
+ * `W` itself is a host array of n_proj device pointers. */
+int moonep_prefetch_weight(moonep_ctx *ctx, const moonep_comm_plan *plan,
+                           int n_proj, uint16_t *const *W, int64_t HHp,
+                           void *stream);
+
+/* Gradient reduce of the redundant experts [API, Buffer.reduce_grad; README,
+ * Weight buffer].  Gh[p] -> [E, HHp] fp32 home-expert gradients, Gs[p] ->
+ * [R*B, HHp] fp32 slot gradients (the [R, B, H, H'] reduce buffer).  For
+ * every expert e held by at least one slot:
+ *   Gh[e] = Gh[e] + Gs[slot_1] + Gs[slot_2] + ...   (fp32, slots in
+ *           ascending (rank, slot) order)
+ * then every used slot is set to 0; unused slots are not touched.  `Gh` and
+ * `Gs` are host arrays of n_proj (<= 4) device pointers. */
+int moonep_reduce_redundant_grad(moonep_ctx *ctx, const moonep_comm_plan *plan,
+                                 int n_proj, float *const *Gh,
+                                 float *const *Gs, int64_t HHp, void *stream);
+
+/* Zero-copy aliases [API, Buffer.hidden_nvsh_buffer_view and
+ * router_weight_buffer_view]: device address of rank `rank`'s [NvS, H] bf16
+ * window (row rank*NvS of the context's hidden buffer) and of its [NvS] fp32
+ * weight window.  NULL if the context was created without views or the rank
+ * is out of range.  Later calls overwrite what they hold. */
+void *moonep_hidden_view(moonep_ctx *ctx, int rank);
+void *moonep_weight_view(moonep_ctx *ctx, int rank);
+
+/* Synchronise `stream`, return the first error any kernel latched since the
+ * last call in *device_status (0 if none) and clear it.  The return value is
+ * the host-side status of the query itself. */
+int moonep_get_status(moonep_ctx *ctx, int *device_status, void *stream);
+
+/* Static text for a status code. */
+const char *moonep_strerror(int code);
+
+/* Number of SMs the copy kernels use for this context. */
+int moonep_num_sms(const moonep_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOONEP_H */

@@ -1,0 +1,359 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Integer and bit-copy outputs (plan arrays, dispatched rows, route weights,
+prefetched weights) must match bit for bit.  Combine must match to within one
+bf16 ulp and the gradient reduce to within 1e-6 relative (both sides add in
+the same order in fp32, so both are in fact expected to be bit-exact and the
+tests also report exactness).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moonep_plan_gb300 import workloads as wl
+from tests.plan_checks import check_plan, decode
+
+pytestmark = pytest.mark.gpu
+
+PLAN_FIELDS = ("dst", "experts_to_copy", "cu_seqlens", "zero_fill_ranges", "remote_stats",
+               "dup_counts")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from combine_moonep_plan_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+
+
+def _buffer(cfg, H=64, dup=True, views=True):
+    from combine_moonep_plan_gb300.api import Buffer
+    return Buffer(S=cfg["S"], H=H, K=cfg["K"], E=cfg["E"], num_ep_ranks=cfg["R"], B=cfg["B"],
+                  token_padding=cfg["tp"], zero_copy_views=views, dup_records=dup)
+
+
+def _oracle_plan(cfg, topk, tpe=None):
+    return oracle.plan(cfg["R"], cfg["E"], cfg["K"], cfg["S"], cfg["B"], cfg["tp"], topk, tpe)
+
+
+def _cmp_plan(gp, op, cfg):
+    for f in PLAN_FIELDS:
+        g = getattr(gp, f).cpu().numpy()
+        assert np.array_equal(g, op[f]), f"plan field {f} differs"
+    if gp.dup_groups is not None:
+        dg = gp.dup_groups.cpu().numpy()
+        dl = gp.dup_loffs.cpu().numpy()
+        for j in range(cfg["R"]):
+            ng, nd = op["dup_counts"][j, 1], op["dup_counts"][j, 0]
+            assert np.array_equal(dg[j, :ng], op["dup_groups"][j, :ng])
+            assert np.array_equal(dl[j, :nd], op["dup_loffs"][j, :nd])
+
+
+def _cfg_of(sh):
+    return dict(R=sh.R, E=sh.E, K=sh.K, S=sh.S, B=sh.B, tp=sh.tp)
+
+
+def _small(name, S):
+    sh = wl.SHAPES[name]
+    return wl.Shape(f"{name}_S{S}", R=sh.R, E=sh.E, K=sh.K, S=S, H=min(sh.H, 512),
+                    Hp=64, B=sh.B, tp=sh.tp, weights=sh.weights)
+
+
+def _routing(sh, kind, seed):
+    if kind == "exact0":
+        return wl.routing(sh, "exact0", seed=seed)[0]
+    if kind == "uniform":
+        return wl.routing(sh, "uniform", seed=seed)[0]
+    if kind == "zipf":
+        return wl.routing(sh, "zipf", zipf_s=1.2, seed=seed)[0]
+    if kind == "zipf_hard":
+        return wl.routing(sh, "zipf", zipf_s=3.0, seed=seed)[0]
+    if kind == "hot":
+        return wl.routing(sh, "hot", hot_share=0.3, seed=seed)[0]
+    if kind == "hot_group0":
+        return wl.routing(sh, "hot", hot_share=0.3, hot_group0=True, seed=seed)[0]
+    raise ValueError(kind)
+
+
+def _full_pipeline(sh, topk, seed, *, dup=True, check_invariants=True):
+    """Plan, dispatch (+weights), combine (+weights) on the GPU and the oracle."""
+    cfg = _cfg_of(sh)
+    R, S, K, E, H = sh.R, sh.S, sh.K, sh.E, sh.H
+    tpe = wl.tokens_per_expert(topk, E)
+    st, op = _oracle_plan(cfg, topk, tpe)
+    assert st == 0
+    if check_invariants and S:
+        check_plan(cfg, topk, op, max_records=256)
+    buf = _buffer(cfg, H=H, dup=dup)
+    x = wl.hidden_bf16(sh, seed)
+    w = wl.route_weights(sh, seed)
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).reshape(R, S, H).cuda()
+    wt = torch.from_numpy(w).cuda()
+    tk = torch.from_numpy(topk).cuda()
+    tp = torch.from_numpy(tpe).cuda()
+    NvS = buf.NvS
+    assert NvS == op["NvS"]
+    # poison the outputs so untouched rows are visible
+    out = torch.full((R * NvS, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    wout = torch.full((R * NvS,), float("nan"), dtype=torch.float32, device="cuda")
+    hid, wn, cu, plan = buf.dispatch(xt, wt, tk, tp, out=out, weights_out=wout)
+    assert buf.get_status() == 0
+    _cmp_plan(plan, op, cfg)
+    assert torch.equal(cu, plan.cu_seqlens)
+    # dispatch parity
+    want = np.full((R * NvS, H), 0x7fc0, np.uint16)
+    want_w = np.full(R * NvS, np.nan, np.float32)
+    oracle.dispatch(R, S, K, E, sh.B, NvS, H, op["dst"], op["zero_fill_ranges"], x, w, want,
+                    want_w)
+    got = hid.view(torch.int16).cpu().numpy().view(np.uint16)
+    touched = np.zeros(R * NvS, bool)
+    touched[decode(op["dst"]).reshape(-1)] = True
+    for j in range(R):
+        for a, b in op["zero_fill_ranges"][j]:
+            touched[j * NvS + a:j * NvS + b] = True
+    assert np.array_equal(got[touched], want[touched]), "dispatched rows differ"
+    gw = wn.cpu().numpy()
+    assert np.array_equal(gw[touched].view(np.uint32), want_w[touched].view(np.uint32))
+    # tail rows untouched (still NaN poison)
+    if (~touched).any():
+        assert np.all(np.isnan(gw[~touched]))
+        tail = got[~touched]
+        assert np.all((tail & 0x7f80) == 0x7f80)
+    # combine parity on random expert outputs with NaN-poisoned padding/tail
+    rng = np.random.default_rng(seed + 17)
+    y = wl.bf16_bits_from_f32(rng.standard_normal((R * NvS, H)).astype(np.float32))
+    valid = np.zeros(R * NvS, bool)
+    valid[decode(op["dst"]).reshape(-1)] = True
+    y[~valid] = 0x7fc1
+    wy = rng.standard_normal(R * NvS).astype(np.float32)
+    wy[~valid] = np.nan
+    ot, ow = oracle.combine(R, S, K, NvS, H, op["dst"], y, wy)
+    yt = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).cuda()
+    cout, cw = buf.combine(plan, yt, torch.from_numpy(wy).cuda())
+    assert buf.get_status() == 0
+    gc = cout.view(torch.int16).cpu().numpy().view(np.uint16).reshape(R * S, H)
+    _assert_bf16_close(gc, ot)
+    assert np.array_equal(cw.cpu().numpy().reshape(R * S, K).view(np.uint32), ow.view(np.uint32))
+    # identity expert: combine(dispatch(x)) == K * x for K a power of two
+    if K & (K - 1) == 0:
+        ident, _ = buf.combine(plan, hid)
+        ref = oracle.bf16_to_f32(x).reshape(R, S, H) * K
+        assert np.array_equal(ident.float().cpu().numpy(), ref)
+    return buf, plan, op
+
+
+def _assert_bf16_close(got, want):
+    """Within one bf16 ulp (the benchmark spec's bound); report exactness."""
+    if np.array_equal(got, want):
+        return
+    g = got.astype(np.int32)
+    w = want.astype(np.int32)
+    # ordered integer representation of bf16
+    g = np.where(g & 0x8000, 0x8000 - g, g)
+    w = np.where(w & 0x8000, 0x8000 - w, w)
+    diff = np.abs(g - w)
+    assert diff.max() <= 1, f"combine differs by {diff.max()} bf16 ulp"
+
+
+# ------------------------------------------------------------------ cases
+
+@pytest.mark.parametrize("kind", ["zipf", "exact0", "uniform", "zipf_hard", "hot"])
+def test_tiny_full_pipeline(kind):
+    sh = wl.SHAPES["tiny"]
+    seeds = {"zipf": 1001, "exact0": 1002, "uniform": 1003, "zipf_hard": 1004, "hot": 1005}
+    topk = _routing(sh, kind, seeds[kind])
+    _full_pipeline(sh, topk, 3)
+
+
+@pytest.mark.parametrize("name", ["mixtral", "deepseek_v3", "kimi_k2", "qwen3_decode"])
+@pytest.mark.parametrize("kind", ["zipf", "zipf_hard", "hot_group0", "exact0"])
+def test_scaled_shapes_pipeline(name, kind):
+    # S chosen so S*K spans several 2048-route planner tiles plus a ragged tail
+    S = {"mixtral": 2100, "deepseek_v3": 600, "kimi_k2": 600, "qwen3_decode": 128}[name]
+    sh = _small(name, S)
+    topk = _routing(sh, kind, 7)
+    _full_pipeline(sh, topk, 11, check_invariants=(name == "qwen3_decode"))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_small_configs(seed):
+    """Random R, E, K (including K outside the specialised set), S, B >= E/R,
+    token_padding and H, skewed routing with repeated experts inside a token."""
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, 9))
+    L = int(rng.integers(1, 9))
+    E = R * L
+    K = int(rng.choice([1, 2, 3, 4, 5, 8, 12]))
+    S = int(rng.integers(1, 700))
+    B = L + int(rng.integers(0, 3))
+    tp = int(rng.choice([1, 2, 3, 8, 16, 128]))
+    H = int(rng.choice([8, 64, 136, 264]))
+    sh = wl.Shape("rand", R=R, E=E, K=K, S=S, H=H, Hp=16, B=B, tp=tp, weights="softmax")
+    p = rng.random(E) ** 4
+    topk = rng.choice(E, size=(R, S, K), p=p / p.sum()).astype(np.int32)
+    _full_pipeline(sh, topk, seed)
+
+
+def test_all_routes_to_one_expert():
+    sh = wl.Shape("one", R=4, E=8, K=2, S=300, H=64, Hp=16, B=2, tp=8, weights="softmax")
+    topk = np.zeros((4, 300, 2), np.int32)
+    buf, plan, op = _full_pipeline(sh, topk, 1)
+    assert np.all(op["experts_to_copy"][1:, 0] == 0)
+
+
+def test_k1_tp1():
+    sh = wl.Shape("k1", R=3, E=6, K=1, S=1000, H=32, Hp=8, B=2, tp=1, weights="softmax")
+    topk = _routing(sh, "zipf_hard", 5)
+    _full_pipeline(sh, topk, 2)
+
+
+def test_empty_tokens():
+    cfg = dict(R=2, E=4, K=2, S=0, B=2, tp=4)
+    buf = _buffer(cfg, H=16)
+    tk = torch.zeros((2, 0, 2), dtype=torch.int32, device="cuda")
+    plan = buf.plan(tk)
+    assert buf.get_status() == 0
+    assert torch.all(plan.cu_seqlens == 0) and torch.all(plan.experts_to_copy == -1)
+
+
+# ----------------------------------------------------- plan properties
+
+def test_plan_is_deterministic_and_clone_matches():
+    sh = _small("deepseek_v3", 512)
+    topk = _routing(sh, "zipf_hard", 3)
+    buf = _buffer(_cfg_of(sh), H=64)
+    tk = torch.from_numpy(topk).cuda()
+    p1 = buf.plan(tk)
+    p2 = buf.plan(tk)
+    c = p1.clone()
+    torch.cuda.synchronize()
+    for f in PLAN_FIELDS + ("dup_groups", "dup_loffs"):
+        assert torch.equal(getattr(p1, f), getattr(p2, f)), f
+        assert torch.equal(getattr(p1, f), getattr(c, f)), f
+
+
+def test_plan_reuse_dispatch_equals_fresh():
+    """Combine-backward: a gradient dispatched with the forward plan lands on
+    the same rows as a fresh dispatch of the same tensor would."""
+    sh = _small("kimi_k2", 300)
+    topk = _routing(sh, "hot", 4)
+    buf = _buffer(_cfg_of(sh), H=sh.H)
+    tk = torch.from_numpy(topk).cuda()
+    x = torch.randn(sh.R, sh.S, sh.H, device="cuda").bfloat16()
+    g = torch.randn(sh.R, sh.S, sh.H, device="cuda").bfloat16()
+    _, _, cu, plan = buf.dispatch(x, None, tk)
+    saved = plan.clone()
+    a, wa, cu2, _ = buf.dispatch(g, plan=saved)
+    assert cu2 is None and wa is None
+    b, _, _, _ = buf.dispatch(g, None, tk)
+    # compare every written row (valid and padding); the tail is unspecified
+    ends = plan.cu_seqlens[:, -1].cpu().tolist()
+    for j, end in enumerate(ends):
+        lo = j * buf.NvS
+        assert torch.equal(a[lo:lo + end].view(torch.int16), b[lo:lo + end].view(torch.int16))
+
+
+def test_zero_copy_views():
+    sh = wl.SHAPES["tiny"]
+    topk = _routing(sh, "zipf", 2)
+    buf = _buffer(_cfg_of(sh), H=sh.H)
+    x = torch.randn(sh.R, sh.S, sh.H, device="cuda").bfloat16()
+    w = torch.rand(sh.R, sh.S, sh.K, device="cuda")
+    hid, wn, _, plan = buf.dispatch(x, w, torch.from_numpy(topk).cuda(), zero_copy=True,
+                                    router_weights_zero_copy=True)
+    assert hid.data_ptr() == buf.hidden_nvsh_buffer_view().data_ptr()
+    assert wn.data_ptr() == buf.router_weight_buffer_view().data_ptr()
+    v1 = buf.hidden_nvsh_buffer_view(1)
+    assert v1.data_ptr() == hid.data_ptr() + buf.NvS * sh.H * 2
+    assert torch.equal(v1, hid[buf.NvS:2 * buf.NvS])
+
+
+# ------------------------------------------------- prefetch and reduce
+
+@pytest.mark.parametrize("name,kind", [("tiny", "zipf"), ("deepseek_v3", "zipf_hard"),
+                                       ("kimi_k2", "hot_group0"), ("mixtral", "zipf_hard")])
+def test_prefetch_and_reduce_parity(name, kind):
+    sh = wl.SHAPES[name] if name == "tiny" else _small(name, 256)
+    cfg = _cfg_of(sh)
+    topk = _routing(sh, kind, 9)
+    st, op = _oracle_plan(cfg, topk)
+    assert st == 0
+    etc = op["experts_to_copy"]
+    assert (etc >= 0).any()
+    buf = _buffer(cfg, H=64)
+    plan = buf.plan(torch.from_numpy(topk).cuda())
+    H, Hp = 64, 40                    # HHp = 2560: several 64 KB-chunk boundaries
+    rows = sh.E + sh.R * sh.B
+    rng = np.random.default_rng(1)
+    Ws = [rng.integers(0, 65535, (rows, H * Hp), dtype=np.uint16) for _ in range(3)]
+    Wt = [torch.from_numpy(W.view(np.int16)).view(torch.bfloat16).reshape(rows, H, Hp).cuda()
+          for W in Ws]
+    buf.prefetch_weight(plan, *Wt)
+    for W, t in zip(Ws, Wt):
+        oracle.prefetch(sh.R, sh.E, sh.B, etc, W, H * Hp)
+        assert np.array_equal(t.view(torch.int16).cpu().numpy().view(np.uint16).reshape(rows, -1), W)
+    Gh = [rng.standard_normal((sh.E, H * Hp)).astype(np.float32) for _ in range(2)]
+    Gs = [rng.standard_normal((sh.R * sh.B, H * Hp)).astype(np.float32) for _ in range(2)]
+    Ght = [torch.from_numpy(g).reshape(sh.E, H, Hp).cuda() for g in Gh]
+    Gst = [torch.from_numpy(g).reshape(sh.R, sh.B, H, Hp).cuda() for g in Gs]
+    buf.reduce_grad(plan, Ght, Gst)
+    assert buf.get_status() == 0
+    for gh, gs, ght, gst in zip(Gh, Gs, Ght, Gst):
+        oracle.reduce(sh.R, sh.E, sh.B, etc, gh, gs, H * Hp)
+        got_h = ght.cpu().numpy().reshape(sh.E, -1)
+        got_s = gst.cpu().numpy().reshape(sh.R * sh.B, -1)
+        rel = np.abs(got_h - gh) / np.maximum(np.abs(gh), 1e-30)
+        assert rel.max() <= 1e-6
+        assert np.array_equal(got_h.view(np.uint32), gh.view(np.uint32)), "reduce not bit-exact"
+        assert np.array_equal(got_s.view(np.uint32), gs.view(np.uint32))
+
+
+# ------------------------------------------------------------- errors
+
+def test_device_errors_latch_status_without_faulting():
+    from combine_moonep_plan_gb300 import _lib
+    sh = wl.SHAPES["tiny"]
+    cfg = _cfg_of(sh)
+    topk = _routing(sh, "zipf", 1)
+    buf = _buffer(cfg, H=sh.H)
+    x = torch.randn(sh.R, sh.S, sh.H, device="cuda").bfloat16()
+    bad = topk.copy()
+    bad[1, 3, 1] = sh.E + 5
+    _, _, _, plan = buf.dispatch(x, None, torch.from_numpy(bad).cuda())
+    out, _ = buf.combine(plan, buf.hidden_nvsh_buffer_view())
+    assert buf.get_status() == _lib.ERR_BAD_EXPERT
+    bad[1, 3, 1] = -4
+    buf.plan(torch.from_numpy(bad).cuda())
+    assert buf.get_status() == _lib.ERR_BAD_EXPERT
+    tpe = wl.tokens_per_expert(topk, sh.E)
+    tpe[0, 2] += 1
+    buf.plan(torch.from_numpy(topk).cuda(), torch.from_numpy(tpe).cuda())
+    assert buf.get_status() == _lib.ERR_HIST_MISMATCH
+    # the context still works afterwards
+    _full_pipeline(sh, topk, 5)
+
+
+def test_slots_error_when_b_too_small():
+    from combine_moonep_plan_gb300 import _lib
+    cfg = dict(R=2, E=4, K=1, S=4, B=1, tp=1)
+    topk = np.array([[[0], [0], [0], [0]], [[0], [0], [1], [1]]], np.int32)
+    buf = _buffer(cfg, H=16)
+    plan = buf.plan(torch.from_numpy(topk).cuda())
+    assert buf.get_status() == _lib.ERR_SLOTS
+    assert torch.all(plan.experts_to_copy == -1)
+    x = torch.randn(2, 4, 16, device="cuda").bfloat16()
+    buf.dispatch(x, plan=plan)
+    buf.combine(plan, buf.hidden_nvsh_buffer_view())
+    assert buf.get_status() == 0
+
+
+def test_destroy_is_idempotent():
+    from combine_moonep_plan_gb300 import _lib
+    buf = _buffer(dict(R=2, E=4, K=2, S=8, B=2, tp=2), H=16)
+    buf.destroy()
+    buf.destroy()
+    assert buf.destroyed
+    with pytest.raises(_lib.MoonepError):
+        buf.plan(torch.zeros((2, 8, 2), dtype=torch.int32, device="cuda"))
