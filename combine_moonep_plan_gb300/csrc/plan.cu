@@ -1,8 +1,8 @@
 // Online planner: S*K routes per rank -> a perfectly balanced plan.
 //
-// "MoonEP Public API Visual Guide", Buffer.dispatch(...): planning converts the
-// S*K routes into a compact dst map, assigns local offsets, reserves E+B padded
-// segments and builds duplicate-route metadata.  "MoonshotAI/MoonEP" README,
+// "MoonEP Public API Visual Guide", Buffer.dispatch(...): the planning step
+// maps every route to its destination row (the dst map), lays out E+B padded
+// segments per rank and records the local duplicates.  "MoonshotAI/MoonEP" README,
 // items 1-2: every rank receives exactly S*K routes; a GPU planning kernel;
 // "How to set B": the redundant experts of a rank come from at most one remote
 // home group.

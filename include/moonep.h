@@ -24,8 +24,7 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
  *     is stream-ordered and asynchronous: nothing synchronises with the host
  *     except moonep_get_status, moonep_ctx_destroy and moonep_plan_destroy
- *     ("statically known shapes eliminate per-layer MoE host
- *     synchronization" [README item 3]).
+ *     (fixed shapes need no per-layer host synchronisation [README item 3]).
  *   - Return value: MOONEP_OK (0) or a negative MOONEP_ERR_*.  Errors found on
  *     the host (bad argument, destroyed context, CUDA launch failure) return
  *     at once and launch nothing.  Errors found by a kernel (bad expert id,
@@ -151,8 +150,8 @@ int moonep_plan_destroy(moonep_comm_plan *plan);
  * must be a plan created for the same configuration and flags. */
 int moonep_plan_clone(const moonep_comm_plan *src, moonep_comm_plan *dst, void *stream);
 
-/* Online planner [API, Buffer.dispatch: "planning converts the S * K logical
- * routes into a compact dst map ..."; README items 1-2].
+/* Online planner [API, Buffer.dispatch(...): the planning step that turns
+ * every rank's S*K routes into the dst map; README items 1-2].
  *   topk  [R, S, K] int32 expert ids, each in [0, E)
  *   tpe   [R, E] int32 per-rank histogram, or NULL; when given it is checked
  *         against a recount (MOONEP_ERR_HIST_MISMATCH)
@@ -170,7 +169,7 @@ int moonep_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
  *   w_nvs       [R*NvS] fp32 out, or NULL: route weight per row, 0 on padding
  * Passing a saved plan again is the plan-reuse path (combine-backward
  * dispatch of an [R, S, H] gradient, weights NULL) [API, Buffer.dispatch:
- * "When an existing plan is passed, planning is skipped"]. */
+ * a saved plan skips planning and ignores the routing inputs]. */
 int moonep_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan,
                     const uint16_t *hidden, const float *w_sk,
                     uint16_t *hidden_nvsh, float *w_nvs, void *stream);

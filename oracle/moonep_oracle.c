@@ -70,8 +70,8 @@ static float bf16_to_f32(uint16_t h) {
 
 /* ------------------------------------------------------------------ sizes */
 
-/* "NvS is a capacity" [API, Notation]; "S x K real tokens plus per-VM-group
- * padding" [README, Usage notation].  A rank holds at most L home segments and
+/* NvS is a row capacity [API, Notation]: the S*K real rows plus the padding
+ * of the segments [README, Usage notation].  A rank holds at most L home segments and
  * B slot segments, each padded by at most tp-1 rows. */
 int64_t mo_nvs(int R, int E, int K, int S, int B, int tp) {
   if (R < 1 || E < 1 || K < 1 || S < 0 || B < 0 || tp < 1 || E % R) return -1;

@@ -145,7 +145,7 @@ def _full_pipeline(sh, topk, seed, *, dup=True, check_invariants=True):
 
 
 def _assert_bf16_close(got, want):
-    """Within one bf16 ulp (the benchmark spec's bound); report exactness."""
+    """Within one bf16 ulp (the accuracy bound for combine); exact is the norm."""
     if np.array_equal(got, want):
         return
     g = got.astype(np.int32)
