@@ -30,6 +30,7 @@ EXPORTS = (
     "moonep_plan_clone", "moonep_plan", "moonep_dispatch", "moonep_combine",
     "moonep_prefetch_weight", "moonep_reduce_redundant_grad", "moonep_hidden_view",
     "moonep_weight_view", "moonep_get_status", "moonep_strerror", "moonep_num_sms",
+    "moonep_plan_noalloc",
 )
 
 
@@ -95,6 +96,7 @@ def load(path: str = LIB_PATH):
         "moonep_weight_view": (vp, [vp, ci]),
         "moonep_get_status": (ci, [vp, ctypes.POINTER(ci), vp]),
         "moonep_strerror": (ctypes.c_char_p, [ci]),
+        "moonep_plan_noalloc": (ci, [cfgp] + [vp] * 10),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

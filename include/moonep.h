@@ -161,6 +161,36 @@ int moonep_plan_clone(const moonep_comm_plan *src, moonep_comm_plan *dst, void *
 int moonep_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
                 moonep_comm_plan *plan, void *stream);
 
+/* Planner for callers that cannot allocate device memory.  The pages have no
+ * counterpart: it exists for callers that must not call cudaMalloc, such as a
+ * framework whose caching allocator owns (and accounts for) all device memory,
+ * or a host path that cannot absorb cudaMalloc's implicit synchronisation.
+ * It needs no context and no plan object and allocates nothing.
+ *   cfg          as for moonep_ctx_create (H and num_sms are not used)
+ *   topk, tpe    as for moonep_plan
+ *   dst[R,S*K], experts_to_copy[R,B], cu_seqlens[R,E+B],
+ *   zero_fill_ranges[R,E+B,2], remote_stats[R,2], dup_counts[R,2]
+ *                caller-allocated device outputs, same contents as the
+ *                fields of the same name that moonep_plan writes
+ *   status       caller-allocated device int32: cleared by the call, then set
+ *                to the first MOONEP_ERR_* a kernel meets (0 if none)
+ * The planner's intermediate tables live in one file-scope device array of
+ * 4 MiB (1 << 20 int32 words) that every GPU loading the library keeps until
+ * the process exits; configurations whose tables do not fit (roughly
+ * E*R*ceil(S*K/2048) + R*S*K + a few tables of E+B words) are rejected with
+ * MOONEP_ERR_INVALID_ARG.  The first call on a device looks up that array's
+ * device address and sets kernel attributes, so make it before any stream
+ * capture.  All calls share the array and a call overwrites what the last
+ * one left there: calls that overlap on the GPU (on different streams, or
+ * from several host threads without ordering) race and give wrong plans.
+ * The plan it produces feeds no other entry point (they take a
+ * moonep_comm_plan). */
+int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk,
+                        const int32_t *tpe, int32_t *dst,
+                        int32_t *experts_to_copy, int32_t *cu_seqlens,
+                        int32_t *zero_fill_ranges, int32_t *remote_stats,
+                        int32_t *dup_counts, int32_t *status, void *stream);
+
 /* Fused-permute dispatch [API, Buffer.dispatch; README item 3].
  *   hidden      [R, S, H] bf16 source rows
  *   w_sk        [R, S, K] fp32 route weights, or NULL
