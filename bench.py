@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep-steps", type=int, default=30)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--hp", type=int, default=None, help="override H' (profiling case)")
     ap.add_argument("--profile-op", default=None,
                     help="comma list of ops (plan,dispatch,combine,prefetch,reduce): "
                          "allocate only what they need and run each --steps times "
@@ -392,12 +393,15 @@ def workload_config(sh, point):
 
 
 def profile_ops(args, sh, point, seed):
-    """Run only the named ops with minimal allocations (profiling case)."""
+    """Run only the named ops, allocating only what they need (profiling case)."""
+    import dataclasses
     import torch
     from combine_moonep_plan_gb300 import workloads as wl
     from combine_moonep_plan_gb300.api import Buffer
     from combine_moonep_plan_gb300.build import build
     build()
+    if args.hp:
+        sh = dataclasses.replace(sh, Hp=args.hp)
     ops = args.profile_op.split(",")
     R, S, K, E, H, B, Hp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.Hp
     topk_np, info = make_routing(sh, point, seed)
@@ -406,39 +410,44 @@ def profile_ops(args, sh, point, seed):
     dev = "cuda"
     topk = torch.from_numpy(topk_np).to(dev)
     plan = buf.plan(topk)
-    x = torch.randn((R, S, H), device=dev).to(torch.bfloat16)
-    w = torch.from_numpy(wl.route_weights(sh, seed)).to(dev)
-    y = torch.empty((R * buf.NvS, H), dtype=torch.bfloat16, device=dev)
-    wn = torch.empty((R * buf.NvS,), dtype=torch.float32, device=dev)
-    buf.dispatch(x, w, plan=plan, out=y, weights_out=wn)
-    W = Gh = Gs = None
+    t = {}
+    if {"dispatch", "combine"} & set(ops):
+        t["x"] = torch.randn((R, S, H), device=dev).to(torch.bfloat16)
+        t["w"] = torch.from_numpy(wl.route_weights(sh, seed)).to(dev)
+        t["y"] = torch.empty((R * buf.NvS, H), dtype=torch.bfloat16, device=dev)
+        t["wn"] = torch.empty((R * buf.NvS,), dtype=torch.float32, device=dev)
+        buf.dispatch(t["x"], t["w"], plan=plan, out=t["y"], weights_out=t["wn"])
+        t["out"] = torch.empty((R, S, H), dtype=torch.bfloat16, device=dev)
+        t["wb"] = torch.empty((R, S, K), dtype=torch.float32, device=dev)
     if "prefetch" in ops:
-        W = torch.randn((E + R * B, H, Hp), device=dev).to(torch.bfloat16)
+        t["W"] = torch.randn((E + R * B, H, Hp), device=dev).to(torch.bfloat16)
     if "reduce" in ops:
-        Gh = torch.randn((E, H, Hp), device=dev)
-        Gs = torch.randn((R, B, H, Hp), device=dev)
-    out = torch.empty((R, S, H), dtype=torch.bfloat16, device=dev)
-    wb = torch.empty((R, S, K), dtype=torch.float32, device=dev)
+        t["Gh"] = torch.randn((E, H, Hp), device=dev)
+        t["Gs"] = torch.randn((R, B, H, Hp), device=dev)
     run = {"plan": lambda: buf.plan(topk, plan=plan),
-           "dispatch": lambda: buf.dispatch(x, w, plan=plan, out=y, weights_out=wn),
-           "combine": lambda: buf.combine(plan, y, wn, out=out, weights_out=wb),
-           "prefetch": lambda: buf.prefetch_weight(plan, W),
-           "reduce": lambda: buf.reduce_grad(plan, [Gh], [Gs])}
+           "dispatch": lambda: buf.dispatch(t["x"], t["w"], plan=plan, out=t["y"],
+                                            weights_out=t["wn"]),
+           "combine": lambda: buf.combine(plan, t["y"], t["wn"], out=t["out"],
+                                          weights_out=t["wb"]),
+           "prefetch": lambda: buf.prefetch_weight(plan, t["W"]),
+           "reduce": lambda: buf.reduce_grad(plan, [t["Gh"]], [t["Gs"]])}
     res = {}
     for op in ops:
         for _ in range(2):
             run[op]()
         torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record()
         for _ in range(args.steps):
             run[op]()
-        b.record()
+        ev1.record()
         torch.cuda.synchronize()
-        res[op] = a.elapsed_time(b) / args.steps
-    print(json.dumps({"profile_case": sh.name, "maxvio": info["maxvio"], "ms": res,
-                      "status": buf.get_status()}), flush=True)
+        res[op] = ev0.elapsed_time(ev1) / args.steps
+    etc = plan.experts_to_copy.cpu().numpy()
+    print(json.dumps({"profile_case": sh.name, "Hp": Hp, "maxvio": info["maxvio"], "ms": res,
+                      "slots_used": int((etc >= 0).sum()), "status": buf.get_status()}),
+          flush=True)
 
 
 def main():

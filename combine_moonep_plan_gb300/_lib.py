@@ -21,6 +21,7 @@ ERR_CUDA = -5
 ERR_DESTROYED = -6
 ERR_PLAN = -7
 ERR_NOMEM = -8
+ERR_TIMEOUT = -9
 PLAN_DUP_RECORDS = 1
 
 #: every symbol include/moonep.h declares

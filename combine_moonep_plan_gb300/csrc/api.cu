@@ -50,8 +50,9 @@ static int validate(const moonep_config *c) {
 
 static size_t scratch_bytes_of(const moonep_config &c) {
   const int64_t C = (int64_t)c.S * c.K;
-  const int64_t tpr = (C + kTile - 1) / kTile;
-  return (size_t)(c.E * c.R * tpr + c.R * C) * sizeof(int32_t) + 256;
+  // planner tiles of either path: at most R * ceil(S*K / 1024)
+  const int64_t tiles = (int64_t)c.R * ((C + 1023) / 1024 > 0 ? (C + 1023) / 1024 : 1);
+  return (size_t)(c.E * (tiles + 2 * c.R) + c.R * C) * sizeof(int32_t) + 512;
 }
 
 }  // namespace moonep
@@ -88,6 +89,7 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
     return MOONEP_ERR_CUDA;
   }
   ctx->sms = (c.num_sms > 0 && c.num_sms < sms) ? c.num_sms : sms;
+  ctx->sms_device = sms;
   ctx->L = c.E / c.R;
   ctx->C = c.S * c.K;
   ctx->EB = c.E + c.B;
@@ -97,20 +99,30 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
   ctx->blocks_dispatch = occupancy_dispatch(c.K);
   ctx->blocks_combine = occupancy_combine(c.K);
   ctx->blocks_copy = occupancy_copy();
-  const size_t hist = (size_t)c.E * ctx->G * sizeof(int32_t);
+  ctx->blocks_reduce = occupancy_reduce();
+  const size_t hist =
+      (size_t)c.E * (plan_hist_tiles(c.R, ctx->C, ctx->sms_device) + 2 * c.R) * sizeof(int32_t);
   const size_t ord = (size_t)c.R * ctx->C * sizeof(int32_t);
   e = cudaMalloc(&ctx->d_status, 256);
   if (e == cudaSuccess) e = cudaMemset(ctx->d_status, 0, 256);
+  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_sync, 2 * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_sync, 0, 2 * sizeof(unsigned long long));
   if (e == cudaSuccess && hist) e = cudaMalloc(&ctx->d_hist, hist);
+  if (e == cudaSuccess && hist) e = cudaMemset(ctx->d_hist, 0, hist);
   if (e == cudaSuccess && ord) e = cudaMalloc(&ctx->d_ord, ord);
   if (e == cudaSuccess && alloc_views) {
     const size_t rows = (size_t)c.R * ctx->NvS;
     e = cudaMalloc(&ctx->d_hidden_view, rows * c.H * sizeof(uint16_t) + 16);
     if (e == cudaSuccess) e = cudaMalloc(&ctx->d_weight_view, rows * sizeof(float) + 16);
   }
-  if (e == cudaSuccess) e = plan_configure(c.R, c.E);
+  if (e == cudaSuccess) e = plan_configure(c.R, c.E, c.B);
+  {
+    const char *t = getenv("MOONEP_TEST_UNPUBLISHED_PLAN");
+    ctx->test_unpublished_plan = (t && t[0] == '1') ? 1 : 0;
+  }
   if (e != cudaSuccess) {
     cudaFree(ctx->d_status);
+    cudaFree(ctx->d_sync);
     cudaFree(ctx->d_hist);
     cudaFree(ctx->d_ord);
     cudaFree(ctx->d_hidden_view);
@@ -127,6 +139,8 @@ int moonep_ctx_destroy(moonep_ctx *ctx) {
   if (!ctx || ctx->destroyed) return MOONEP_OK;
   cudaError_t e = cudaDeviceSynchronize();
   cudaFree(ctx->d_status);
+  cudaFree(ctx->d_sync);
+  ctx->d_sync = nullptr;
   cudaFree(ctx->d_hist);
   cudaFree(ctx->d_ord);
   cudaFree(ctx->d_hidden_view);
@@ -324,6 +338,7 @@ const char *moonep_strerror(int code) {
     case MOONEP_ERR_DESTROYED: return "context destroyed";
     case MOONEP_ERR_PLAN: return "plan row outside the dispatched buffer";
     case MOONEP_ERR_NOMEM: return "device allocation failed";
+    case MOONEP_ERR_TIMEOUT: return "a planner block gave up waiting for the balance step";
     default: return "unknown status";
   }
 }

@@ -71,12 +71,18 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Args a) {
   const int64_t nw = ((int64_t)gridDim.x * kThreads) >> 5;
   const int K = KT > 0 ? KT : a.K;
   const int64_t units = a.ntok * a.nchunk;
+  // The next unit's dst entries are loaded one unit ahead, so their latency
+  // overlaps the current unit's row loads.
+  int32_t d_next = 0;
+  if (wid < units && lane < K) d_next = __ldg(a.dst + (wid / a.nchunk) * K + lane);
   for (int64_t u = wid; u < units; u += nw) {
     const int64_t t = u / a.nchunk;
     const int c = (int)(u - t * a.nchunk);
+    const int32_t d_cur = d_next;
+    if (u + nw < units && lane < K) d_next = __ldg(a.dst + ((u + nw) / a.nchunk) * K + lane);
     int64_t g = 0;
     if (lane < K) {
-      g = decode_row(__ldg(a.dst + t * K + lane));
+      g = decode_row(d_cur);
       if (g >= a.total_rows) {
         set_status(a.status, MOONEP_ERR_PLAN);
         g = 0;

@@ -47,13 +47,19 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
   const int64_t tok_units = a.ntok * a.nchunk;
   const int64_t P = a.meta[kMetaP];
   const int64_t units = tok_units + P * a.nchunk;
+  // The next token unit's dst entries are loaded one unit ahead.
+  int32_t d_next = 0;
+  if (wid < tok_units && lane < K) d_next = __ldg(a.dst + (wid / a.nchunk) * K + lane);
   for (int64_t u = wid; u < units; u += nw) {
     if (u < tok_units) {
       const int64_t t = u / a.nchunk;
       const int c = (int)(u - t * a.nchunk);
+      const int32_t d_cur = d_next;
+      if (u + nw < tok_units && lane < K)
+        d_next = __ldg(a.dst + ((u + nw) / a.nchunk) * K + lane);
       int64_t g = -1;
       if (lane < K) {
-        const int64_t gg = decode_row(__ldg(a.dst + t * K + lane));
+        const int64_t gg = decode_row(d_cur);
         if (gg < a.total_rows) {
           g = gg;
         } else {

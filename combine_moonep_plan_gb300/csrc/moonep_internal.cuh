@@ -32,7 +32,7 @@ enum {
 // Word offsets of the tables inside plan->internal (see PlanLayout::make).
 struct PlanLayout {
   int64_t qoff, T, home_rowbase, keep, piece_first, piece_count, piece_start,
-      piece_len, piece_recv, slot_rowbase, slot_b, nseg, pad_prefix, copy_slot,
+      piece_len, piece_recv, slot_rowbase, slot_b, nseg, padw, pad_prefix, copy_slot,
       copy_expert, red_expert, red_first, red_slot, dupflag, total;
   static PlanLayout make(int R, int E, int B, int NvS, bool dup_records) {
     PlanLayout l;
@@ -51,6 +51,7 @@ struct PlanLayout {
     l.slot_rowbase = take((int64_t)R * L);
     l.slot_b = take((int64_t)R * L);
     l.nseg = take((int64_t)R * EB);
+    l.padw = take((int64_t)R * EB);
     l.pad_prefix = take((int64_t)R * EB + 1);
     l.copy_slot = take((int64_t)R * B);
     l.copy_expert = take((int64_t)R * B);
@@ -69,14 +70,17 @@ struct moonep_ctx {
   moonep_config cfg;
   int device;
   int sms;         // SMs the copy kernels may use
+  int sms_device;  // SMs of the device
   int L, C, EB, NvS, TPR, G;  // E/R, S*K, E+B, rows per rank, tiles per rank, R*TPR
   int destroyed;
   int32_t *d_status;   // sticky first error
-  int32_t *d_hist;     // [E, G] tile histograms -> exclusive tile offsets
+  int32_t *d_hist;     // tile histograms, then [R, E] totals and [R, E] rank starts
   int32_t *d_ord;      // [R*C] ordinal of a route among its tile's routes to the same expert
   uint16_t *d_hidden_view;  // optional [R*NvS, H] bf16
   float *d_weight_view;     // optional [R*NvS] fp32
-  int blocks_dispatch, blocks_combine, blocks_copy;  // resident blocks per SM
+  unsigned long long *d_sync;  // [2] planner arrival counter, published target
+  int test_unpublished_plan;   // test hook: the planner's balance block never publishes
+  int blocks_dispatch, blocks_combine, blocks_copy, blocks_reduce;  // resident blocks per SM
 };
 
 namespace moonep {
@@ -98,10 +102,15 @@ int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj,
 int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, float *const *Gh,
                   float *const *Gs, int64_t HHp, cudaStream_t st);
 // Opt the planner kernels into the dynamic shared memory E experts need.
-cudaError_t plan_configure(int R, int E);
+cudaError_t plan_configure(int R, int E, int B);
+// K when the single-launch planner handles this shape (0: the tile path).
+int plan_fused_choice(int R, int E, int K, int B, int C, int sms, bool *nseg_shared);
+// Tiles the histogram area must hold (either planner path).
+int plan_hist_tiles(int R, int C, int sms);
 int occupancy_dispatch(int K);
 int occupancy_combine(int K);
 int occupancy_copy();
+int occupancy_reduce();
 
 // Latch the first error code into the status word.
 __device__ __forceinline__ void set_status(int32_t *status, int code) {

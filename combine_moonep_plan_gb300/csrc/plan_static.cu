@@ -32,7 +32,7 @@ int64_t round_words(int64_t w) { return (w + 63) / 64 * 64; }
 // Once per device, with that device current: the device address of the
 // scratch array (the host-side symbol is only a stand-in, not a device
 // address) and the planner kernels' shared-memory limits.
-int setup(int device, int R, int E, int32_t **scratch) {
+int setup(int device, int R, int E, int B, int32_t **scratch) {
   if (device < 0 || device >= kMaxDevices) return MOONEP_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (!g_scratch_addr[device]) {
@@ -45,7 +45,7 @@ int setup(int device, int R, int E, int32_t **scratch) {
     g_scratch_addr[device] = static_cast<int32_t *>(ptr);
   }
   if (E > g_scratch_E[device]) {
-    if (plan_configure(R, E) != cudaSuccess) {
+    if (plan_configure(R, E, B) != cudaSuccess) {
       cudaGetLastError();
       return MOONEP_ERR_CUDA;
     }
@@ -79,24 +79,36 @@ extern "C" int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk
       !remote_stats || !dup_counts || (C > 0 && (!topk || !dst)))
     return MOONEP_ERR_INVALID_ARG;
 
-  // scratch: tile histograms [E, R*tiles], ordinals [R*S*K], plan tables
-  const int64_t tpr = (C + kTile - 1) / kTile;
-  const int64_t hist_words = round_words((int64_t)c.E * c.R * tpr);
-  const int64_t ord_words = round_words((int64_t)c.R * C);
-  const PlanLayout lay = PlanLayout::make(c.R, c.E, c.B, (int)nvs, false);
-  if (hist_words + ord_words + lay.total > kNoAllocScratchWords) return MOONEP_ERR_INVALID_ARG;
-
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess) {
+  int device = 0, sms = 0;
+  if (cudaGetDevice(&device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
     cudaGetLastError();
     return MOONEP_ERR_CUDA;
   }
+  // scratch: planner sync words, histograms of either planner path
+  // [E, tiles] plus [R, E] totals and [R, E] rank starts, ordinals [R*S*K],
+  // plan tables
+  const int64_t tpr = (C + kTile - 1) / kTile;
+  const int64_t sync_words = 64;
+  const int64_t hist_tiles = plan_hist_tiles(c.R, (int)C, sms);
+  const int64_t hist_words = round_words((int64_t)c.E * (hist_tiles + 2 * c.R));
+  const int64_t ord_words = round_words((int64_t)c.R * C);
+  const PlanLayout lay = PlanLayout::make(c.R, c.E, c.B, (int)nvs, false);
+  if (sync_words + hist_words + ord_words + lay.total > kNoAllocScratchWords)
+    return MOONEP_ERR_INVALID_ARG;
+
   int32_t *scratch = nullptr;
-  int st = setup(device, c.R, c.E, &scratch);
+  int st = setup(device, c.R, c.E, c.B, &scratch);
   if (st) return st;
 
   cudaStream_t s = (cudaStream_t)stream;
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return MOONEP_ERR_CUDA;
+  // The planner's arrival counters, per-rank totals and error word must start
+  // at zero: clear them on every call.
+  if (cudaMemsetAsync(scratch, 0, sync_words * sizeof(int32_t), s) != cudaSuccess ||
+      cudaMemsetAsync(scratch + sync_words + (int64_t)c.E * hist_tiles, 0,
+                      (size_t)c.R * c.E * sizeof(int32_t), s) != cudaSuccess)
+    return MOONEP_ERR_CUDA;
 
   // A context and a plan that only point: no member owns memory.
   moonep_ctx ctx{};
@@ -107,10 +119,12 @@ extern "C" int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk
   ctx.EB = c.E + c.B;
   ctx.NvS = (int)nvs;
   ctx.TPR = (int)tpr;
+  ctx.sms = ctx.sms_device = sms;
   ctx.G = (int)(c.R * tpr);
   ctx.d_status = status;
-  ctx.d_hist = scratch;
-  ctx.d_ord = scratch + hist_words;
+  ctx.d_sync = reinterpret_cast<unsigned long long *>(scratch);
+  ctx.d_hist = scratch + sync_words;
+  ctx.d_ord = scratch + sync_words + hist_words;
   moonep_comm_plan plan{};
   plan.dst = dst;
   plan.experts_to_copy = experts_to_copy;
@@ -118,7 +132,7 @@ extern "C" int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk
   plan.zero_fill_ranges = zero_fill_ranges;
   plan.remote_stats = remote_stats;
   plan.dup_counts = dup_counts;
-  plan.internal = scratch + hist_words + ord_words;
+  plan.internal = scratch + sync_words + hist_words + ord_words;
   plan.internal_bytes = lay.total * sizeof(int32_t);
   plan.N = (int)C;
   plan.R = c.R;
@@ -128,5 +142,7 @@ extern "C" int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk
   plan.S = c.S;
   plan.NvS = plan.NvS_padded = (int)nvs;
   plan.flags = 0;
+  if (cudaMemsetAsync(plan.internal, 0, kMetaWords * sizeof(int32_t), s) != cudaSuccess)
+    return MOONEP_ERR_CUDA;
   return launch_plan(&ctx, topk, tpe, &plan, s);
 }

@@ -25,7 +25,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxProj = 4;
 constexpr int kChunkVec = 4096;  // 16-byte vectors per unit (64 KB)
-constexpr int kPU = 4;           // vectors per thread per step
+constexpr int kPU = 4;           // vectors per thread per step (prefetch)
+constexpr int kRV = 4;           // vectors per thread per round (reduce)
 
 struct PrefetchArgs {
   uint4 *W[kMaxProj];
@@ -87,44 +88,32 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
     float4 *slots = a.Gs[p];
     const int64_t v_begin = c * kChunkVec;
     const int64_t v_end = min(v_begin + kChunkVec, a.vec_per_row);
-    // Two vectors per thread, up to four slot rows loaded before they are
-    // added, so several loads are in flight; adds stay in slot-list order.
-    for (int64_t v = v_begin + threadIdx.x; v < v_end; v += 2 * kThreads) {
-      float4 acc[2];
-      bool ok[2];
+    // kRV vectors per thread in flight per round: the home row, then each
+    // slot row in list order (the adds stay in (rank, slot) order).
+    for (int64_t v = v_begin + threadIdx.x; v < v_end; v += kRV * kThreads) {
+      float4 acc[kRV];
 #pragma unroll
-      for (int i = 0; i < 2; i++) {
-        ok[i] = v + i * kThreads < v_end;
-        if (ok[i]) acc[i] = ld_once_f4(home + v + i * kThreads);
-      }
-      for (int f = f0; f < f1; f += 4) {
-        float4 x[4][2];
+      for (int i = 0; i < kRV; i++)
+        if (v + i * kThreads < v_end) acc[i] = ld_once_f4(home + v + i * kThreads);
+      for (int f = f0; f < f1; f++) {
+        float4 *sp = slots + (int64_t)a.red_slot[f] * a.vec_per_row + v;
+        float4 x[kRV];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-          if (f + q >= f1) break;
-          const float4 *sp = slots + (int64_t)a.red_slot[f + q] * a.vec_per_row + v;
+        for (int i = 0; i < kRV; i++)
+          if (v + i * kThreads < v_end) x[i] = ld_once_f4(sp + i * kThreads);
 #pragma unroll
-          for (int i = 0; i < 2; i++)
-            if (ok[i]) x[q][i] = ld_once_f4(sp + i * kThreads);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-          if (f + q >= f1) break;
-          float4 *sp = slots + (int64_t)a.red_slot[f + q] * a.vec_per_row + v;
-#pragma unroll
-          for (int i = 0; i < 2; i++) {
-            if (!ok[i]) continue;
-            acc[i].x = acc[i].x + x[q][i].x;
-            acc[i].y = acc[i].y + x[q][i].y;
-            acc[i].z = acc[i].z + x[q][i].z;
-            acc[i].w = acc[i].w + x[q][i].w;
-            st_global_f4(sp + i * kThreads, zero);
-          }
+        for (int i = 0; i < kRV; i++) {
+          if (v + i * kThreads >= v_end) continue;
+          acc[i].x = acc[i].x + x[i].x;
+          acc[i].y = acc[i].y + x[i].y;
+          acc[i].z = acc[i].z + x[i].z;
+          acc[i].w = acc[i].w + x[i].w;
+          st_global_f4(sp + i * kThreads, zero);
         }
       }
 #pragma unroll
-      for (int i = 0; i < 2; i++)
-        if (ok[i]) st_global_f4(home + v + i * kThreads, acc[i]);
+      for (int i = 0; i < kRV; i++)
+        if (v + i * kThreads < v_end) st_global_f4(home + v + i * kThreads, acc[i]);
     }
   }
 }
@@ -134,6 +123,14 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
 int occupancy_copy() {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefetch_kernel, kThreads, 0) !=
+      cudaSuccess)
+    n = 1;
+  return n > 0 ? n : 1;
+}
+
+int occupancy_reduce() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reduce_kernel, kThreads, 0) !=
       cudaSuccess)
     n = 1;
   return n > 0 ? n : 1;
@@ -179,8 +176,7 @@ int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, flo
   a.vec_per_row = HHp / 4;
   a.nchunk = (a.vec_per_row + kChunkVec - 1) / kChunkVec;
   if (a.vec_per_row == 0 || c.B == 0) return MOONEP_OK;
-  const int grid = ctx->sms * ctx->blocks_copy;
-  reduce_kernel<<<grid, kThreads, 0, st>>>(a);
+  reduce_kernel<<<ctx->sms * ctx->blocks_reduce, kThreads, 0, st>>>(a);
   return cuda_status(cudaGetLastError());
 }
 

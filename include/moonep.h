@@ -55,6 +55,7 @@ extern "C" {
 #define MOONEP_ERR_DESTROYED (-6)     /* context already destroyed (host) */
 #define MOONEP_ERR_PLAN (-7)          /* plan row outside [0, R*NvS) (device) */
 #define MOONEP_ERR_NOMEM (-8)         /* device allocation failed (host) */
+#define MOONEP_ERR_TIMEOUT (-9)       /* a planner block gave up waiting (device) */
 
 /* Constructor controls [API, Buffer(...)]: E % R == 0; B prefetch slots per
  * rank (B = E/R is what training needs [README, How to set B]; smaller B is

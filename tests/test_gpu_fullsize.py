@@ -1,0 +1,156 @@
+"""Parity at the five workload shapes' full sizes, in the launch configuration
+bench.py uses.
+
+* the plan is compared with the oracle's bit for bit (every field);
+* dispatch is checked in full on the device as the scatter it is (every
+  route's row equals its token's row, every padding row and weight is zero,
+  every route weight lands), and against the oracle on sampled tokens;
+* combine is checked against the oracle on sampled tokens (the oracle computes
+  them one by one from the gathered rows) and, in full, by the closed form
+  combine(dispatch(x)) = K*x;
+* prefetch in full (every used slot equals its home row, unused slots keep
+  their checksum); gradient reduce against the oracle on sampled columns.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moonep_plan_gb300 import workloads as wl
+from tests.plan_checks import decode
+
+pytestmark = pytest.mark.gpu
+
+POINTS = [("tiny", "zipf1.2"), ("mixtral", 1.0), ("mixtral", 3.0), ("deepseek_v3", 2.0),
+          ("deepseek_v3", 0.0), ("kimi_k2", "hot30"), ("qwen3_decode", "zipf1")]
+
+
+def _routing(sh, point, seed):
+    if point == "hot30":
+        return wl.routing(sh, "hot", hot_share=0.30, seed=seed)[0]
+    if point == "zipf1":
+        return wl.routing(sh, "zipf", zipf_s=1.0, seed=seed)[0]
+    if point == "zipf1.2":
+        return wl.routing(sh, "zipf", zipf_s=1.2, seed=seed)[0]
+    if point == 0.0:
+        return wl.routing(sh, "exact0", seed=seed)[0]
+    return wl.routing(sh, "zipf", target_maxvio=float(point), seed=seed)[0]
+
+
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from combine_moonep_plan_gb300 import build
+    build.build()
+    yield
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,point", POINTS, ids=[f"{n}-{p}" for n, p in POINTS])
+def test_full_size_parity(name, point):
+    from combine_moonep_plan_gb300.api import Buffer
+    sh = wl.SHAPES[name]
+    R, S, K, E, H, Hp, B, tp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.Hp, sh.B, sh.tp
+    seed = wl.seed_for(name, 7)
+    topk = _routing(sh, point, seed)
+    tpe = wl.tokens_per_expert(topk, E)
+    st, op = oracle.plan(R, E, K, S, B, tp, topk, tpe, dup_records=False)
+    assert st == 0
+    NvS = op["NvS"]
+
+    buf = Buffer(S=S, H=H, K=K, E=E, num_ep_ranks=R, B=B, token_padding=tp,
+                 zero_copy_views=False)
+    dev = "cuda"
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    x = torch.randn((R, S, H), generator=g, device=dev).to(torch.bfloat16)
+    w = torch.from_numpy(wl.route_weights(sh, seed)).to(dev)
+    out = torch.full((R * NvS, H), float("nan"), dtype=torch.bfloat16, device=dev)
+    wout = torch.full((R * NvS,), float("nan"), dtype=torch.float32, device=dev)
+    hid, wn, cu, plan = buf.dispatch(x, w, torch.from_numpy(topk).to(dev),
+                                     torch.from_numpy(tpe).to(dev), out=out, weights_out=wout)
+    assert buf.get_status() == 0
+
+    # plan: bit-exact with the oracle
+    for f in ("dst", "experts_to_copy", "cu_seqlens", "zero_fill_ranges", "remote_stats",
+              "dup_counts"):
+        assert np.array_equal(getattr(plan, f).cpu().numpy(), op[f]), f
+
+    # dispatch: the full scatter, on the device
+    gidx = torch.from_numpy(decode(op["dst"]).reshape(-1)).to(dev)
+    tok = torch.arange(R * S, device=dev).repeat_interleave(K)
+    xf = x.reshape(R * S, H)
+    for c0 in range(0, gidx.numel(), 1 << 16):
+        c1 = c0 + (1 << 16)
+        assert torch.equal(hid[gidx[c0:c1]].view(torch.int16), xf[tok[c0:c1]].view(torch.int16))
+    assert torch.equal(wn[gidx].view(torch.int32), w.reshape(-1).view(torch.int32))
+    zfr = op["zero_fill_ranges"]
+    pad = np.concatenate([np.arange(j * NvS + a, j * NvS + b) for j in range(R)
+                          for a, b in zfr[j] if b > a] or [np.zeros(0, np.int64)])
+    if len(pad):
+        pt = torch.from_numpy(pad).to(dev)
+        assert torch.all(hid[pt].view(torch.int16) == 0)
+        assert torch.all(wn[pt].view(torch.int32) == 0)
+    # sampled tokens against the oracle's dispatch of those tokens' rows
+    rng = np.random.default_rng(seed)
+    toks = np.unique(rng.integers(0, R * S, 256))
+    rows = decode(op["dst"]).reshape(R * S, K)[toks]
+    got = _bits(hid[torch.from_numpy(rows.reshape(-1)).to(dev)]).reshape(len(toks), K, H)
+    xs = _bits(xf[torch.from_numpy(toks).to(dev)])
+    sub_dst = np.arange(len(toks) * K, dtype=np.int32).reshape(1, -1)
+    want = oracle.dispatch(1, len(toks), K, 0, 0, len(toks) * K, H, sub_dst,
+                           np.zeros((1, 0, 2), np.int32), xs)
+    assert np.array_equal(got.reshape(-1, H), want)
+
+    # combine: sampled tokens via the oracle, plus the closed form in full
+    y = torch.randn((R * NvS, H), generator=g, device=dev).to(torch.bfloat16)
+    cout, cw = buf.combine(plan, y, wn)
+    assert buf.get_status() == 0
+    ysub = _bits(y[torch.from_numpy(rows.reshape(-1)).to(dev)])
+    want, _ = oracle.combine(1, len(toks), K, len(toks) * K, H,
+                             np.arange(len(toks) * K, dtype=np.int32), ysub)
+    assert np.array_equal(_bits(cout.reshape(R * S, H)[torch.from_numpy(toks).to(dev)]), want)
+    assert torch.equal(cw.reshape(-1).view(torch.int32), w.reshape(-1).view(torch.int32))
+    if K & (K - 1) == 0:
+        ident, _ = buf.combine(plan, hid)
+        assert torch.equal(ident.float(), x.float() * K)
+    del y, out, wout, cout, cw, hid, wn, x
+
+    # prefetch: every used slot equals its home row; unused slots untouched
+    etc = op["experts_to_copy"]
+    W = torch.randn((E + R * B, H, Hp), generator=g, device=dev).to(torch.bfloat16)
+    W32 = W.view(E + R * B, -1).view(torch.int32)
+
+    def checksums():
+        return torch.stack([W32[i].to(torch.int64).sum() for i in range(E + R * B)]).cpu()
+    before = checksums()
+    buf.prefetch_weight(plan, W)
+    after = checksums()
+    for j in range(R):
+        for b in range(B):
+            row = E + j * B + b
+            if etc[j, b] >= 0:
+                assert torch.equal(W[row].view(torch.int16), W[etc[j, b]].view(torch.int16))
+            else:
+                assert before[row] == after[row]
+    del W, W32
+
+    # gradient reduce: sampled column windows against the oracle
+    HHp = H * Hp
+    Gh = torch.randn((E, H, Hp), generator=g, device=dev)
+    Gs = torch.randn((R, B, H, Hp), generator=g, device=dev)
+    wins = [(0, 4096), (HHp // 2 - 2048, HHp // 2 + 2048), (HHp - 4096, HHp)]
+    gh0 = [Gh.view(E, -1)[:, a:b].cpu().numpy().copy() for a, b in wins]
+    gs0 = [Gs.view(R * B, -1)[:, a:b].cpu().numpy().copy() for a, b in wins]
+    buf.reduce_grad(plan, [Gh], [Gs])
+    assert buf.get_status() == 0
+    for (a, b), gh, gs in zip(wins, gh0, gs0):
+        oracle.reduce(R, E, B, etc.reshape(-1), gh, gs, b - a)
+        assert np.array_equal(Gh.view(E, -1)[:, a:b].cpu().numpy().view(np.uint32),
+                              gh.view(np.uint32))
+        assert np.array_equal(Gs.view(R * B, -1)[:, a:b].cpu().numpy().view(np.uint32),
+                              gs.view(np.uint32))
+    buf.destroy()

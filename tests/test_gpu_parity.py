@@ -357,3 +357,24 @@ def test_destroy_is_idempotent():
     assert buf.destroyed
     with pytest.raises(_lib.MoonepError):
         buf.plan(torch.zeros((2, 8, 2), dtype=torch.int32, device="cuda"))
+
+
+def test_planner_wait_limit_reports_timeout(monkeypatch):
+    """The planner's blocks wait for the balance step with a time limit.  A
+    test hook stops the balance block from publishing; the waiting blocks must
+    give up, latch MOONEP_ERR_TIMEOUT and leave a plan every later kernel can
+    still consume without leaving its buffers."""
+    from combine_moonep_plan_gb300 import _lib
+    monkeypatch.setenv("MOONEP_TEST_UNPUBLISHED_PLAN", "1")
+    sh = wl.SHAPES["tiny"]
+    buf = _buffer(_cfg_of(sh), H=sh.H)
+    monkeypatch.delenv("MOONEP_TEST_UNPUBLISHED_PLAN")
+    topk = _routing(sh, "zipf", 8)
+    x = torch.randn(sh.R, sh.S, sh.H, device="cuda").bfloat16()
+    _, _, _, plan = buf.dispatch(x, None, torch.from_numpy(topk).cuda())
+    buf.combine(plan, buf.hidden_nvsh_buffer_view())
+    assert buf.get_status() == _lib.ERR_TIMEOUT
+    g = decode(plan.dst.cpu().numpy())
+    assert g.min() >= 0 and g.max() < sh.R * buf.NvS
+    # a context created without the hook plans normally
+    _full_pipeline(sh, topk, 8)
