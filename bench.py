@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--sweep-steps", type=int, default=30)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--hp", type=int, default=None, help="override H' (profiling case)")
+    ap.add_argument("--s", type=int, default=None, help="override S (profiling case)")
     ap.add_argument("--profile-op", default=None,
                     help="comma list of ops (plan,dispatch,combine,prefetch,reduce): "
                          "allocate only what they need and run each --steps times "
@@ -402,6 +403,8 @@ def profile_ops(args, sh, point, seed):
     build()
     if args.hp:
         sh = dataclasses.replace(sh, Hp=args.hp)
+    if args.s:
+        sh = dataclasses.replace(sh, S=args.s)
     ops = args.profile_op.split(",")
     R, S, K, E, H, B, Hp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.Hp
     topk_np, info = make_routing(sh, point, seed)

@@ -11,7 +11,10 @@
 // their primaries (to save link bytes between GPUs); on one GPU every row is
 // read directly, so there is a single rounding at the end.
 // Units of (token, chunk of 32*U 16-byte vectors) are strided over the warps
-// of a persistent grid; each lane keeps K*U 16-byte loads in flight.
+// of a persistent grid; each lane keeps K*U 16-byte loads in flight.  Every
+// unit reads 2 KB contiguous from each of its K rows: with K = 8 and 1 KB per
+// row the reads were scattered enough to hold HBM near 70 %; 2 KB per row (in
+// two batches of four rows, 128-thread blocks) reaches the copy bandwidth.
 // HBM bytes per call: read N*H*2 + N*4 (dst) [+ N*4 weights]; write
 // R*S*H*2 [+ N*4].
 #include "copy_common.cuh"
@@ -20,7 +23,6 @@
 namespace moonep {
 namespace {
 
-constexpr int kThreads = 256;
 
 struct Args {
   const uint4 *y;
@@ -64,11 +66,14 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 }
 
 // KT: compile-time K (0 = runtime K, up to 32).  U: vectors per lane per unit.
-template <int KT, int U>
-__global__ void __launch_bounds__(kThreads) combine_kernel(Args a) {
+// BT: threads per block (128 for K = 8, whose ~110 registers per thread leave
+// room for more resident warps in small blocks).  KB: rows loaded per batch
+// (K = 8 reads 2 KB of each row per unit, in two batches of four rows).
+template <int KT, int U, int BT, int KB>
+__global__ void __launch_bounds__(BT) combine_kernel(Args a) {
   const int lane = threadIdx.x & 31;
-  const int64_t wid = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const int64_t nw = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int64_t wid = ((int64_t)blockIdx.x * BT + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * BT) >> 5;
   const int K = KT > 0 ? KT : a.K;
   const int64_t units = a.ntok * a.nchunk;
   // The next unit's dst entries are loaded one unit ahead, so their latency
@@ -93,21 +98,26 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Args a) {
     float acc[U][8];
     if (KT > 0) {
       constexpr int KK = KT > 0 ? KT : 1;
-      uint4 x[KK][U];
 #pragma unroll
-      for (int k = 0; k < KK; k++) {
-        const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k) * a.H8;
+      for (int k0 = 0; k0 < KK; k0 += KB) {
+        uint4 x[KB][U];
+#pragma unroll
+        for (int kk = 0; kk < KB; kk++) {
+          const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k0 + kk) * a.H8;
+#pragma unroll
+          for (int i = 0; i < U; i++) {
+            const int v = v0 + 32 * i;
+            if (v < a.H8) x[kk][i] = ld_stream(row + v);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < U; i++) {
-          const int v = v0 + 32 * i;
-          if (v < a.H8) x[k][i] = ld_stream(row + v);
+#pragma unroll
+          for (int kk = 0; kk < KB; kk++) {
+            if (k0 + kk == 0) set_bf16x8(acc[i], x[kk][i]);
+            else add_bf16x8(acc[i], x[kk][i]);
+          }
         }
-      }
-#pragma unroll
-      for (int i = 0; i < U; i++) {
-        set_bf16x8(acc[i], x[0][i]);
-#pragma unroll
-        for (int k = 1; k < KK; k++) add_bf16x8(acc[i], x[k][i]);
       }
     } else {
       for (int k = 0; k < K; k++) {
@@ -130,19 +140,22 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Args a) {
   }
 }
 
-template <int KT, int U>
+template <int KT, int U, int BT, int KB>
 void launch(const Args &a, int grid, cudaStream_t st) {
-  combine_kernel<KT, U><<<grid, kThreads, 0, st>>>(a);
+  combine_kernel<KT, U, BT, KB><<<grid, BT, 0, st>>>(a);
 }
 
 }  // namespace
 
 int occupancy_combine(int K) {
   int n = 0;
-  void *f = K == 1 ? (void *)combine_kernel<1, 4> : K == 2 ? (void *)combine_kernel<2, 4>
-          : K == 4 ? (void *)combine_kernel<4, 4> : K == 8 ? (void *)combine_kernel<8, 2>
-          : (void *)combine_kernel<0, 2>;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess) n = 1;
+  void *f = K == 1 ? (void *)combine_kernel<1, 4, 256, 1>
+          : K == 2 ? (void *)combine_kernel<2, 4, 256, 2>
+          : K == 4 ? (void *)combine_kernel<4, 4, 256, 4>
+          : K == 8 ? (void *)combine_kernel<8, 4, 128, 4>
+                   : (void *)combine_kernel<0, 2, 256, 1>;
+  const int bt = K == 8 ? 128 : 256;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, bt, 0) != cudaSuccess) n = 1;
   return n > 0 ? n : 1;
 }
 
@@ -160,16 +173,16 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
   a.total_rows = (int64_t)c.R * ctx->NvS;
   a.K = c.K;
   a.H8 = c.H / 8;
-  const int U = (c.K == 1 || c.K == 2 || c.K == 4) ? 4 : 2;
+  const int U = (c.K == 1 || c.K == 2 || c.K == 4 || c.K == 8) ? 4 : 2;
   a.nchunk = (a.H8 + 32 * U - 1) / (32 * U);
   if (a.ntok == 0 || a.H8 == 0) return MOONEP_OK;
   const int grid = ctx->sms * ctx->blocks_combine;
   switch (c.K) {
-    case 1: launch<1, 4>(a, grid, st); break;
-    case 2: launch<2, 4>(a, grid, st); break;
-    case 4: launch<4, 4>(a, grid, st); break;
-    case 8: launch<8, 2>(a, grid, st); break;
-    default: launch<0, 2>(a, grid, st); break;
+    case 1: launch<1, 4, 256, 1>(a, grid, st); break;
+    case 2: launch<2, 4, 256, 2>(a, grid, st); break;
+    case 4: launch<4, 4, 256, 4>(a, grid, st); break;
+    case 8: launch<8, 4, 128, 4>(a, grid, st); break;
+    default: launch<0, 2, 256, 1>(a, grid, st); break;
   }
   return cuda_status(cudaGetLastError());
 }

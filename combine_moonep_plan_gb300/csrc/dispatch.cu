@@ -20,8 +20,8 @@ namespace moonep {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kU = 4;                  // 16-byte vectors per lane per unit
-constexpr int kChunk = 32 * kU;        // vectors per unit (2 KB)
+constexpr int kU = 8;                  // 16-byte vectors per lane per unit
+constexpr int kChunk = 32 * kU;        // vectors per unit (4 KB)
 
 struct Args {
   const uint4 *hidden;

@@ -26,7 +26,6 @@ constexpr int kThreads = 256;
 constexpr int kMaxProj = 4;
 constexpr int kChunkVec = 4096;  // 16-byte vectors per unit (64 KB)
 constexpr int kPU = 4;           // vectors per thread per step (prefetch)
-constexpr int kRV = 4;           // vectors per thread per round (reduce)
 
 struct PrefetchArgs {
   uint4 *W[kMaxProj];
@@ -72,7 +71,19 @@ struct ReduceArgs {
   int64_t nchunk;
 };
 
+constexpr int kRedChunk = 2048;  // float4 per unit (32 KB of the home row)
+constexpr int kRV = 2;           // float4 per thread per round
+constexpr int kNS = 7;           // slot rows loaded together with the home row
+constexpr int kMaxSlotsPerExpert = 256;
+
+// One unit = one 32 KB chunk of one expert's row (and of its slot rows).  A
+// thread loads the home element and up to kNS slot elements together, adds
+// them in slot-list order, zeroes the slot elements and stores the sum, so a
+// round trip to memory covers the whole column instead of one row at a time.
 __global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
+  __shared__ float4 *s_slot[kMaxSlotsPerExpert];
+  __shared__ float4 *s_home;
+  __shared__ int s_n;
   const int64_t D = a.meta[kMetaD];
   const int64_t per_proj = D * a.nchunk;
   const int64_t units = per_proj * a.n_proj;
@@ -82,38 +93,58 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
     const int64_t rem = unit - p * per_proj;
     const int64_t di = rem / a.nchunk;
     const int64_t c = rem - di * a.nchunk;
-    const int e = a.red_expert[di];
-    const int f0 = a.red_first[di], f1 = a.red_first[di + 1];
-    float4 *home = a.Gh[p] + (int64_t)e * a.vec_per_row;
-    float4 *slots = a.Gs[p];
-    const int64_t v_begin = c * kChunkVec;
-    const int64_t v_end = min(v_begin + kChunkVec, a.vec_per_row);
-    // kRV vectors per thread in flight per round: the home row, then each
-    // slot row in list order (the adds stay in (rank, slot) order).
+    __syncthreads();  // the previous unit is done with the shared pointers
+    if (threadIdx.x == 0) {
+      const int f0 = a.red_first[di], f1 = a.red_first[di + 1];
+      s_n = min(f1 - f0, kMaxSlotsPerExpert);
+      s_home = a.Gh[p] + (int64_t)a.red_expert[di] * a.vec_per_row;
+    }
+    {
+      const int f0 = a.red_first[di], f1 = a.red_first[di + 1];
+      for (int q = threadIdx.x; q < f1 - f0 && q < kMaxSlotsPerExpert; q += kThreads)
+        s_slot[q] = a.Gs[p] + (int64_t)a.red_slot[f0 + q] * a.vec_per_row;
+    }
+    __syncthreads();
+    const int n = s_n;
+    float4 *home = s_home;
+    const int64_t v_begin = c * kRedChunk;
+    const int64_t v_end = min(v_begin + kRedChunk, a.vec_per_row);
     for (int64_t v = v_begin + threadIdx.x; v < v_end; v += kRV * kThreads) {
+      bool ok[kRV];
       float4 acc[kRV];
 #pragma unroll
-      for (int i = 0; i < kRV; i++)
-        if (v + i * kThreads < v_end) acc[i] = ld_once_f4(home + v + i * kThreads);
-      for (int f = f0; f < f1; f++) {
-        float4 *sp = slots + (int64_t)a.red_slot[f] * a.vec_per_row + v;
-        float4 x[kRV];
+      for (int i = 0; i < kRV; i++) {
+        ok[i] = v + i * kThreads < v_end;
+        if (ok[i]) acc[i] = ld_once_f4(home + v + i * kThreads);
+      }
+      for (int f = 0; f < n; f += kNS) {
+        float4 x[kNS][kRV];
 #pragma unroll
-        for (int i = 0; i < kRV; i++)
-          if (v + i * kThreads < v_end) x[i] = ld_once_f4(sp + i * kThreads);
+        for (int q = 0; q < kNS; q++) {
+          if (f + q < n) {
 #pragma unroll
-        for (int i = 0; i < kRV; i++) {
-          if (v + i * kThreads >= v_end) continue;
-          acc[i].x = acc[i].x + x[i].x;
-          acc[i].y = acc[i].y + x[i].y;
-          acc[i].z = acc[i].z + x[i].z;
-          acc[i].w = acc[i].w + x[i].w;
-          st_global_f4(sp + i * kThreads, zero);
+            for (int i = 0; i < kRV; i++)
+              if (ok[i]) x[q][i] = ld_once_f4(s_slot[f + q] + v + i * kThreads);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kNS; q++) {
+          if (f + q < n) {
+#pragma unroll
+            for (int i = 0; i < kRV; i++) {
+              if (!ok[i]) continue;
+              acc[i].x = acc[i].x + x[q][i].x;
+              acc[i].y = acc[i].y + x[q][i].y;
+              acc[i].z = acc[i].z + x[q][i].z;
+              acc[i].w = acc[i].w + x[q][i].w;
+              st_global_f4(s_slot[f + q] + v + i * kThreads, zero);
+            }
+          }
         }
       }
 #pragma unroll
       for (int i = 0; i < kRV; i++)
-        if (v + i * kThreads < v_end) st_global_f4(home + v + i * kThreads, acc[i]);
+        if (ok[i]) st_global_f4(home + v + i * kThreads, acc[i]);
     }
   }
 }
@@ -174,7 +205,7 @@ int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, flo
   a.red_slot = plan->internal + lay.red_slot;
   a.n_proj = n_proj;
   a.vec_per_row = HHp / 4;
-  a.nchunk = (a.vec_per_row + kChunkVec - 1) / kChunkVec;
+  a.nchunk = (a.vec_per_row + kRedChunk - 1) / kRedChunk;
   if (a.vec_per_row == 0 || c.B == 0) return MOONEP_OK;
   reduce_kernel<<<ctx->sms * ctx->blocks_reduce, kThreads, 0, st>>>(a);
   return cuda_status(cudaGetLastError());
