@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep-steps", type=int, default=30)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step in a CUDA graph and replay it in the timed region")
     ap.add_argument("--hp", type=int, default=None, help="override H' (profiling case)")
     ap.add_argument("--s", type=int, default=None, help="override S (profiling case)")
     ap.add_argument("--profile-op", default=None,
@@ -249,46 +251,80 @@ def max_over_ranks(x, dist):
 
 
 def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
-    """Same step through the public API, inputs from pinned host memory and
-    the combined result read back, copies inside the timed region."""
+    """The same step through the public API with inputs in pinned host memory:
+    every step copies its inputs host->device and reads the combined result
+    (and the gathered route weights) back.  Copies run on their own streams,
+    double-buffered, so step i's compute overlaps step i+1's inputs and step
+    i-1's result; the timed region spans the first input copy to the last
+    result copy."""
     from combine_moonep_plan_gb300 import workloads as wl
     R, S, K, E, H = sh.R, sh.S, sh.K, sh.E, sh.H
-    pin = dict(pin_memory=True)
-    h_topk = torch.from_numpy(topk_np).pin_memory()
-    h_tpe = torch.from_numpy(wl.tokens_per_expert(topk_np, E)).pin_memory()
     g = torch.Generator().manual_seed(seed)
-    h_hidden = torch.randn((R, S, H), generator=g).to(torch.bfloat16).pin_memory()
-    h_w = torch.from_numpy(wl.route_weights(sh, seed)).pin_memory()
-    h_grad = torch.randn((R, S, H), generator=g).to(torch.bfloat16).pin_memory()
-    h_out = torch.empty((R, S, H), dtype=torch.bfloat16, **pin)
-    h_wout = torch.empty((R, S, K), dtype=torch.float32, **pin)
+    h_in = {
+        "topk": torch.from_numpy(topk_np).pin_memory(),
+        "tpe": torch.from_numpy(wl.tokens_per_expert(topk_np, E)).pin_memory(),
+        "hidden": torch.randn((R, S, H), generator=g).to(torch.bfloat16).pin_memory(),
+        "w_sk": torch.from_numpy(wl.route_weights(sh, seed)).pin_memory(),
+        "grad": torch.randn((R, S, H), generator=g).to(torch.bfloat16).pin_memory(),
+    }
+    h_out = [{"out": torch.empty((R, S, H), dtype=torch.bfloat16, pin_memory=True),
+              "w_back": torch.empty((R, S, K), dtype=torch.float32, pin_memory=True)}
+             for _ in range(2)]
     st = Step(buf, sh, topk_np, seed, torch)
-    bi = sum(t.numel() * t.element_size() for t in (h_topk, h_tpe, h_hidden, h_w, h_grad))
-    bo = h_out.numel() * h_out.element_size() + h_wout.numel() * h_wout.element_size()
-
-    def one():
-        st.topk.copy_(h_topk, non_blocking=True)
-        st.tpe.copy_(h_tpe, non_blocking=True)
-        st.hidden.copy_(h_hidden, non_blocking=True)
-        st.w_sk.copy_(h_w, non_blocking=True)
-        st.grad.copy_(h_grad, non_blocking=True)
-        st.run()
-        h_out.copy_(st.out, non_blocking=True)
-        h_wout.copy_(st.w_back, non_blocking=True)
-
+    sets = []
     for _ in range(2):
-        one()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    start.record()
-    for _ in range(steps):
-        one()
-    end.record()
-    torch.cuda.synchronize()
-    ms = max_over_ranks(start.elapsed_time(end), dist)
+        sets.append({k: torch.empty_like(v, device="cuda") for k, v in h_in.items()} |
+                    {"out": torch.empty((R, S, H), dtype=torch.bfloat16, device="cuda"),
+                     "w_back": torch.empty((R, S, K), dtype=torch.float32, device="cuda")})
+    bi = sum(t.numel() * t.element_size() for t in h_in.values())
+    bo = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    compute = torch.cuda.Stream()
+    h2d = torch.cuda.Stream()
+    d2h = torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    inputs_ready = [ev(), ev()]
+    computed = [ev(), ev()]
+    read_back = [ev(), ev()]
+    used = [False, False]
+
+    def run(n, timed):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        h2d.record_event(start) if timed else None
+        for i in range(n):
+            b = i % 2
+            d = sets[b]
+            with torch.cuda.stream(h2d):
+                if used[b]:
+                    h2d.wait_event(computed[b])      # step i-2 no longer reads this set
+                for k, v in h_in.items():
+                    d[k].copy_(v, non_blocking=True)
+                h2d.record_event(inputs_ready[b])
+            with torch.cuda.stream(compute):
+                compute.wait_event(inputs_ready[b])
+                if used[b]:
+                    compute.wait_event(read_back[b])  # step i-2's result has been read
+                st.topk, st.tpe, st.hidden, st.w_sk, st.grad = (d["topk"], d["tpe"], d["hidden"],
+                                                                 d["w_sk"], d["grad"])
+                st.out, st.w_back = d["out"], d["w_back"]
+                st.run()
+                compute.record_event(computed[b])
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(computed[b])
+                h_out[b]["out"].copy_(d["out"], non_blocking=True)
+                h_out[b]["w_back"].copy_(d["w_back"], non_blocking=True)
+                d2h.record_event(read_back[b])
+            used[b] = True
+        if timed:
+            d2h.record_event(end)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) if timed else 0.0
+
+    run(3, False)
+    ms = max_over_ranks(run(steps, True), dist)
     del st
     return ms / steps, bi, bo
 
@@ -375,6 +411,26 @@ def reference_arm(args, sh, point, topk_np, seed, dist):
                              "sample": sample, "wall_s": wall},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def recorded_traffic(op, config):
+    """DRAM bytes per launch of `op` on `config` from profiles/traffic.md, if
+    the kernel's source is unchanged since the capture (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) < 5 or cells[0] != op or cells[1] != config:
+            continue
+        src = os.path.join(ROOT, cells[3])
+        if not os.path.exists(src):
+            return None
+        if hashlib.sha1(open(src, "rb").read()).hexdigest() != cells[4]:
+            return None
+        return int(cells[2])
+    return None
 
 
 def R_S(sh):
@@ -502,6 +558,30 @@ def main():
     if status != 0:
         raise SystemExit(f"device status {status} during warm-up")
 
+    graph_ms = None
+    if args.graph:
+        # plan -> dispatch -> prefetch -> combine -> grad dispatch -> reduce as
+        # one CUDA graph (the decode-sized case is launch-latency bound)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step.run()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step.run()
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
+        torch.cuda.synchronize()
+        ga = torch.cuda.Event(enable_timing=True)
+        gb = torch.cuda.Event(enable_timing=True)
+        ga.record()
+        for _ in range(args.steps):
+            graph.replay()
+        gb.record()
+        torch.cuda.synchronize()
+        graph_ms = max_over_ranks(ga.elapsed_time(gb), dist) / args.steps
+
     sampler = ClockSampler(local)
     time.sleep(0.3)
     total_ms, per_op, (t0, t1) = timed_steps(step, args.steps, torch, dist)
@@ -580,11 +660,14 @@ def main():
         "ops": ops, "plan_counts": counts,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": peak_src, "traffic": None},
+                     "peak_source": peak_src, "traffic": recorded_traffic(dom, sh.name)},
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks, "sweep": sweep, "device_status": status,
     }
+    if graph_ms is not None:
+        line["graph_replay"] = {"ms_per_step": graph_ms,
+                                "tokens_per_s": tokens / (graph_ms / 1e3)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
