@@ -217,12 +217,20 @@ __device__ int block_exclusive_scan(int32_t *v, int n) {
 // slots, segments and cu_seqlens, padding prefix, row bases, copy and reduce
 // lists.  Called by one whole block of kBalThreads threads with t.T filled;
 // err holds the error bits found so far.
+// When `ready` is given, the tables the route assignment needs (group
+// offsets, kept prefixes, pieces, row bases, the valid flag) are published
+// there as soon as they are written (ready = target), and the rest (padding
+// prefix, copy and reduce lists, experts_to_copy, counts) is finished while
+// the other CTAs already assign routes.
 __device__ void balance_tail(const PlanDims &d, const BalTables &t, PlanOut o, int32_t *in,
-                             const PlanLayout &lay, int32_t *status, int err_in) {
+                             const PlanLayout &lay, int32_t *status, int err_in,
+                             unsigned long long *ready = nullptr,
+                             unsigned long long target = 0) {
   __shared__ int sG[kMaxR], sKeep[kMaxR], sRecvPiece[kMaxR], sNslots[kMaxR], sRankPad[kMaxR];
   __shared__ int pDonor[kMaxR], pRecv[kMaxR], pLen[kMaxR], pStart[kMaxR];
   __shared__ int sNp, sErr, sP, sU;
   __shared__ int sPadOff[kMaxR], sSlotOff[kMaxR];
+  __shared__ int sPart[2][32];  // per-warp partial sums of a rank's segments
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kWarps = kBalThreads / 32;
   const int R = d.R, E = d.E, L = d.L, B = d.B, EB = d.EB, C = d.C;
@@ -263,7 +271,38 @@ __device__ void balance_tail(const PlanDims &d, const BalTables &t, PlanOut o, i
   // Phase C: the chain balance on one warp (lane j holds rank j and j + 32):
   // each round fills the lowest-index rank below C from the lowest-index rank
   // above C; at most R rounds.
-  if (warp == 0) {
+  if (warp == 0 && R <= 32) {
+    // lane j holds rank j
+    int rem = lane < R ? sG[lane] : C, don = 0, np = 0;
+    for (int round = 0; round <= R; round++) {
+      const unsigned rb = __ballot_sync(0xffffffffu, rem < C);
+      if (!rb) break;
+      const unsigned db = __ballot_sync(0xffffffffu, rem > C);
+      if (!db || np >= R) {  // only reachable from a broken histogram
+        if (lane == 0) sErr |= kErrHist;
+        break;
+      }
+      const int recv = __ffs(rb) - 1, donor = __ffs(db) - 1;
+      const int dd = C - __shfl_sync(0xffffffffu, rem, recv);
+      if (lane == 0) {
+        pDonor[np] = donor;
+        pRecv[np] = recv;
+        pLen[np] = dd;
+        sRecvPiece[recv] = np;
+      }
+      np++;
+      if (lane == donor) {
+        rem -= dd;
+        don += dd;
+      }
+      if (lane == recv) rem = C;
+    }
+    if (lane < R) {
+      sKeep[lane] = sG[lane] - don;
+      in[lay.keep + lane] = sKeep[lane];
+    }
+    if (lane == 0) sNp = np;
+  } else if (warp == 0) {
     const int C_ = C;
     int rem0 = lane < R ? sG[lane] : C_, rem1 = lane + 32 < R ? sG[lane + 32] : C_;
     int don0 = 0, don1 = 0, np = 0;
@@ -296,8 +335,6 @@ __device__ void balance_tail(const PlanDims &d, const BalTables &t, PlanOut o, i
         if (recv < 32) rem0 = C_; else rem1 = C_;
       }
     }
-    __syncwarp();
-    // kept prefixes
     for (int h2 = 0; h2 < 2; h2++) {
       const int j = lane + 32 * h2;
       if (j < R) {
@@ -305,7 +342,6 @@ __device__ void balance_tail(const PlanDims &d, const BalTables &t, PlanOut o, i
         in[lay.keep + j] = sKeep[j];
       }
     }
-    __syncwarp();
     if (lane == 0) sNp = np;
   }
   __syncthreads();
@@ -375,28 +411,81 @@ __device__ void balance_tail(const PlanDims &d, const BalTables &t, PlanOut o, i
 
   // Phase E: per rank, padded segment lengths -> cu_seqlens, padding ranges,
   // segment starts (kept in nseg) and padding prefix inside the rank (pad).
-  for (int j = warp; j < R; j += kWarps) {
+  // With R < 32 each rank's E+B segments are split over wpr warps: partial
+  // sums first, then each warp rescans its part from its offset.
+  const int wpr = R >= kWarps ? 1 : kWarps / R;  // warps per rank (R * wpr <= 32)
+  const int part = (EB + wpr - 1) / wpr;
+  if (wpr > 1 && warp < R * wpr) {
+    const int pj = warp / wpr, pw = warp % wpr;
+    const int x_lo = min(EB, pw * part), x_hi = min(EB, x_lo + part);
+    int sum = 0, psum = 0;
+    for (int x = x_lo + lane; x < x_hi; x += 32) {
+      const int n = nseg[pj * EB + x];
+      const int padded = (n + d.tp - 1) / d.tp * d.tp;
+      sum += padded;
+      psum += padded - n;
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, o2);
+      psum += __shfl_xor_sync(0xffffffffu, psum, o2);
+    }
+    if (lane == 0) {
+      sPart[0][warp] = sum;
+      sPart[1][warp] = psum;
+    }
+  }
+  __syncthreads();
+  for (int task = warp; task < R * wpr; task += kWarps) {
+    const int pj = task / wpr, pw = task % wpr;
+    const int x_lo = min(EB, pw * part), x_hi = min(EB, x_lo + part);
     int carry = 0, pcarry = 0;
-    for (int x0 = 0; x0 < EB; x0 += 32) {
+    for (int q = 0; q < pw; q++) {
+      carry += sPart[0][pj * wpr + q];
+      pcarry += sPart[1][pj * wpr + q];
+    }
+    for (int x0 = x_lo; x0 < x_hi; x0 += 32) {
       const int x = x0 + lane;
-      const int n = x < EB ? nseg[j * EB + x] : 0;
+      const int n = x < x_hi ? nseg[pj * EB + x] : 0;
       const int padded = (n + d.tp - 1) / d.tp * d.tp;
       const int pc = padded - n;
       const int incl = warp_incl_scan(padded);
       const int pincl = warp_incl_scan(pc);
-      if (x < EB) {
+      if (x < x_hi) {
         const int end = carry + incl;
         const int start = end - padded;
-        o.cu[j * EB + x] = end;
-        o.zfr[2 * (j * EB + x)] = start + n;
-        o.zfr[2 * (j * EB + x) + 1] = end;
-        nseg[j * EB + x] = start;
-        t.pad[j * EB + x] = pcarry + pincl - pc;
+        o.cu[pj * EB + x] = end;
+        o.zfr[2 * (pj * EB + x)] = start + n;
+        o.zfr[2 * (pj * EB + x) + 1] = end;
+        nseg[pj * EB + x] = start;
+        t.pad[pj * EB + x] = pcarry + pincl - pc;
       }
       carry += __shfl_sync(0xffffffffu, incl, 31);
       pcarry += __shfl_sync(0xffffffffu, pincl, 31);
     }
-    if (lane == 0) sRankPad[j] = pcarry;
+    if (lane == 0 && pw == wpr - 1) sRankPad[pj] = pcarry;
+  }
+  __syncthreads();
+  // row bases the route assignment needs
+  for (int e = tid; e < E; e += kBalThreads)
+    in[lay.home_rowbase + e] = nseg[(e / L) * EB + e] - sQ[e];
+  for (int i = tid; i < R * L; i += kBalThreads) {
+    const int j = i / L, u = i % L;
+    const int b = slot_b[i];
+    const int p = sRecvPiece[j];
+    if (b >= 0 && p >= 0) {
+      const int e = pDonor[p] * L + u;
+      in[lay.slot_rowbase + i] = nseg[j * EB + E + b] - max(pStart[p], sQ[e]);
+    }
+  }
+  if (ready != nullptr) {
+    if (tid == 0) in[kMetaValid] = sErr == 0 ? 1 : 0;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      atomicExch(ready, target);
+    }
   }
   // slot copies per expert (a receiver holds an expert at most once)
   for (int e = tid; e < E; e += kBalThreads) {
@@ -432,17 +521,6 @@ __device__ void balance_tail(const PlanDims &d, const BalTables &t, PlanOut o, i
   // experts_to_copy.
   for (int i = tid; i < R * EB; i += kBalThreads)
     in[lay.pad_prefix + i] = t.pad[i] + sPadOff[i / EB];
-  for (int e = tid; e < E; e += kBalThreads)
-    in[lay.home_rowbase + e] = nseg[(e / L) * EB + e] - sQ[e];
-  for (int i = tid; i < R * L; i += kBalThreads) {
-    const int j = i / L, u = i % L;
-    const int b = slot_b[i];
-    const int p = sRecvPiece[j];
-    if (b >= 0 && p >= 0) {
-      const int e = pDonor[p] * L + u;
-      in[lay.slot_rowbase + i] = nseg[j * EB + E + b] - max(pStart[p], sQ[e]);
-    }
-  }
   for (int i = tid; i < R * B; i += kBalThreads) {
     const int j = i / B, b = i % B;
     o.etc[i] = setc[i];
@@ -551,7 +629,7 @@ plan_balance_kernel(PlanDims d, const int32_t *__restrict__ tpe, int32_t *hist, 
           const int b = (r + 1 < R) ? col[(r + 1) * d.TPR] : carry;
           cnt = b - a;
         }
-        if (cnt != tpe[(int64_t)r * E + e]) atomicOr(&sErr0, kErrHist);
+        if (cnt != tpe[(int64_t)r * E + e]) set_status(status, MOONEP_ERR_HIST_MISMATCH);
       }
     }
   }
@@ -800,7 +878,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
       const int v = __ldcg(a.totals + i);
       a.totals[i] = 0;
       sCnt[i] = v;
-      if (a.tpe != nullptr && v != __ldg(a.tpe + i)) atomicOr(&s_err, kErrHist);
     }
     __syncthreads();
     const BalTables tb = bal_tables(sBal, d, a.in + a.lay.nseg, a.in + a.lay.padw, a.nseg_shared != 0);
@@ -815,13 +892,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
       a.in[a.lay.T + e] = run;
     }
     __syncthreads();
-    balance_tail(d, tb, a.o, a.in, a.lay, a.status, s_err | __ldcg(a.in + kMetaErr));
-    __threadfence();  // every table this thread wrote, before the publication
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      if (a.publish) atomicExch(a.sync + 1, s_target);
-    }
+    // publishes the routing tables part-way through (unless a test withholds it)
+    balance_tail(d, tb, a.o, a.in, a.lay, a.status, s_err | __ldcg(a.in + kMetaErr),
+                 a.publish ? a.sync + 1 : nullptr, s_target);
+    // tokens_per_expert against the recount, after the publication: a
+    // mismatch latches its error but the plan stands (it is built from the
+    // recount)
+    if (a.tpe != nullptr)
+      for (int i = tid; i < R * E; i += kFusedThreads)
+        if (sCnt[i] != __ldg(a.tpe + i)) set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
   } else {
     if (tid == 0) {
       const long long t0 = globaltimer_ns();

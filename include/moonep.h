@@ -155,7 +155,8 @@ int moonep_plan_clone(const moonep_comm_plan *src, moonep_comm_plan *dst, void *
  * every rank's S*K routes into the dst map; README items 1-2].
  *   topk  [R, S, K] int32 expert ids, each in [0, E)
  *   tpe   [R, E] int32 per-rank histogram, or NULL; when given it is checked
- *         against a recount (MOONEP_ERR_HIST_MISMATCH)
+ *         against a recount of topk: a mismatch latches
+ *         MOONEP_ERR_HIST_MISMATCH, and the plan is built from the recount
  * Fills every array of `plan`.  Deterministic: the same inputs give the same
  * plan, bit for bit.  Every rank receives exactly S*K routes; the experts a
  * rank prefetches come from one remote home group, at most B of them. */

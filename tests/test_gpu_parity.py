@@ -378,3 +378,12 @@ def test_planner_wait_limit_reports_timeout(monkeypatch):
     assert g.min() >= 0 and g.max() < sh.R * buf.NvS
     # a context created without the hook plans normally
     _full_pipeline(sh, topk, 8)
+
+
+@pytest.mark.parametrize("R,L,K,S,tp", [(40, 2, 2, 100, 4), (64, 1, 4, 40, 8), (33, 3, 8, 64, 16)])
+def test_many_ranks(R, L, K, S, tp):
+    """More than 32 ranks: the chain and segment scans take their wide paths."""
+    E = R * L
+    sh = wl.Shape("wide", R=R, E=E, K=K, S=S, H=64, Hp=8, B=L, tp=tp, weights="softmax")
+    topk = _routing(sh, "zipf_hard", R)
+    _full_pipeline(sh, topk, R, check_invariants=False)
