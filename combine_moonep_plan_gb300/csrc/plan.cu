@@ -786,6 +786,9 @@ size_t fused_smem_words(int R, int E, int B, bool nseg_shared) {
          bal_tables_words(R, E, B, nseg_shared);
 }
 
+// IT routes per thread (1, 2, 4 or 8; tile = 1024 * IT routes).  A compile-time
+// count keeps only the routes' registers live across the balance step.
+template <int IT>
 __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs a) {
   extern __shared__ int32_t sm[];
   const PlanDims d = a.d;
@@ -817,18 +820,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
 
   // 1. counts and in-warp ordinals
   int32_t *hw = h + warp * E;
-  const int items = a.items;
+  constexpr int items = IT;
   const int wbase = t * kFusedThreads * items + warp * 32 * items;
-  int e_reg[kFusedMaxItems], o_reg[kFusedMaxItems];
+  int e_reg[items], o_reg[items];
   bool bad = false;
 #pragma unroll
-  for (int c = 0; c < kFusedMaxItems; c++) {
+  for (int c = 0; c < items; c++) {
     const int i = wbase + c * 32 + lane;
-    e_reg[c] = (c < items && i < C) ? __ldg(src + i) : -1;
+    e_reg[c] = i < C ? __ldg(src + i) : -1;
   }
 #pragma unroll
-  for (int c = 0; c < kFusedMaxItems; c++) {
-    if (c >= items) break;
+  for (int c = 0; c < items; c++) {
     const int i = wbase + c * 32 + lane;
     int e = e_reg[c];
     if (i < C && (e < 0 || e >= E)) bad = true;
@@ -950,8 +952,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   const unsigned lt_mask = lanemask_lt();
   int32_t *dst = a.o.dst + (int64_t)r * C;
 #pragma unroll
-  for (int c = 0; c < kFusedMaxItems; c++) {
-    if (c >= items) break;
+  for (int c = 0; c < items; c++) {
     const int i = wbase + c * 32 + lane;
     const bool in_range = i < C;
     int j = R, row = 0;
@@ -1138,8 +1139,11 @@ cudaError_t plan_configure(int R, int E, int B) {
   if (e == cudaSuccess && plan_fused_choice(R, E, 1, B, 0, 1 << 30, &ns)) {
     const int fsmem = (int)(fused_smem_words(R, E, B, ns) * sizeof(int32_t));
     if (fsmem > 48 * 1024) {
-      e = cudaFuncSetAttribute(plan_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               fsmem);
+      const void *fs[] = {(const void *)plan_fused_kernel<1>, (const void *)plan_fused_kernel<2>,
+                          (const void *)plan_fused_kernel<4>, (const void *)plan_fused_kernel<8>};
+      for (const void *f : fs)
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, fsmem);
     }
   }
   return e;
@@ -1196,7 +1200,11 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     fa.wait_ns = ctx->test_unpublished_plan ? 200000000LL : 1000000000LL;
     void *args[] = {&fa};
     const size_t smem = fused_smem_words(d.R, d.E, d.B, nseg_shared) * sizeof(int32_t);
-    e = cudaLaunchCooperativeKernel((const void *)plan_fused_kernel, dim3(fa.G), dim3(kFusedThreads), args, smem, st);
+    const void *kern = fa.items == 1   ? (const void *)plan_fused_kernel<1>
+                       : fa.items == 2 ? (const void *)plan_fused_kernel<2>
+                       : fa.items == 4 ? (const void *)plan_fused_kernel<4>
+                                       : (const void *)plan_fused_kernel<8>;
+    e = cudaLaunchCooperativeKernel(kern, dim3(fa.G), dim3(kFusedThreads), args, smem, st);
     if (e != cudaSuccess) return cuda_status(e);
   } else {
     e = cudaMemsetAsync(in, 0, kMetaWords * sizeof(int32_t), st);
