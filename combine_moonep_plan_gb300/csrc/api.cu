@@ -101,7 +101,7 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
   ctx->blocks_copy = occupancy_copy();
   ctx->blocks_reduce = occupancy_reduce();
   const size_t hist =
-      (size_t)c.E * (plan_hist_tiles(c.R, ctx->C, ctx->sms_device) + 2 * c.R) * sizeof(int32_t);
+      (size_t)plan_scratch_words(c.R, c.E, ctx->C, ctx->sms_device) * sizeof(int32_t);
   const size_t ord = (size_t)c.R * ctx->C * sizeof(int32_t);
   e = cudaMalloc(&ctx->d_status, 256);
   if (e == cudaSuccess) e = cudaMemset(ctx->d_status, 0, 256);
@@ -117,8 +117,8 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
   }
   if (e == cudaSuccess) e = plan_configure(c.R, c.E, c.B);
   {
-    const char *t = getenv("MOONEP_TEST_UNPUBLISHED_PLAN");
-    ctx->test_unpublished_plan = (t && t[0] == '1') ? 1 : 0;
+    const char *t = getenv("MOONEP_TEST_PLANNER_TIMEOUT");
+    ctx->test_planner_timeout = (t && t[0] == '1') ? 1 : 0;
   }
   if (e != cudaSuccess) {
     cudaFree(ctx->d_status);
@@ -322,6 +322,16 @@ int moonep_get_status(moonep_ctx *ctx, int *device_status, void *stream) {
   cudaError_t e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaMemcpy(&v, ctx->d_status, sizeof(v), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(ctx->d_status, 0, sizeof(int32_t));
+  // A planner wait that ran out may have left its counters and accumulators
+  // out of step: start them again from zero.
+  if (e == cudaSuccess && v == MOONEP_ERR_TIMEOUT) {
+    const moonep_config &c = ctx->cfg;
+    const int64_t off = plan_totals_offset(c.R, c.E, ctx->C, ctx->sms_device);
+    const int64_t words = plan_scratch_words(c.R, c.E, ctx->C, ctx->sms_device) - off;
+    e = cudaMemset(ctx->d_sync, 0, 2 * sizeof(unsigned long long));
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_hist + off, 0, (size_t)words * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  }
   if (e != cudaSuccess) return MOONEP_ERR_CUDA;
   *device_status = v;
   return MOONEP_OK;

@@ -30,17 +30,32 @@ enum {
 };
 
 // Word offsets of the tables inside plan->internal (see PlanLayout::make).
+// Usable prefetch slots per rank: a rank receives at most one piece, from one
+// home group, so it never fills more than L = E/R slots.
+inline int usable_slots(int R, int E, int B) { return B < E / R ? B : E / R; }
+
+// Words of the balance step's tables (shared memory, or the plan's internal
+// area when they do not fit): per expert T, Q, home row base, slot copies and
+// their index (+1 each), per (rank, donor-local expert) slot and row base,
+// experts_to_copy of the usable slots, and per segment (E + R*Bm) valid rows
+// plus two prefix sums.
+inline size_t bal_tables_words(int R, int E, int B) {
+  const size_t Bm = (size_t)usable_slots(R, E, B);
+  const size_t nseg = (size_t)E + (size_t)R * Bm;
+  return 7 * (size_t)E + 2 + (size_t)R * Bm + nseg + 2 * (nseg + 1);
+}
+
+// Layout of plan->internal (int32 words after the meta words).
 struct PlanLayout {
-  int64_t qoff, T, home_rowbase, keep, piece_first, piece_count, piece_start,
-      piece_len, piece_recv, slot_rowbase, slot_b, nseg, padw, pad_prefix, copy_slot,
-      copy_expert, red_expert, red_first, red_slot, dupflag, total;
+  int64_t qoff, home_rowbase, keep, piece_first, piece_count, piece_start, piece_len,
+      piece_recv, slot_rowbase, bal, pad_prefix, copy_slot, copy_expert, red_expert, red_first,
+      red_slot, dupflag, total;
   static PlanLayout make(int R, int E, int B, int NvS, bool dup_records) {
     PlanLayout l;
     const int L = E / R, EB = E + B;
     int64_t o = kMetaWords;
     auto take = [&o](int64_t n) { int64_t at = o; o += (n + 3) / 4 * 4; return at; };
     l.qoff = take(E);
-    l.T = take(E);
     l.home_rowbase = take(E);
     l.keep = take(R);
     l.piece_first = take(R);
@@ -49,9 +64,7 @@ struct PlanLayout {
     l.piece_len = take(R);
     l.piece_recv = take(R);
     l.slot_rowbase = take((int64_t)R * L);
-    l.slot_b = take((int64_t)R * L);
-    l.nseg = take((int64_t)R * EB);
-    l.padw = take((int64_t)R * EB);
+    l.bal = take((int64_t)bal_tables_words(R, E, B));
     l.pad_prefix = take((int64_t)R * EB + 1);
     l.copy_slot = take((int64_t)R * B);
     l.copy_expert = take((int64_t)R * B);
@@ -74,12 +87,12 @@ struct moonep_ctx {
   int L, C, EB, NvS, TPR, G;  // E/R, S*K, E+B, rows per rank, tiles per rank, R*TPR
   int destroyed;
   int32_t *d_status;   // sticky first error
-  int32_t *d_hist;     // tile histograms, then [R, E] totals and [R, E] rank starts
+  int32_t *d_hist;     // planner scratch: tile histograms, [R, E] totals, duplicate counts, error bits
   int32_t *d_ord;      // [R*C] ordinal of a route among its tile's routes to the same expert
   uint16_t *d_hidden_view;  // optional [R*NvS, H] bf16
   float *d_weight_view;     // optional [R*NvS] fp32
-  unsigned long long *d_sync;  // [2] planner arrival counter, published target
-  int test_unpublished_plan;   // test hook: the planner's balance block never publishes
+  unsigned long long *d_sync;  // [2] planner counters: arrivals, tile blocks done
+  int test_planner_timeout;    // test hook: the planner's arrival wait never completes
   int blocks_dispatch, blocks_combine, blocks_copy, blocks_reduce;  // resident blocks per SM
 };
 
@@ -104,9 +117,14 @@ int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, flo
 // Opt the planner kernels into the dynamic shared memory E experts need.
 cudaError_t plan_configure(int R, int E, int B);
 // K when the single-launch planner handles this shape (0: the tile path).
-int plan_fused_choice(int R, int E, int K, int B, int C, int sms, bool *nseg_shared);
+int plan_fused_choice(int R, int E, int K, int B, int C, int sms);
 // Tiles the histogram area must hold (either planner path).
 int plan_hist_tiles(int R, int C, int sms);
+// The planner's scratch (ctx->d_hist): E words per tile, then the [R, E]
+// totals (at plan_totals_offset), 2R duplicate counts and an error word, all
+// zero between calls.
+int64_t plan_totals_offset(int R, int E, int C, int sms);
+int64_t plan_scratch_words(int R, int E, int C, int sms);
 int occupancy_dispatch(int K);
 int occupancy_combine(int K);
 int occupancy_copy();

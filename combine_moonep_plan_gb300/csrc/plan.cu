@@ -38,6 +38,7 @@ namespace {
 
 struct PlanDims {
   int R, E, K, S, B, tp, L, C, EB, NvS, TPR, G;
+  int Bm;  // usable slots per rank: min(B, L)
 };
 
 struct PlanOut {
@@ -148,230 +149,225 @@ plan_hist_kernel(const int32_t *__restrict__ topk, PlanDims d, int32_t *__restri
 constexpr int kBalThreads = 1024;
 constexpr int kMaxR = 64;
 
-// Shared-memory working set of the balance step (all pointers generic: nseg
-// and pad may live in global memory when R*(E+B) is too large for shared
-// memory).
-struct BalTables {
-  int32_t *T;       // [E] routes per expert
-  int32_t *Q;       // [E] offset of P_e inside Q_home(e)
-  int32_t *slot_b;  // [R*L] slot of (receiver j, donor-local expert u), -1 if none
-  int32_t *etc;     // [R*B] experts_to_copy
-  int32_t *rcnt;    // [E] slot copies per expert, then first index in the reduce list
-  int32_t *rhas;    // [E] expert has copies, then its index among such experts
-  int32_t *nseg;    // [R*(E+B)] valid rows, then segment starts
-  int32_t *pad;     // [R*(E+B)] padding rows, then their prefix inside the rank
+// Per-rank and per-piece state of the balance step (shared memory).
+struct BalSmall {
+  int G[kMaxR];           // routes of rank j's home group
+  int keep[kMaxR];        // prefix of Q_j the home rank keeps
+  int recv_piece[kMaxR];  // piece (chain order) rank j receives, -1 if none
+  int nslots[kMaxR];      // slots rank j uses
+  int slot_off[kMaxR];    // rank j's first entry in the copy list
+  int donor[kMaxR], recv[kMaxR], len[kMaxR], start[kMaxR];  // pieces, chain order
+  int pf[kMaxR], pc[kMaxR];             // per donor: first entry and count below
+  int ps[kMaxR], pl[kMaxR], pr[kMaxR];  // pieces grouped by donor: Q start, length, receiver
+  int part[2][32];                      // per-warp partial sums of the block scans
+  int np, err, U;
 };
 
-inline size_t bal_tables_words(int R, int E, int B, bool nseg_shared) {
-  return (size_t)5 * E + (size_t)R * B + (nseg_shared ? 2 * (size_t)R * (E + B) : 0);
-}
+// Tables of the balance step, one entry per expert, per (rank, donor-local
+// expert), per slot or per segment.  Segments are numbered rank by rank: the
+// rank's L home experts, then its Bm = min(B, L) usable slots (a rank
+// receives one piece, from one home group, so it never fills more than L
+// slots).  All pointers are generic: shared memory, or global memory when the
+// tables are too large.
+struct BalTables {
+  int32_t *T;        // [E] routes per expert
+  int32_t *Q;        // [E] offset of P_e inside Q_home(e)
+  int32_t *home_rb;  // [E] row of Q position 0 of expert e on its home rank
+  int32_t *slot_b;   // [R*L] slot of (receiver j, donor-local expert u), -1 if none
+  int32_t *slot_rb;  // [R*L] row of Q position 0 of that slot's expert on rank j
+  int32_t *etc;      // [R*Bm] expert held by slot b of rank j, -1 if none
+  int32_t *n;        // [R*(L+Bm)] valid rows per segment
+  int32_t *start;    // [R*(L+Bm)+1] padded rows, then their exclusive prefix
+  int32_t *padx;     // [R*(L+Bm)+1] padding rows, then their exclusive prefix
+  int32_t *rcnt;     // [E+1] slot copies per expert, then first index in the reduce list
+  int32_t *rhas;     // [E+1] expert has copies, then its index among such experts
+};
 
-__device__ __forceinline__ BalTables bal_tables(int32_t *base, const PlanDims &d,
-                                                int32_t *nseg_global, int32_t *pad_global,
-                                                bool nseg_shared) {
+__device__ __forceinline__ BalTables bal_tables(int32_t *base, const PlanDims &d) {
+  const int nseg = d.E + d.R * d.Bm;
   BalTables t;
   t.T = base;
   t.Q = t.T + d.E;
-  t.slot_b = t.Q + d.E;
-  t.etc = t.slot_b + d.R * d.L;
-  t.rcnt = t.etc + d.R * d.B;
-  t.rhas = t.rcnt + d.E;
-  t.nseg = nseg_shared ? t.rhas + d.E : nseg_global;
-  t.pad = nseg_shared ? t.nseg + d.R * d.EB : pad_global;
+  t.home_rb = t.Q + d.E;
+  t.slot_b = t.home_rb + d.E;
+  t.slot_rb = t.slot_b + d.E;
+  t.etc = t.slot_rb + d.E;
+  t.n = t.etc + d.R * d.Bm;
+  t.start = t.n + nseg;
+  t.padx = t.start + nseg + 1;
+  t.rcnt = t.padx + nseg + 1;
+  t.rhas = t.rcnt + d.E + 1;
   return t;
 }
 
-// Exclusive prefix sum of v[0..n) in place, by a whole block of kBalThreads
-// threads (each thread sums a contiguous run, then the runs are scanned);
-// returns the total to every thread.
-__device__ int block_exclusive_scan(int32_t *v, int n) {
-  __shared__ int wsum[32];
-  __shared__ int total;
+// Exclusive prefix sums of a[0..cnt) and b[0..cnt) in place, by a whole block
+// of kBalThreads threads (each thread takes a contiguous run, then the runs
+// are scanned); a[cnt] and b[cnt] receive the totals when `totals` is set.
+// With tp > 0, a[i] is first replaced by n rounded up to tp and b[i] by the
+// rounding's padding, where n = a[i].
+__device__ void block_scan2(int32_t *a, int32_t *b, int cnt, int tp, bool totals,
+                            int (*part)[32]) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (n + kBalThreads - 1) / kBalThreads;
-  const int b0 = min(n, tid * per), b1 = min(n, b0 + per);
-  int local = 0;
-  for (int i = b0; i < b1; i++) local += v[i];
-  const int incl = warp_incl_scan(local);
-  if (lane == 31) wsum[warp] = incl;
+  const int per = (cnt + kBalThreads - 1) / kBalThreads;
+  const int b0 = min(cnt, tid * per), b1 = min(cnt, b0 + per);
+  int sa = 0, sb = 0;
+  for (int i = b0; i < b1; i++) {
+    int va = a[i], vb = b[i];
+    if (tp > 0) {
+      const int p = (va + tp - 1) / tp * tp;
+      vb = p - va;
+      va = p;
+      a[i] = va;
+      b[i] = vb;
+    }
+    sa += va;
+    sb += vb;
+  }
+  const int ia = warp_incl_scan(sa), ib = warp_incl_scan(sb);
+  if (lane == 31) {
+    part[0][warp] = ia;
+    part[1][warp] = ib;
+  }
   __syncthreads();
   if (warp == 0) {
-    const int w = wsum[lane];
-    const int wi = warp_incl_scan(w);
-    wsum[lane] = wi - w;
-    if (lane == 31) total = wi;
+    const int wa = part[0][lane], wb = part[1][lane];
+    const int xa = warp_incl_scan(wa), xb = warp_incl_scan(wb);
+    part[0][lane] = xa - wa;
+    part[1][lane] = xb - wb;
+    if (lane == 31 && totals) {
+      a[cnt] = xa;
+      b[cnt] = xb;
+    }
   }
   __syncthreads();
-  int run = wsum[warp] + incl - local;
+  int ra = part[0][warp] + ia - sa, rb = part[1][warp] + ib - sb;
   for (int i = b0; i < b1; i++) {
-    const int x = v[i];
-    v[i] = run;
-    run += x;
+    const int va = a[i], vb = b[i];
+    a[i] = ra;
+    b[i] = rb;
+    ra += va;
+    rb += vb;
   }
-  const int tot = total;
   __syncthreads();
-  return tot;
 }
 
-// Everything after the per-expert totals: group offsets, the chain balance,
-// slots, segments and cu_seqlens, padding prefix, row bases, copy and reduce
-// lists.  Called by one whole block of kBalThreads threads with t.T filled;
-// err holds the error bits found so far.
-// When `ready` is given, the tables the route assignment needs (group
-// offsets, kept prefixes, pieces, row bases, the valid flag) are published
-// there as soon as they are written (ready = target), and the rest (padding
-// prefix, copy and reduce lists, experts_to_copy, counts) is finished while
-// the other CTAs already assign routes.
-__device__ void balance_tail(const PlanDims &d, const BalTables &t, PlanOut o, int32_t *in,
-                             const PlanLayout &lay, int32_t *status, int err_in,
-                             unsigned long long *ready = nullptr,
-                             unsigned long long target = 0) {
-  __shared__ int sG[kMaxR], sKeep[kMaxR], sRecvPiece[kMaxR], sNslots[kMaxR], sRankPad[kMaxR];
-  __shared__ int pDonor[kMaxR], pRecv[kMaxR], pLen[kMaxR], pStart[kMaxR];
-  __shared__ int sNp, sErr, sP, sU;
-  __shared__ int sPadOff[kMaxR], sSlotOff[kMaxR];
-  __shared__ int sPart[2][32];  // per-warp partial sums of a rank's segments
+// Stage 1 of the balance step, from the per-expert totals t.T: offsets inside
+// the home groups, the chain balance (pieces), slots, segment sizes, their
+// padded starts, and the row bases the route assignment needs.  Called by a
+// whole block of kBalThreads threads; err_in holds the error bits found so
+// far.  Writes only t and s.
+__device__ void balance_route(const PlanDims &d, const BalTables &t, BalSmall &s, int err_in) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kWarps = kBalThreads / 32;
-  const int R = d.R, E = d.E, L = d.L, B = d.B, EB = d.EB, C = d.C;
-  int32_t *sT = t.T, *sQ = t.Q, *slot_b = t.slot_b, *setc = t.etc, *nseg = t.nseg;
+  const int R = d.R, E = d.E, L = d.L, B = d.B, Bm = d.Bm, LB = L + Bm, C = d.C;
 
   if (tid == 0) {
-    sErr = err_in;
-    sNp = 0;
+    s.err = err_in;
+    s.np = 0;
   }
-  for (int i = tid; i < R * B; i += kBalThreads) setc[i] = -1;
-  for (int i = tid; i < R * EB; i += kBalThreads) nseg[i] = 0;
-  for (int i = tid; i < R * L; i += kBalThreads) slot_b[i] = -1;
+  for (int i = tid; i < R * L; i += kBalThreads) {
+    t.slot_b[i] = -1;
+    t.slot_rb[i] = 0;
+  }
+  for (int i = tid; i < R * Bm; i += kBalThreads) t.etc[i] = -1;
+  for (int i = tid; i < R * LB; i += kBalThreads) {
+    t.n[i] = 0;
+    t.start[i] = 0;
+  }
   for (int j = tid; j < R; j += kBalThreads) {
-    sRecvPiece[j] = -1;
-    sNslots[j] = 0;
-  }
-  for (int i = tid; i < 2 * R; i += kBalThreads) {
-    o.remote_stats[i] = 0;
-    o.dup_counts[i] = 0;
+    s.recv_piece[j] = -1;
+    s.nslots[j] = 0;
   }
   // Phase B: offset of P_e inside Q_home(e) (one warp per home group), G_j.
   for (int j = warp; j < R; j += kWarps) {
     int carry = 0;
     for (int u0 = 0; u0 < L; u0 += 32) {
       const int u = u0 + lane;
-      const int v = u < L ? sT[j * L + u] : 0;
+      const int v = u < L ? t.T[j * L + u] : 0;
       const int incl = warp_incl_scan(v);
-      if (u < L) {
-        sQ[j * L + u] = carry + incl - v;
-        in[lay.qoff + j * L + u] = carry + incl - v;
-      }
+      if (u < L) t.Q[j * L + u] = carry + incl - v;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) sG[j] = carry;
+    if (lane == 0) s.G[j] = carry;
   }
   __syncthreads();
 
   // Phase C: the chain balance on one warp (lane j holds rank j and j + 32):
   // each round fills the lowest-index rank below C from the lowest-index rank
   // above C; at most R rounds.
-  if (warp == 0 && R <= 32) {
-    // lane j holds rank j
-    int rem = lane < R ? sG[lane] : C, don = 0, np = 0;
-    for (int round = 0; round <= R; round++) {
-      const unsigned rb = __ballot_sync(0xffffffffu, rem < C);
-      if (!rb) break;
-      const unsigned db = __ballot_sync(0xffffffffu, rem > C);
-      if (!db || np >= R) {  // only reachable from a broken histogram
-        if (lane == 0) sErr |= kErrHist;
-        break;
-      }
-      const int recv = __ffs(rb) - 1, donor = __ffs(db) - 1;
-      const int dd = C - __shfl_sync(0xffffffffu, rem, recv);
-      if (lane == 0) {
-        pDonor[np] = donor;
-        pRecv[np] = recv;
-        pLen[np] = dd;
-        sRecvPiece[recv] = np;
-      }
-      np++;
-      if (lane == donor) {
-        rem -= dd;
-        don += dd;
-      }
-      if (lane == recv) rem = C;
-    }
-    if (lane < R) {
-      sKeep[lane] = sG[lane] - don;
-      in[lay.keep + lane] = sKeep[lane];
-    }
-    if (lane == 0) sNp = np;
-  } else if (warp == 0) {
-    const int C_ = C;
-    int rem0 = lane < R ? sG[lane] : C_, rem1 = lane + 32 < R ? sG[lane + 32] : C_;
+  if (warp == 0) {
+    int rem0 = lane < R ? s.G[lane] : C, rem1 = lane + 32 < R ? s.G[lane + 32] : C;
     int don0 = 0, don1 = 0, np = 0;
     for (int round = 0; round <= R; round++) {
-      const unsigned rb0 = __ballot_sync(0xffffffffu, rem0 < C_);
-      const unsigned rb1 = __ballot_sync(0xffffffffu, rem1 < C_);
+      const unsigned rb0 = __ballot_sync(0xffffffffu, rem0 < C);
+      const unsigned rb1 = R > 32 ? __ballot_sync(0xffffffffu, rem1 < C) : 0u;
       if (!rb0 && !rb1) break;
-      const unsigned db0 = __ballot_sync(0xffffffffu, rem0 > C_);
-      const unsigned db1 = __ballot_sync(0xffffffffu, rem1 > C_);
+      const unsigned db0 = __ballot_sync(0xffffffffu, rem0 > C);
+      const unsigned db1 = R > 32 ? __ballot_sync(0xffffffffu, rem1 > C) : 0u;
       if ((!db0 && !db1) || np >= R) {  // only reachable from a broken histogram
-        if (lane == 0) sErr |= kErrHist;
+        if (lane == 0) s.err |= kErrHist;
         break;
       }
       const int recv = rb0 ? __ffs(rb0) - 1 : 32 + __ffs(rb1) - 1;
       const int donor = db0 ? __ffs(db0) - 1 : 32 + __ffs(db1) - 1;
       const int rr = recv < 32 ? __shfl_sync(0xffffffffu, rem0, recv)
                                : __shfl_sync(0xffffffffu, rem1, recv - 32);
-      const int dd = C_ - rr;
+      const int dd = C - rr;
       if (lane == 0) {
-        pDonor[np] = donor;
-        pRecv[np] = recv;
-        pLen[np] = dd;
-        sRecvPiece[recv] = np;
+        s.donor[np] = donor;
+        s.recv[np] = recv;
+        s.len[np] = dd;
+        s.recv_piece[recv] = np;
       }
       np++;
       if (lane == (donor & 31)) {
-        if (donor < 32) { rem0 -= dd; don0 += dd; } else { rem1 -= dd; don1 += dd; }
+        if (donor < 32) {
+          rem0 -= dd;
+          don0 += dd;
+        } else {
+          rem1 -= dd;
+          don1 += dd;
+        }
       }
       if (lane == (recv & 31)) {
-        if (recv < 32) rem0 = C_; else rem1 = C_;
+        if (recv < 32)
+          rem0 = C;
+        else
+          rem1 = C;
       }
     }
-    for (int h2 = 0; h2 < 2; h2++) {
-      const int j = lane + 32 * h2;
-      if (j < R) {
-        sKeep[j] = sG[j] - (h2 ? don1 : don0);
-        in[lay.keep + j] = sKeep[j];
-      }
-    }
-    if (lane == 0) sNp = np;
+    if (lane < R) s.keep[lane] = s.G[lane] - don0;
+    if (lane + 32 < R) s.keep[lane + 32] = s.G[lane + 32] - don1;
+    if (lane == 0) s.np = np;
   }
   __syncthreads();
 
-  // Phase D: per piece (one warp each): where its run starts (after the
-  // donor's kept prefix and its earlier pieces), its place in the
-  // donor-grouped piece list, and the receiver's slots; per donor: its piece
-  // list range; per home expert: its kept routes.
-  const int np_all = sNp;
+  // Phase D: per donor, its range in the donor-grouped piece list; per piece
+  // (one warp each): where its run starts (after the donor's kept prefix and
+  // its earlier pieces), its place in that list, and the receiver's slots;
+  // per home expert: its kept routes.
+  const int np_all = s.np;
   for (int l = tid; l < R; l += kBalThreads) {
     int first = 0, count = 0;
     for (int q = 0; q < np_all; q++) {
-      first += pDonor[q] < l;
-      count += pDonor[q] == l;
+      first += s.donor[q] < l;
+      count += s.donor[q] == l;
     }
-    in[lay.piece_first + l] = first;
-    in[lay.piece_count + l] = count;
+    s.pf[l] = first;
+    s.pc[l] = count;
   }
   for (int p = warp; p < np_all; p += kWarps) {
-    const int l = pDonor[p], j = pRecv[p], dd = pLen[p];
-    int a = sKeep[l], pos = 0;
+    const int l = s.donor[p], j = s.recv[p], dd = s.len[p];
+    int a = s.keep[l], pos = 0;
     for (int q = 0; q < np_all; q++) {
-      if (q < p && pDonor[q] == l) a += pLen[q];
-      pos += pDonor[q] < l || (pDonor[q] == l && q < p);
+      if (q < p && s.donor[q] == l) a += s.len[q];
+      pos += s.donor[q] < l || (s.donor[q] == l && q < p);
     }
     if (lane == 0) {
-      pStart[p] = a;
-      in[lay.piece_start + pos] = a;
-      in[lay.piece_len + pos] = dd;
-      in[lay.piece_recv + pos] = j;
+      s.start[p] = a;
+      s.ps[pos] = a;
+      s.pl[pos] = dd;
+      s.pr[pos] = j;
     }
     int nslots = 0;
     for (int u0 = 0; u0 < L; u0 += 32) {
@@ -380,222 +376,191 @@ __device__ void balance_tail(const PlanDims &d, const BalTables &t, PlanOut o, i
       bool present = false;
       int lo = 0, hi = 0;
       if (u < L) {
-        lo = max(a, sQ[e]);
-        hi = min(a + dd, sQ[e] + sT[e]);
-        present = sT[e] > 0 && hi > lo;
+        lo = max(a, t.Q[e]);
+        hi = min(a + dd, t.Q[e] + t.T[e]);
+        present = t.T[e] > 0 && hi > lo;
       }
       const unsigned bal = __ballot_sync(0xffffffffu, present);
       const int b = nslots + __popc(bal & lanemask_lt());
       if (present) {
-        if (b < B) {
-          setc[j * B + b] = e;
-          nseg[j * EB + E + b] = hi - lo;
-          slot_b[j * L + u] = b;
+        if (b < B) {  // b < L, so b < Bm
+          t.etc[j * Bm + b] = e;
+          t.n[j * LB + L + b] = hi - lo;
+          t.start[j * LB + L + b] = hi - lo;
+          t.slot_b[j * L + u] = b;
         } else {
-          atomicOr(&sErr, kErrSlots);
+          atomicOr(&s.err, kErrSlots);
         }
       }
       nslots += __popc(bal);
     }
-    if (lane == 0) {
-      sNslots[j] = min(nslots, B);
-      o.remote_stats[2 * j] = dd;
-      o.remote_stats[2 * j + 1] = min(nslots, B);
-    }
+    if (lane == 0) s.nslots[j] = min(nslots, B);
   }
   for (int e = tid; e < E; e += kBalThreads) {
     const int j = e / L;
-    nseg[j * EB + e] = min(max(sKeep[j] - sQ[e], 0), sT[e]);
+    const int v = min(max(s.keep[j] - t.Q[e], 0), t.T[e]);
+    t.n[j * LB + (e - j * L)] = v;
+    t.start[j * LB + (e - j * L)] = v;
   }
   __syncthreads();
 
-  // Phase E: per rank, padded segment lengths -> cu_seqlens, padding ranges,
-  // segment starts (kept in nseg) and padding prefix inside the rank (pad).
-  // With R < 32 each rank's E+B segments are split over wpr warps: partial
-  // sums first, then each warp rescans its part from its offset.
-  const int wpr = R >= kWarps ? 1 : kWarps / R;  // warps per rank (R * wpr <= 32)
-  const int part = (EB + wpr - 1) / wpr;
-  if (wpr > 1 && warp < R * wpr) {
-    const int pj = warp / wpr, pw = warp % wpr;
-    const int x_lo = min(EB, pw * part), x_hi = min(EB, x_lo + part);
-    int sum = 0, psum = 0;
-    for (int x = x_lo + lane; x < x_hi; x += 32) {
-      const int n = nseg[pj * EB + x];
-      const int padded = (n + d.tp - 1) / d.tp * d.tp;
-      sum += padded;
-      psum += padded - n;
-    }
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) {
-      sum += __shfl_xor_sync(0xffffffffu, sum, o2);
-      psum += __shfl_xor_sync(0xffffffffu, psum, o2);
-    }
-    if (lane == 0) {
-      sPart[0][warp] = sum;
-      sPart[1][warp] = psum;
-    }
+  // Phase E: every segment rounded up to token_padding; starts and padding
+  // rows as prefix sums over all ranks' segments in order.
+  block_scan2(t.start, t.padx, R * LB, d.tp, true, s.part);
+
+  // Row bases: the row of Q position 0 of each expert on its home rank and in
+  // each slot (rank-local rows).
+  for (int e = tid; e < E; e += kBalThreads) {
+    const int j = e / L;
+    t.home_rb[e] = t.start[j * LB + (e - j * L)] - t.start[j * LB] - t.Q[e];
   }
-  __syncthreads();
-  for (int task = warp; task < R * wpr; task += kWarps) {
-    const int pj = task / wpr, pw = task % wpr;
-    const int x_lo = min(EB, pw * part), x_hi = min(EB, x_lo + part);
-    int carry = 0, pcarry = 0;
-    for (int q = 0; q < pw; q++) {
-      carry += sPart[0][pj * wpr + q];
-      pcarry += sPart[1][pj * wpr + q];
-    }
-    for (int x0 = x_lo; x0 < x_hi; x0 += 32) {
-      const int x = x0 + lane;
-      const int n = x < x_hi ? nseg[pj * EB + x] : 0;
-      const int padded = (n + d.tp - 1) / d.tp * d.tp;
-      const int pc = padded - n;
-      const int incl = warp_incl_scan(padded);
-      const int pincl = warp_incl_scan(pc);
-      if (x < x_hi) {
-        const int end = carry + incl;
-        const int start = end - padded;
-        o.cu[pj * EB + x] = end;
-        o.zfr[2 * (pj * EB + x)] = start + n;
-        o.zfr[2 * (pj * EB + x) + 1] = end;
-        nseg[pj * EB + x] = start;
-        t.pad[pj * EB + x] = pcarry + pincl - pc;
-      }
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-      pcarry += __shfl_sync(0xffffffffu, pincl, 31);
-    }
-    if (lane == 0 && pw == wpr - 1) sRankPad[pj] = pcarry;
-  }
-  __syncthreads();
-  // row bases the route assignment needs
-  for (int e = tid; e < E; e += kBalThreads)
-    in[lay.home_rowbase + e] = nseg[(e / L) * EB + e] - sQ[e];
   for (int i = tid; i < R * L; i += kBalThreads) {
-    const int j = i / L, u = i % L;
-    const int b = slot_b[i];
-    const int p = sRecvPiece[j];
-    if (b >= 0 && p >= 0) {
-      const int e = pDonor[p] * L + u;
-      in[lay.slot_rowbase + i] = nseg[j * EB + E + b] - max(pStart[p], sQ[e]);
-    }
+    const int j = i / L, u = i - j * L;
+    const int b = t.slot_b[i];
+    const int p = s.recv_piece[j];
+    if (b >= 0 && p >= 0)
+      t.slot_rb[i] = t.start[j * LB + L + b] - t.start[j * LB] - max(s.start[p], t.Q[s.donor[p] * L + u]);
   }
-  if (ready != nullptr) {
-    if (tid == 0) in[kMetaValid] = sErr == 0 ? 1 : 0;
-    __threadfence();
-    __syncthreads();
+  __syncthreads();
+}
+
+// Stage 2 of the balance step: experts_to_copy, cu_seqlens,
+// zero_fill_ranges, remote_stats, the padding prefix, the copy and reduce
+// lists and the meta words; a neutral plan (every later kernel a no-op) when
+// the balance failed or `ok` is false.  Called by one whole block after
+// balance_route.
+__device__ void balance_outputs(const PlanDims &d, const BalTables &t, BalSmall &s, PlanOut o,
+                                int32_t *in, const PlanLayout &lay, int32_t *status, bool ok) {
+  const int tid = threadIdx.x;
+  const int R = d.R, E = d.E, L = d.L, B = d.B, Bm = d.Bm, LB = L + Bm, EB = d.EB, tp = d.tp;
+  const int err = s.err;
+  if (!ok || err != 0) {
     if (tid == 0) {
-      __threadfence();
-      atomicExch(ready, target);
+      in[kMetaValid] = 0;
+      in[kMetaP] = 0;
+      in[kMetaU] = 0;
+      in[kMetaD] = 0;
+      if (ok)
+        set_status(status, (err & kErrBadExpert) ? MOONEP_ERR_BAD_EXPERT
+                           : (err & kErrHist)    ? MOONEP_ERR_HIST_MISMATCH
+                                                 : MOONEP_ERR_SLOTS);
     }
+    for (int i = tid; i < R * B; i += kBalThreads) o.etc[i] = -1;
+    for (int i = tid; i < R * EB; i += kBalThreads) {
+      o.cu[i] = 0;
+      o.zfr[2 * i] = 0;
+      o.zfr[2 * i + 1] = 0;
+    }
+    for (int i = tid; i <= R * EB; i += kBalThreads) in[lay.pad_prefix + i] = 0;
+    for (int i = tid; i < 2 * R; i += kBalThreads) o.remote_stats[i] = 0;
+    return;
+  }
+  if (tid == 0) {
+    int u = 0;
+    for (int j = 0; j < R; j++) {
+      s.slot_off[j] = u;
+      u += s.nslots[j];
+    }
+    s.U = u;
+  }
+  for (int i = tid; i < R * B; i += kBalThreads) {
+    const int j = i / B, b = i - j * B;
+    o.etc[i] = b < Bm ? t.etc[j * Bm + b] : -1;
+  }
+  for (int j = tid; j < R; j += kBalThreads) {
+    const int p = s.recv_piece[j];
+    o.remote_stats[2 * j] = p >= 0 ? s.len[p] : 0;
+    o.remote_stats[2 * j + 1] = s.nslots[j];
   }
   // slot copies per expert (a receiver holds an expert at most once)
   for (int e = tid; e < E; e += kBalThreads) {
-    const int l = e / L, u = e % L;
+    const int l = e / L, u = e - l * L;
     int cnt = 0;
     for (int j = 0; j < R; j++) {
-      const int p = sRecvPiece[j];
-      if (p >= 0 && pDonor[p] == l && slot_b[j * L + u] >= 0) cnt++;
+      const int p = s.recv_piece[j];
+      if (p >= 0 && s.donor[p] == l && t.slot_b[j * L + u] >= 0) cnt++;
     }
     t.rcnt[e] = cnt;
     t.rhas[e] = cnt > 0;
   }
+  // cu_seqlens, zero-fill ranges and the padding prefix of every (rank,
+  // segment): a segment that is neither a home expert nor a usable slot of
+  // the rank is empty and sits where the rank's running prefix stands.
+  for (int i = tid; i < R * EB; i += kBalThreads) {
+    const int j = i / EB, x = i - j * EB;
+    const int base = j * LB;
+    int c, nn = 0;
+    if (x < E) {
+      if (x / L == j) {
+        c = base + (x - j * L);
+        nn = t.n[c];
+      } else {
+        c = x < j * L ? base : base + L;
+      }
+    } else if (x - E < Bm) {
+      c = base + L + (x - E);
+      nn = t.n[c];
+    } else {
+      c = base + LB;
+    }
+    const int st = t.start[c] - t.start[base];
+    const int end = st + (nn + tp - 1) / tp * tp;
+    o.cu[i] = end;
+    o.zfr[2 * i] = st + nn;
+    o.zfr[2 * i + 1] = end;
+    in[lay.pad_prefix + i] = t.padx[c];
+  }
   __syncthreads();
-
-  // Phase F: rank offsets of padding rows and of used slots; reduce-list
-  // positions.
-  if (tid == 0) {
-    int p = 0, u = 0;
-    for (int j = 0; j < R; j++) {
-      sPadOff[j] = p;
-      p += sRankPad[j];
-      sSlotOff[j] = u;
-      u += sNslots[j];
-    }
-    sP = p;
-    sU = u;
-    in[lay.pad_prefix + R * EB] = p;
-  }
-  const int ncopies = block_exclusive_scan(t.rcnt, E);
-  const int nexperts = block_exclusive_scan(t.rhas, E);
-
-  // Phase G: global padding prefix, row bases, copy list, reduce list,
-  // experts_to_copy.
-  for (int i = tid; i < R * EB; i += kBalThreads)
-    in[lay.pad_prefix + i] = t.pad[i] + sPadOff[i / EB];
+  // copy list: every used slot, rank by rank
   for (int i = tid; i < R * B; i += kBalThreads) {
-    const int j = i / B, b = i % B;
-    o.etc[i] = setc[i];
-    if (b < sNslots[j]) {
-      in[lay.copy_slot + sSlotOff[j] + b] = i;
-      in[lay.copy_expert + sSlotOff[j] + b] = setc[i];
+    const int j = i / B, b = i - j * B;
+    if (b < s.nslots[j]) {
+      in[lay.copy_slot + s.slot_off[j] + b] = i;
+      in[lay.copy_expert + s.slot_off[j] + b] = t.etc[j * Bm + b];
     }
   }
-  // experts with copies in ascending id; their slots in ascending rank
+  // reduce list: experts with copies in ascending id; their slots in
+  // ascending rank
+  block_scan2(t.rcnt, t.rhas, E, 0, true, s.part);
+  const int ncopies = t.rcnt[E], nexperts = t.rhas[E];
   for (int e = tid; e < E; e += kBalThreads) {
     const int first = t.rcnt[e];
-    const int next = e + 1 < E ? t.rcnt[e + 1] : ncopies;
-    if (next == first) continue;
+    if (t.rcnt[e + 1] == first) continue;
     const int di = t.rhas[e];
-    const int l = e / L, u = e % L;
+    const int l = e / L, u = e - l * L;
     in[lay.red_expert + di] = e;
     in[lay.red_first + di] = first;
     int c = 0;
     for (int j = 0; j < R; j++) {
-      const int p = sRecvPiece[j];
-      if (p >= 0 && pDonor[p] == l && slot_b[j * L + u] >= 0)
-        in[lay.red_slot + first + c++] = j * B + slot_b[j * L + u];
+      const int p = s.recv_piece[j];
+      if (p >= 0 && s.donor[p] == l && t.slot_b[j * L + u] >= 0)
+        in[lay.red_slot + first + c++] = j * B + t.slot_b[j * L + u];
     }
   }
   if (tid == 0) {
+    in[lay.pad_prefix + R * EB] = t.padx[R * LB];
     in[lay.red_first + nexperts] = ncopies;
     in[kMetaD] = nexperts;
+    in[kMetaP] = t.padx[R * LB];
+    in[kMetaU] = s.U;
+    in[kMetaValid] = 1;
   }
-  __syncthreads();
-
-  // Phase H: publish, or neutralise the plan on error.  The error word is
-  // left at zero for the next plan.
-  const int err = sErr;
-  if (err == 0) {
-    if (tid == 0) {
-      in[kMetaP] = sP;
-      in[kMetaU] = sU;
-      in[kMetaValid] = 1;
-      in[kMetaErr] = 0;
-    }
-    return;
-  }
-  if (tid == 0) {
-    in[kMetaErr] = 0;
-    in[kMetaValid] = 0;
-    in[kMetaP] = 0;
-    in[kMetaU] = 0;
-    in[kMetaD] = 0;
-    set_status(status, (err & kErrBadExpert) ? MOONEP_ERR_BAD_EXPERT
-                       : (err & kErrHist)    ? MOONEP_ERR_HIST_MISMATCH
-                                             : MOONEP_ERR_SLOTS);
-  }
-  for (int i = tid; i < R * B; i += kBalThreads) o.etc[i] = -1;
-  for (int i = tid; i < R * EB; i += kBalThreads) {
-    o.cu[i] = 0;
-    o.zfr[2 * i] = 0;
-    o.zfr[2 * i + 1] = 0;
-  }
-  for (int i = tid; i <= R * EB; i += kBalThreads) in[lay.pad_prefix + i] = 0;
-  for (int i = tid; i < 2 * R; i += kBalThreads) o.remote_stats[i] = 0;
 }
 
 // Tile path: one CTA scans every expert's tile counts (where each tile's
-// routes start inside P_e), then runs the balance tail.
-__global__ void __launch_bounds__(kBalThreads)
+// routes start inside P_e), runs the balance step, and leaves the tables the
+// route assignment needs in the plan's internal area.
+__global__ void __launch_bounds__(kBalThreads, 1)
 plan_balance_kernel(PlanDims d, const int32_t *__restrict__ tpe, int32_t *hist, PlanOut o,
-                    int32_t *in, PlanLayout lay, int32_t *status, int nseg_shared) {
+                    int32_t *in, PlanLayout lay, int32_t *status, int tables_shared) {
   extern __shared__ int32_t sm[];
+  __shared__ BalSmall bs;
   __shared__ int sErr0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kWarps = kBalThreads / 32;
-  const int R = d.R, E = d.E, G = d.G;
-  const BalTables t = bal_tables(sm, d, in + lay.nseg, in + lay.padw, nseg_shared != 0);
+  const int R = d.R, E = d.E, G = d.G, L = d.L;
+  const BalTables t = bal_tables(tables_shared ? sm : in + lay.bal, d);
   if (tid == 0) sErr0 = in[kMetaErr];
-  __syncthreads();
   // Each warp scans whole columns; the column's values are loaded 128 at a
   // time (four per lane) before the scan so the loads overlap.
   for (int e = warp; e < E; e += kWarps) {
@@ -617,10 +582,7 @@ plan_balance_kernel(PlanDims d, const int32_t *__restrict__ tpe, int32_t *hist, 
       }
     }
     __syncwarp();
-    if (lane == 0) {
-      t.T[e] = carry;
-      in[lay.T + e] = carry;
-    }
+    if (lane == 0) t.T[e] = carry;
     if (tpe != nullptr) {
       for (int r = lane; r < R; r += 32) {
         int cnt = 0;
@@ -634,7 +596,23 @@ plan_balance_kernel(PlanDims d, const int32_t *__restrict__ tpe, int32_t *hist, 
     }
   }
   __syncthreads();
-  balance_tail(d, t, o, in, lay, status, sErr0);
+  balance_route(d, t, bs, sErr0);
+  // tables of the route assignment kernel
+  for (int e = tid; e < E; e += kBalThreads) {
+    in[lay.qoff + e] = t.Q[e];
+    in[lay.home_rowbase + e] = t.home_rb[e];
+  }
+  for (int i = tid; i < R * L; i += kBalThreads) in[lay.slot_rowbase + i] = t.slot_rb[i];
+  for (int j = tid; j < R; j += kBalThreads) {
+    in[lay.keep + j] = bs.keep[j];
+    in[lay.piece_first + j] = bs.pf[j];
+    in[lay.piece_count + j] = bs.pc[j];
+    in[lay.piece_start + j] = bs.ps[j];
+    in[lay.piece_len + j] = bs.pl[j];
+    in[lay.piece_recv + j] = bs.pr[j];
+  }
+  for (int i = tid; i < 2 * R; i += kBalThreads) o.dup_counts[i] = 0;
+  balance_outputs(d, t, bs, o, in, lay, status, true);
 }
 
 // ------------------------------------------------------------------ K3
@@ -736,20 +714,26 @@ plan_assign_kernel(PlanDims d, const int32_t *__restrict__ topk, const int32_t *
 
 // ------------------------------------------------------------- fused
 //
-// The whole planner in one cooperative launch of R*ceil(S*K/8192) blocks of
-// 1024 threads, one per 8192-route tile of a source rank:
-//   1. each warp walks 8 chunks of 32 consecutive routes and counts them per
-//      expert (warp-aggregated, stable ordinals kept in registers);
-//   2. per-expert offsets of the warps; the tile's histogram to global;
-//   3. the last block to arrive sums the tiles per rank, checks
-//      tokens_per_expert, scans over ranks and runs the balance step for every
-//      rank, then publishes; the others wait for that (bounded by a time
-//      limit);
-//   4. every block adds the earlier tiles of its rank to its offsets, maps its
-//      routes to (rank, row), marks duplicates with warp shuffles inside each
-//      token's K lanes, and writes dst.
+// The whole planner in one cooperative launch: G tile blocks of 1024
+// threads, R*ceil(S*K/(1024*IT)) of them, one per tile of a source rank, plus
+// one table block:
+//   1. each warp of a tile block walks IT chunks of 32 consecutive routes and
+//      counts them per expert (warp-aggregated, stable ordinals kept in
+//      registers);
+//   2. per-expert offsets of the warps; the tile's histogram to global; the
+//      tile's counts added to its rank's totals;
+//   3. every block waits until all have arrived (bounded by a time limit),
+//      reads the per-rank totals and runs the balance step's first stage in
+//      its own shared memory (each block computes the same tables from the
+//      same totals);
+//   4. each tile block adds the earlier tiles of its rank to its offsets, maps
+//      its routes to (rank, row), marks duplicates with warp shuffles inside
+//      each token's K lanes, and writes dst; meanwhile the table block writes
+//      the plan's other outputs (cu_seqlens, padding, copy and reduce lists),
+//      then, once every tile block is done, the duplicate counts, and clears
+//      the cross-block accumulators for the next call.
 // Used when K divides 32 (a token's routes then never straddle a 32-route
-// chunk), the tiles fit on the SMs at once and the tables fit in shared
+// chunk), the blocks fit on the SMs at once and the tables fit in shared
 // memory; otherwise the three-kernel tile path runs.
 
 constexpr int kFusedThreads = 1024;
@@ -759,20 +743,20 @@ constexpr int kFusedMaxItems = 8;  // routes per thread: 1, 2, 4 or 8 (tile = 10
 struct FusedArgs {
   PlanDims d;
   const int32_t *topk, *tpe;
-  int32_t *hist;      // [G, E] tile counts, then [R, E] where each rank starts in P_e
+  int32_t *hist;    // [G, E] tile counts
+  int32_t *totals;  // [R, E] routes per (rank, expert): zero between calls
+  int32_t *aux;     // [2R] duplicate counts, [1] error bits: zero between calls
   PlanOut o;
   int32_t *in;
   PlanLayout lay;
   int32_t *status;
-  unsigned long long *sync;  // [0] arrivals, [1] last published arrival target
+  // [0] arrivals (G + 1 per call), [1] tile blocks done (G per call)
+  unsigned long long *sync;
   int32_t *dupflag;
-  int32_t *totals;    // [R, E] routes per (rank, expert): zero between calls
-  int32_t *rank_off;  // [R, E] where each rank's routes start inside P_e
   int items;          // routes per thread; tile = 1024 * items routes
-  int tpr, G;         // tiles per rank, R * tpr
-  int nseg_shared;
-  int publish;        // 0 only when a test makes the wait run out
-  long long wait_ns;  // limit of the wait for the balance step
+  int tpr, G;         // tiles per rank, tile blocks (R * tpr)
+  int unreachable;    // test hook: the arrival wait can never be satisfied
+  long long wait_ns;  // limit of each wait
 };
 
 __device__ __forceinline__ long long globaltimer_ns() {
@@ -781,9 +765,25 @@ __device__ __forceinline__ long long globaltimer_ns() {
   return t;
 }
 
-size_t fused_smem_words(int R, int E, int B, bool nseg_shared) {
-  return (size_t)kFusedWarps * E + 4 * (size_t)E + 8 * (size_t)R + (size_t)E * R +
-         bal_tables_words(R, E, B, nseg_shared);
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Spin (thread 0) until *p reaches target or the limit passes; true if reached.
+__device__ bool wait_counter(const unsigned long long *p, unsigned long long target,
+                             long long limit_ns) {
+  const long long t0 = globaltimer_ns();
+  while (ld_acquire(p) < target) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
+size_t fused_smem_words(int R, int E, int B) {
+  return (size_t)kFusedWarps * E + (size_t)E * R + (size_t)E + bal_tables_words(R, E, B);
 }
 
 // IT routes per thread (1, 2, 4 or 8; tile = 1024 * IT routes).  A compile-time
@@ -791,165 +791,147 @@ size_t fused_smem_words(int R, int E, int B, bool nseg_shared) {
 template <int IT>
 __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs a) {
   extern __shared__ int32_t sm[];
+  __shared__ BalSmall bs;
+  __shared__ int s_bad, s_ok, s_err, s_done;
+  __shared__ unsigned long long s_target;
   const PlanDims d = a.d;
   const int R = d.R, E = d.E, L = d.L, C = d.C;
   const int g = blockIdx.x;
-  const int r = g / a.tpr, t = g % a.tpr;
+  const bool table_block = g == a.G;
+  const int r = table_block ? 0 : g / a.tpr, t = table_block ? 0 : g % a.tpr;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int32_t *h = sm;                       // [warps][E]
-  int32_t *sQoff = h + kFusedWarps * E;  // [E]
-  int32_t *sHomeRb = sQoff + E;          // [E]
-  int32_t *sSrc = sHomeRb + E;           // [E]
-  int32_t *sSlotRb = sSrc + E;           // [R*L]
-  int32_t *sR = sSlotRb + R * L;         // keep, first, count, start, len, recv [R each], dups [2R]
-  int32_t *sCnt = sR + 8 * R;            // [R*E] (balance block)
-  int32_t *sBal = sCnt + E * R;          // balance tables
-  __shared__ int s_last, s_timeout, s_valid, s_bad, s_err;
-  __shared__ unsigned long long s_target;
+  int32_t *h = sm;                     // [warps][E]
+  int32_t *sCnt = h + kFusedWarps * E;  // [R*E]
+  int32_t *sSrc = sCnt + E * R;         // [E]
+  const BalTables tb = bal_tables(sSrc + E, d);
 
   const int32_t *src = a.topk + (int64_t)r * C;
   const unsigned lt = lanemask_lt();
   const int nbits = key_bits(E);
-  for (int i = tid; i < kFusedWarps * E; i += kFusedThreads) h[i] = 0;
-  if (tid == 0) {
-    s_bad = 0;
-    s_err = 0;
-    s_timeout = 0;
-  }
-  __syncthreads();
-
-  // 1. counts and in-warp ordinals
-  int32_t *hw = h + warp * E;
   constexpr int items = IT;
   const int wbase = t * kFusedThreads * items + warp * 32 * items;
   int e_reg[items], o_reg[items];
-  bool bad = false;
-#pragma unroll
-  for (int c = 0; c < items; c++) {
-    const int i = wbase + c * 32 + lane;
-    e_reg[c] = i < C ? __ldg(src + i) : -1;
-  }
-#pragma unroll
-  for (int c = 0; c < items; c++) {
-    const int i = wbase + c * 32 + lane;
-    int e = e_reg[c];
-    if (i < C && (e < 0 || e >= E)) bad = true;
-    if (i >= C || e < 0 || e >= E) e = -1;
-    const unsigned m = match_key(e >= 0 ? e : E, nbits);
-    int base = 0;
-    if (e >= 0) base = hw[e];
-    __syncwarp();
-    if (e >= 0 && (m & lt) == 0) hw[e] = base + __popc(m);
-    __syncwarp();
-    e_reg[c] = e;
-    o_reg[c] = base + __popc(m & lt);
-  }
-  if (bad) atomicOr(&s_bad, 1);
-  __syncthreads();
-  if (tid == 0 && s_bad) {
-    atomicOr(a.in + kMetaErr, kErrBadExpert);
-    set_status(a.status, MOONEP_ERR_BAD_EXPERT);
-  }
-  // 2. warp offsets per expert; the tile's histogram
-  for (int e = tid; e < E; e += kFusedThreads) {
-    int run = 0;
-    for (int w = 0; w < kFusedWarps; w++) {
-      const int v = h[w * E + e];
-      h[w * E + e] = run;
-      run += v;
-    }
-    a.hist[(int64_t)g * E + e] = run;
-    if (run) atomicAdd(a.totals + (int64_t)r * E + e, run);
-  }
-  __threadfence();  // this thread's histogram entries, before the arrival
-  __syncthreads();
-
-  // 3. the last block to arrive balances; the others wait for it
-  if (tid == 0) {
-    __threadfence();
-    const unsigned long long G = (unsigned long long)a.G;
-    const unsigned long long old = atomicAdd(a.sync, 1ull);
-    s_last = old % G == G - 1;
-    s_target = old - old % G + G;
-  }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    // per-rank counts (summed by the tiles' atomics); cleared for the next call
-    for (int i = tid; i < R * E; i += kFusedThreads) {
-      const int v = __ldcg(a.totals + i);
-      a.totals[i] = 0;
-      sCnt[i] = v;
-    }
+  if (tid == 0) s_bad = 0;
+  if (!table_block) {
+    for (int i = tid; i < kFusedWarps * E; i += kFusedThreads) h[i] = 0;
     __syncthreads();
-    const BalTables tb = bal_tables(sBal, d, a.in + a.lay.nseg, a.in + a.lay.padw, a.nseg_shared != 0);
-    // where each rank's routes start inside P_e, and T_e
+
+    // 1. counts and in-warp ordinals
+    int32_t *hw = h + warp * E;
+    bool bad = false;
+#pragma unroll
+    for (int c = 0; c < items; c++) {
+      const int i = wbase + c * 32 + lane;
+      e_reg[c] = i < C ? __ldg(src + i) : -1;
+    }
+#pragma unroll
+    for (int c = 0; c < items; c++) {
+      const int i = wbase + c * 32 + lane;
+      int e = e_reg[c];
+      if (i < C && (e < 0 || e >= E)) bad = true;
+      if (i >= C || e < 0 || e >= E) e = -1;
+      const unsigned m = match_key(e >= 0 ? e : E, nbits);
+      int base = 0;
+      if (e >= 0) base = hw[e];
+      __syncwarp();
+      if (e >= 0 && (m & lt) == 0) hw[e] = base + __popc(m);
+      __syncwarp();
+      e_reg[c] = e;
+      o_reg[c] = base + __popc(m & lt);
+    }
+    if (bad) atomicOr(&s_bad, 1);
+    __syncthreads();
+    if (tid == 0 && s_bad) {
+      atomicOr(a.aux + 2 * R, kErrBadExpert);
+      set_status(a.status, MOONEP_ERR_BAD_EXPERT);
+    }
+    // 2. warp offsets per expert; the tile's histogram; the rank's totals
     for (int e = tid; e < E; e += kFusedThreads) {
       int run = 0;
+      for (int w = 0; w < kFusedWarps; w++) {
+        const int v = h[w * E + e];
+        h[w * E + e] = run;
+        run += v;
+      }
+      a.hist[(int64_t)g * E + e] = run;
+      if (run) atomicAdd(a.totals + (int64_t)r * E + e, run);
+    }
+    __threadfence();  // this thread's histogram entries and totals, before the arrival
+  }
+  __syncthreads();
+
+  // 3. all blocks arrive; each waits for the rest
+  if (tid == 0) {
+    __threadfence();
+    const unsigned long long n = (unsigned long long)a.G + 1;
+    const unsigned long long old = atomicAdd(a.sync, 1ull);
+    const unsigned long long target = old - old % n + n;
+    s_target = target;
+    s_ok = wait_counter(a.sync, target + (a.unreachable ? 1 : 0), a.wait_ns);
+    if (!s_ok) set_status(a.status, MOONEP_ERR_TIMEOUT);
+    s_err = s_ok ? __ldcg(a.aux + 2 * R) : 0;
+  }
+  __syncthreads();
+  const bool ok = s_ok;
+  if (ok) {
+    for (int i = tid; i < R * E; i += kFusedThreads) sCnt[i] = __ldcg(a.totals + i);
+    __syncthreads();
+    for (int e = tid; e < E; e += kFusedThreads) {
+      int tot = 0, before = 0;
       for (int j = 0; j < R; j++) {
-        a.rank_off[(int64_t)j * E + e] = run;
-        run += sCnt[j * E + e];
+        const int v = sCnt[j * E + e];
+        before += j < r ? v : 0;
+        tot += v;
       }
-      tb.T[e] = run;
-      a.in[a.lay.T + e] = run;
+      tb.T[e] = tot;
+      sSrc[e] = before;
     }
-    __syncthreads();
-    // publishes the routing tables part-way through (unless a test withholds it)
-    balance_tail(d, tb, a.o, a.in, a.lay, a.status, s_err | __ldcg(a.in + kMetaErr),
-                 a.publish ? a.sync + 1 : nullptr, s_target);
-    // tokens_per_expert against the recount, after the publication: a
-    // mismatch latches its error but the plan stands (it is built from the
-    // recount)
+    // tokens_per_expert against the recount, a slice per block: a mismatch
+    // latches its error but the plan stands (it is built from the recount)
     if (a.tpe != nullptr)
-      for (int i = tid; i < R * E; i += kFusedThreads)
+      for (int i = g * kFusedThreads + tid; i < R * E; i += (a.G + 1) * kFusedThreads)
         if (sCnt[i] != __ldg(a.tpe + i)) set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
-  } else {
+    __syncthreads();
+    balance_route(d, tb, bs, s_err);
+  }
+
+  if (table_block) {
+    balance_outputs(d, tb, bs, a.o, a.in, a.lay, a.status, ok);
+    // the duplicate counts once every tile block has added its own; then
+    // the accumulators start the next call at zero
     if (tid == 0) {
-      const long long t0 = globaltimer_ns();
-      const volatile unsigned long long *ready = a.sync + 1;
-      while (*ready < s_target) {
-        if (globaltimer_ns() - t0 > a.wait_ns) {
-          s_timeout = 1;
-          set_status(a.status, MOONEP_ERR_TIMEOUT);
-          break;
-        }
-        __nanosleep(256);
-      }
-      __threadfence();
+      const unsigned long long done = s_target / ((unsigned long long)a.G + 1) * a.G;
+      s_done = wait_counter(a.sync + 1, done, a.wait_ns);
+      if (!s_done) set_status(a.status, MOONEP_ERR_TIMEOUT);
     }
     __syncthreads();
+    for (int i = tid; i < 2 * R; i += kFusedThreads) {
+      a.o.dup_counts[i] = s_done ? __ldcg(a.aux + i) : 0;
+      a.aux[i] = 0;
+    }
+    for (int i = tid; i < R * E; i += kFusedThreads) a.totals[i] = 0;
+    if (tid == 0) a.aux[2 * R] = 0;
+    return;
   }
 
   // 4. this tile's routes -> (rank, row), duplicate marks, dst
   for (int e = tid; e < E; e += kFusedThreads) {
-    sQoff[e] = __ldcg(a.in + a.lay.qoff + e);
-    sHomeRb[e] = __ldcg(a.in + a.lay.home_rowbase + e);
-    // where this tile's routes start inside P_e: the rank's start plus the
+    // where this tile's routes start inside P_e: the earlier ranks, then the
     // rank's earlier tiles
-    int off = __ldcg(a.rank_off + (int64_t)r * E + e);
+    int off = sSrc[e];
 #pragma unroll 4
     for (int tt = 0; tt < t; tt++) off += __ldcg(a.hist + (int64_t)(r * a.tpr + tt) * E + e);
     sSrc[e] = off;
   }
-  for (int i = tid; i < R * L; i += kFusedThreads) sSlotRb[i] = __ldcg(a.in + a.lay.slot_rowbase + i);
-  for (int j = tid; j < R; j += kFusedThreads) {
-    sR[j] = __ldcg(a.in + a.lay.keep + j);
-    sR[R + j] = __ldcg(a.in + a.lay.piece_first + j);
-    sR[2 * R + j] = __ldcg(a.in + a.lay.piece_count + j);
-    sR[3 * R + j] = __ldcg(a.in + a.lay.piece_start + j);
-    sR[4 * R + j] = __ldcg(a.in + a.lay.piece_len + j);
-    sR[5 * R + j] = __ldcg(a.in + a.lay.piece_recv + j);
-  }
-  for (int i = tid; i < 2 * R; i += kFusedThreads) sR[6 * R + i] = 0;
-  if (tid == 0) s_valid = (__ldcg(a.in + kMetaValid) != 0) && !s_timeout;
+  int32_t *sDup = bs.part[0];  // [2R] duplicate counts of this block (R <= 64: part has 64)
+  for (int i = tid; i < 2 * R; i += kFusedThreads) sDup[i] = 0;
   __syncthreads();
-  const bool valid = s_valid;
+  const bool valid = ok && bs.err == 0;
   const int K = d.K;
   // A token's K routes sit in K consecutive lanes.  Routes of one token that
   // land on the same rank share the key (token lane group, rank).
   const int dkey_bits = key_bits((32 / K) * (R + 1));
   const int rkey_bits = key_bits(R);
-  const unsigned lt_mask = lanemask_lt();
   int32_t *dst = a.o.dst + (int64_t)r * C;
 #pragma unroll
   for (int c = 0; c < items; c++) {
@@ -960,25 +942,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
       j = 0;
       if (valid) {
         const int e = e_reg[c];
-        const int p = sQoff[e] + sSrc[e] + h[warp * E + e] + o_reg[c];
+        const int p = tb.Q[e] + sSrc[e] + h[warp * E + e] + o_reg[c];
         const int l = e / L;
-        if (p < sR[l]) {
+        if (p < bs.keep[l]) {
           j = l;
-          row = sHomeRb[e] + p;
+          row = tb.home_rb[e] + p;
         } else {
-          const int q0 = sR[R + l], qn = sR[2 * R + l];
+          const int q0 = bs.pf[l], qn = bs.pc[l];
           for (int pc = q0; pc < q0 + qn; pc++)
-            if (p < sR[3 * R + pc] + sR[4 * R + pc]) {
-              j = sR[5 * R + pc];
-              row = sSlotRb[j * L + (e - l * L)] + p;
+            if (p < bs.ps[pc] + bs.pl[pc]) {
+              j = bs.pr[pc];
+              row = tb.slot_rb[j * L + (e - l * L)] + p;
               break;
             }
         }
       }
     }
     const unsigned same = match_key((lane / K) * (R + 1) + j, dkey_bits);
-    const bool primary = (same & lt_mask) == 0;
-    const bool has_dup = (same & ~lt_mask & ~(1u << lane)) != 0;
+    const bool primary = (same & lt) == 0;
+    const bool has_dup = (same & ~lt & ~(1u << lane)) != 0;
     const bool cnt_dup = in_range && valid && !primary;
     const bool cnt_grp = in_range && valid && primary && has_dup;
     if (in_range) {
@@ -992,16 +974,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     if (md | mg) {
       const int rk = (cnt_dup || cnt_grp) ? j : R;
       const unsigned mr = match_key(rk, rkey_bits);
-      if (rk < R && (mr & lt_mask) == 0) {
+      if (rk < R && (mr & lt) == 0) {
         const int nd = __popc(mr & md), ng = __popc(mr & mg);
-        if (nd) atomicAdd(&sR[6 * R + 2 * rk], nd);
-        if (ng) atomicAdd(&sR[6 * R + 2 * rk + 1], ng);
+        if (nd) atomicAdd(&sDup[2 * rk], nd);
+        if (ng) atomicAdd(&sDup[2 * rk + 1], ng);
       }
     }
   }
   __syncthreads();
   for (int i = tid; i < 2 * R; i += kFusedThreads)
-    if (sR[6 * R + i]) atomicAdd(a.o.dup_counts + i, sR[6 * R + i]);
+    if (sDup[i]) atomicAdd(a.aux + i, sDup[i]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) atomicAdd(a.sync + 1, 1ull);
 }
 
 // ------------------------------------------------------------------ K4
@@ -1075,20 +1060,18 @@ plan_dup_kernel(PlanDims d, const int32_t *__restrict__ dst, const int32_t *__re
 
 }  // namespace
 
-// Fused path if K divides 32, a warp walks at most 64 chunks of 32 routes,
-// and its tables fit in shared memory.  Returns K (template) or 0.
 // Routes per thread of the single-launch planner: the fewest (most tiles,
-// most SMs at work) for which every tile fits on the SMs at once; 0 if none.
+// most SMs at work) for which every tile block and the table block fit on
+// the SMs at once; 0 if none.
 int plan_fused_items(int R, int C, int sms) {
   for (int items = 1; items <= kFusedMaxItems; items *= 2) {
     const int tpr = (C + kFusedThreads * items - 1) / (kFusedThreads * items);
-    if ((int64_t)R * (tpr > 0 ? tpr : 1) <= sms) return items;
+    if ((int64_t)R * (tpr > 0 ? tpr : 1) + 1 <= sms) return items;
   }
   return 0;
 }
 
-// Tiles of either planner path: the histogram area holds E words per tile,
-// then the fused path's [R, E] totals and [R, E] rank starts.
+// Tiles of either planner path (the histogram area holds E words per tile).
 int plan_hist_tiles(int R, int C, int sms) {
   const int tile_path = R * ((C + kTile - 1) / kTile);
   const int items = plan_fused_items(R, C, sms);
@@ -1096,30 +1079,36 @@ int plan_hist_tiles(int R, int C, int sms) {
   return tile_path > fused ? tile_path : fused;
 }
 
+int64_t plan_totals_offset(int R, int E, int C, int sms) {
+  return (int64_t)E * plan_hist_tiles(R, C, sms);
+}
+
+int64_t plan_scratch_words(int R, int E, int C, int sms) {
+  return plan_totals_offset(R, E, C, sms) + (int64_t)R * E + 2 * R + 8;
+}
+
 int plan_fused_tiles(int C, int items) {
   const int tpr = (C + kFusedThreads * items - 1) / (kFusedThreads * items);
   return tpr > 0 ? tpr : 1;
 }
 
-int plan_fused_choice(int R, int E, int K, int B, int C, int sms, bool *nseg_shared) {
+// Shared memory the planner kernels may use.
+constexpr size_t kPlanSmemLimit = 200 * 1024;
+
+int plan_fused_choice(int R, int E, int K, int B, int C, int sms) {
   if (32 % K != 0 || R > kMaxR || plan_fused_items(R, C, sms) == 0) return 0;
-  const size_t limit = 200 * 1024 / sizeof(int32_t);
-  if (fused_smem_words(R, E, B, true) <= limit) {
-    *nseg_shared = true;
-    return K;
-  }
-  if (fused_smem_words(R, E, B, false) <= limit) {
-    *nseg_shared = false;
-    return K;
-  }
-  return 0;
+  return fused_smem_words(R, E, B) * sizeof(int32_t) <= kPlanSmemLimit ? K : 0;
+}
+
+static bool bal_in_shared(int R, int E, int B) {
+  return bal_tables_words(R, E, B) * sizeof(int32_t) <= kPlanSmemLimit;
 }
 
 cudaError_t plan_configure(int R, int E, int B) {
   const int hist_smem = (kPlanThreads / 32) * E * (int)sizeof(int32_t);
   const int assign_smem = (3 * E + 8 * R) * (int)sizeof(int32_t);
-  const bool bal_shared = bal_tables_words(R, E, B, true) * sizeof(int32_t) <= 160 * 1024;
-  const int bal_smem = (int)(bal_tables_words(R, E, B, bal_shared) * sizeof(int32_t));
+  const int bal_smem =
+      bal_in_shared(R, E, B) ? (int)(bal_tables_words(R, E, B) * sizeof(int32_t)) : 0;
   cudaError_t e = cudaSuccess;
   if (hist_smem > 48 * 1024)
     e = cudaFuncSetAttribute(plan_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1135,9 +1124,8 @@ cudaError_t plan_configure(int R, int E, int B) {
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, assign_smem);
   }
-  bool ns = false;
-  if (e == cudaSuccess && plan_fused_choice(R, E, 1, B, 0, 1 << 30, &ns)) {
-    const int fsmem = (int)(fused_smem_words(R, E, B, ns) * sizeof(int32_t));
+  if (e == cudaSuccess && plan_fused_choice(R, E, 1, B, 0, 1 << 30)) {
+    const int fsmem = (int)(fused_smem_words(R, E, B) * sizeof(int32_t));
     if (fsmem > 48 * 1024) {
       const void *fs[] = {(const void *)plan_fused_kernel<1>, (const void *)plan_fused_kernel<2>,
                           (const void *)plan_fused_kernel<4>, (const void *)plan_fused_kernel<8>};
@@ -1165,6 +1153,7 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
   d.NvS = ctx->NvS;
   d.TPR = ctx->TPR;
   d.G = ctx->G;
+  d.Bm = usable_slots(d.R, d.E, d.B);
   const bool dup = (plan->flags & MOONEP_PLAN_DUP_RECORDS) != 0;
   PlanLayout lay = PlanLayout::make(d.R, d.E, d.B, d.NvS, dup);
   int32_t *in = plan->internal;
@@ -1176,8 +1165,7 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
   }
   PlanOut o{plan->dst, plan->experts_to_copy, plan->cu_seqlens, plan->zero_fill_ranges,
             plan->remote_stats, plan->dup_counts, plan->dup_groups, plan->dup_loffs};
-  bool nseg_shared = false;
-  const int fused_k = plan_fused_choice(d.R, d.E, d.K, d.B, d.C, ctx->sms_device, &nseg_shared);
+  const int fused_k = plan_fused_choice(d.R, d.E, d.K, d.B, d.C, ctx->sms_device);
   if (fused_k > 0 && ctx->d_sync != nullptr) {
     FusedArgs fa;
     fa.d = d;
@@ -1187,24 +1175,23 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     fa.items = plan_fused_items(d.R, d.C, ctx->sms_device);
     fa.tpr = plan_fused_tiles(d.C, fa.items);
     fa.G = d.R * fa.tpr;
-    fa.totals = ctx->d_hist + (int64_t)d.E * plan_hist_tiles(d.R, d.C, ctx->sms_device);
-    fa.rank_off = fa.totals + (int64_t)d.R * d.E;
+    fa.totals = ctx->d_hist + plan_totals_offset(d.R, d.E, d.C, ctx->sms_device);
+    fa.aux = fa.totals + (int64_t)d.R * d.E;
     fa.o = o;
     fa.in = in;
     fa.lay = lay;
     fa.status = ctx->d_status;
     fa.sync = ctx->d_sync;
     fa.dupflag = dupflag;
-    fa.nseg_shared = nseg_shared ? 1 : 0;
-    fa.publish = ctx->test_unpublished_plan ? 0 : 1;
-    fa.wait_ns = ctx->test_unpublished_plan ? 200000000LL : 1000000000LL;
+    fa.unreachable = ctx->test_planner_timeout;
+    fa.wait_ns = ctx->test_planner_timeout ? 200000000LL : 1000000000LL;
     void *args[] = {&fa};
-    const size_t smem = fused_smem_words(d.R, d.E, d.B, nseg_shared) * sizeof(int32_t);
+    const size_t smem = fused_smem_words(d.R, d.E, d.B) * sizeof(int32_t);
     const void *kern = fa.items == 1   ? (const void *)plan_fused_kernel<1>
                        : fa.items == 2 ? (const void *)plan_fused_kernel<2>
                        : fa.items == 4 ? (const void *)plan_fused_kernel<4>
                                        : (const void *)plan_fused_kernel<8>;
-    e = cudaLaunchCooperativeKernel(kern, dim3(fa.G), dim3(kFusedThreads), args, smem, st);
+    e = cudaLaunchCooperativeKernel(kern, dim3(fa.G + 1), dim3(kFusedThreads), args, smem, st);
     if (e != cudaSuccess) return cuda_status(e);
   } else {
     e = cudaMemsetAsync(in, 0, kMetaWords * sizeof(int32_t), st);
@@ -1214,9 +1201,9 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
       plan_hist_kernel<<<d.G, kPlanThreads, smem, st>>>(topk, d, ctx->d_hist, ctx->d_ord, in,
                                                          ctx->d_status);
     }
-    const bool bal_shared = bal_tables_words(d.R, d.E, d.B, true) * sizeof(int32_t) <= 160 * 1024;
+    const bool bal_shared = bal_in_shared(d.R, d.E, d.B);
     plan_balance_kernel<<<1, kBalThreads,
-                          bal_tables_words(d.R, d.E, d.B, bal_shared) * sizeof(int32_t), st>>>(
+                          bal_shared ? bal_tables_words(d.R, d.E, d.B) * sizeof(int32_t) : 0, st>>>(
         d, tpe, ctx->d_hist, o, in, lay, ctx->d_status, bal_shared ? 1 : 0);
     if ((int64_t)d.R * d.S > 0) {
       const int64_t ntok = (int64_t)d.R * d.S;

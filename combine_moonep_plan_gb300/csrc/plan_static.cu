@@ -85,13 +85,13 @@ extern "C" int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk
     cudaGetLastError();
     return MOONEP_ERR_CUDA;
   }
-  // scratch: planner sync words, histograms of either planner path
-  // [E, tiles] plus [R, E] totals and [R, E] rank starts, ordinals [R*S*K],
+  // scratch: planner sync words, the planner's scratch (histograms of either
+  // path, [R, E] totals, duplicate counts, error word), ordinals [R*S*K],
   // plan tables
   const int64_t tpr = (C + kTile - 1) / kTile;
   const int64_t sync_words = 64;
-  const int64_t hist_tiles = plan_hist_tiles(c.R, (int)C, sms);
-  const int64_t hist_words = round_words((int64_t)c.E * (hist_tiles + 2 * c.R));
+  const int64_t totals_off = plan_totals_offset(c.R, c.E, (int)C, sms);
+  const int64_t hist_words = round_words(plan_scratch_words(c.R, c.E, (int)C, sms));
   const int64_t ord_words = round_words((int64_t)c.R * C);
   const PlanLayout lay = PlanLayout::make(c.R, c.E, c.B, (int)nvs, false);
   if (sync_words + hist_words + ord_words + lay.total > kNoAllocScratchWords)
@@ -103,11 +103,14 @@ extern "C" int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk
 
   cudaStream_t s = (cudaStream_t)stream;
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return MOONEP_ERR_CUDA;
-  // The planner's arrival counters, per-rank totals and error word must start
-  // at zero: clear them on every call.
+  // The planner's counters, per-rank totals, duplicate counts and error word
+  // must start at zero: clear them on every call (the scratch serves every
+  // shape).
   if (cudaMemsetAsync(scratch, 0, sync_words * sizeof(int32_t), s) != cudaSuccess ||
-      cudaMemsetAsync(scratch + sync_words + (int64_t)c.E * hist_tiles, 0,
-                      (size_t)c.R * c.E * sizeof(int32_t), s) != cudaSuccess)
+      cudaMemsetAsync(scratch + sync_words + totals_off, 0,
+                      (size_t)(plan_scratch_words(c.R, c.E, (int)C, sms) - totals_off) *
+                          sizeof(int32_t),
+                      s) != cudaSuccess)
     return MOONEP_ERR_CUDA;
 
   // A context and a plan that only point: no member owns memory.

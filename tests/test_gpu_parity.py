@@ -360,15 +360,15 @@ def test_destroy_is_idempotent():
 
 
 def test_planner_wait_limit_reports_timeout(monkeypatch):
-    """The planner's blocks wait for the balance step with a time limit.  A
-    test hook stops the balance block from publishing; the waiting blocks must
-    give up, latch MOONEP_ERR_TIMEOUT and leave a plan every later kernel can
-    still consume without leaving its buffers."""
+    """The planner's blocks wait for one another with a time limit.  A test
+    hook makes the arrival wait unsatisfiable; every block must give up, latch
+    MOONEP_ERR_TIMEOUT and leave a plan every later kernel can still consume
+    without leaving its buffers."""
     from combine_moonep_plan_gb300 import _lib
-    monkeypatch.setenv("MOONEP_TEST_UNPUBLISHED_PLAN", "1")
+    monkeypatch.setenv("MOONEP_TEST_PLANNER_TIMEOUT", "1")
     sh = wl.SHAPES["tiny"]
     buf = _buffer(_cfg_of(sh), H=sh.H)
-    monkeypatch.delenv("MOONEP_TEST_UNPUBLISHED_PLAN")
+    monkeypatch.delenv("MOONEP_TEST_PLANNER_TIMEOUT")
     topk = _routing(sh, "zipf", 8)
     x = torch.randn(sh.R, sh.S, sh.H, device="cuda").bfloat16()
     _, _, _, plan = buf.dispatch(x, None, torch.from_numpy(topk).cuda())
