@@ -76,7 +76,6 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
   const int64_t nw = ((int64_t)gridDim.x * BT) >> 5;
   const int K = KT > 0 ? KT : a.K;
   const int64_t units = a.ntok * a.nchunk;
-  const uint64_t pol = l2_evict_first();
   // The next unit's dst entries are loaded one unit ahead, so their latency
   // overlaps the current unit's row loads.
   int32_t d_next = 0;
@@ -108,7 +107,7 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
 #pragma unroll
           for (int i = 0; i < U; i++) {
             const int v = v0 + 32 * i;
-            if (v < a.H8) x[kk][i] = ld_stream_hint(row + v, pol);
+            if (v < a.H8) x[kk][i] = ld_stream(row + v);
           }
         }
 #pragma unroll
@@ -136,7 +135,7 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
 #pragma unroll
     for (int i = 0; i < U; i++) {
       const int v = v0 + 32 * i;
-      if (v < a.H8) st_stream_hint(op + v, pack_bf16x8(acc[i]), pol);
+      if (v < a.H8) st_global(op + v, pack_bf16x8(acc[i]));
     }
   }
 }

@@ -47,7 +47,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
   const int64_t tok_units = a.ntok * a.nchunk;
   const int64_t P = a.meta[kMetaP];
   const int64_t units = tok_units + P * a.nchunk;
-  const uint64_t pol = l2_evict_first();
   // The next token unit's dst entries are loaded one unit ahead.
   int32_t d_next = 0;
   if (wid < tok_units && lane < K) d_next = __ldg(a.dst + (wid / a.nchunk) * K + lane);
@@ -74,7 +73,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
 #pragma unroll
       for (int i = 0; i < kU; i++) {
         const int v = v0 + 32 * i;
-        if (v < a.H8) x[i] = ld_stream_hint(src + v, pol);
+        if (v < a.H8) x[i] = ld_stream(src + v);
       }
       if (KT > 0) {
 #pragma unroll
@@ -85,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
 #pragma unroll
           for (int i = 0; i < kU; i++) {
             const int v = v0 + 32 * i;
-            if (v < a.H8) st_stream_hint(dp + v, x[i], pol);
+            if (v < a.H8) st_global(dp + v, x[i]);
           }
         }
       } else {
@@ -96,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
 #pragma unroll
           for (int i = 0; i < kU; i++) {
             const int v = v0 + 32 * i;
-            if (v < a.H8) st_stream_hint(dp + v, x[i], pol);
+            if (v < a.H8) st_global(dp + v, x[i]);
           }
         }
       }
@@ -122,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
 #pragma unroll
       for (int i = 0; i < kU; i++) {
         const int v = c * kChunk + lane + 32 * i;
-        if (v < a.H8) st_stream_hint(dp + v, z, pol);
+        if (v < a.H8) st_global(dp + v, z);
       }
       if (c == 0 && lane == 0 && a.w_out) a.w_out[g] = 0.0f;
     }

@@ -39,7 +39,6 @@ __global__ void __launch_bounds__(kThreads) prefetch_kernel(PrefetchArgs a) {
   const int64_t U = a.meta[kMetaU];
   const int64_t per_proj = U * a.nchunk;
   const int64_t units = per_proj * a.n_proj;
-  const uint64_t pol = l2_evict_first();
   for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
     const int p = (int)(unit / per_proj);
     const int64_t rem = unit - p * per_proj;
@@ -55,10 +54,10 @@ __global__ void __launch_bounds__(kThreads) prefetch_kernel(PrefetchArgs a) {
       uint4 x[kPU];
 #pragma unroll
       for (int i = 0; i < kPU; i++)
-        if (v + i * kThreads < v_end) x[i] = ld_stream_hint(src + v + i * kThreads, pol);
+        if (v + i * kThreads < v_end) x[i] = ld_stream(src + v + i * kThreads);
 #pragma unroll
       for (int i = 0; i < kPU; i++)
-        if (v + i * kThreads < v_end) st_stream_hint(dst + v + i * kThreads, x[i], pol);
+        if (v + i * kThreads < v_end) st_global(dst + v + i * kThreads, x[i]);
     }
   }
 }
@@ -89,7 +88,6 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
   const int64_t per_proj = D * a.nchunk;
   const int64_t units = per_proj * a.n_proj;
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  const uint64_t pol = l2_evict_first();
   for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
     const int p = (int)(unit / per_proj);
     const int64_t rem = unit - p * per_proj;
@@ -117,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
 #pragma unroll
       for (int i = 0; i < kRV; i++) {
         ok[i] = v + i * kThreads < v_end;
-        if (ok[i]) acc[i] = ld_once_f4_hint(home + v + i * kThreads, pol);
+        if (ok[i]) acc[i] = ld_once_f4(home + v + i * kThreads);
       }
       for (int f = 0; f < n; f += kNS) {
         float4 x[kNS][kRV];
@@ -126,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
           if (f + q < n) {
 #pragma unroll
             for (int i = 0; i < kRV; i++)
-              if (ok[i]) x[q][i] = ld_once_f4_hint(s_slot[f + q] + v + i * kThreads, pol);
+              if (ok[i]) x[q][i] = ld_once_f4(s_slot[f + q] + v + i * kThreads);
           }
         }
 #pragma unroll
@@ -139,14 +137,14 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
               acc[i].y = acc[i].y + x[q][i].y;
               acc[i].z = acc[i].z + x[q][i].z;
               acc[i].w = acc[i].w + x[q][i].w;
-              st_f4_hint(s_slot[f + q] + v + i * kThreads, zero, pol);
+              st_global_f4(s_slot[f + q] + v + i * kThreads, zero);
             }
           }
         }
       }
 #pragma unroll
       for (int i = 0; i < kRV; i++)
-        if (ok[i]) st_f4_hint(home + v + i * kThreads, acc[i], pol);
+        if (ok[i]) st_global_f4(home + v + i * kThreads, acc[i]);
     }
   }
 }
