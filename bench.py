@@ -191,7 +191,7 @@ class Step:
         b.reduce_grad(self.plan, [self.Gh], [self.Gs])
         rec(6)
 
-    LAUNCHES_PER_STEP = 8  # plan: 3 kernels; dispatch, prefetch, combine, dispatch, reduce
+    LAUNCHES_PER_STEP = 6  # plan (one cooperative launch), dispatch, prefetch, combine, dispatch, reduce
 
     def algorithmic_bytes(self):
         """Bytes each op must move (reads + writes), per launch."""
