@@ -57,6 +57,8 @@ def _bind(path):
     lib.mo_combine.argtypes = [ci] * 3 + [i64] * 4 + [vp, vp, i64, vp, vp, vp, vp]
     lib.mo_prefetch.restype = None
     lib.mo_prefetch.argtypes = [ci] * 3 + [vp, i64, i64, i64, vp]
+    lib.mo_prefetch_bytes.restype = None
+    lib.mo_prefetch_bytes.argtypes = [ci] * 3 + [vp, i64, i64, i64, vp]
     lib.mo_reduce.restype = None
     lib.mo_reduce.argtypes = [ci] * 3 + [vp, i64, i64, i64, vp, vp]
     lib.mo_f32_to_bf16.restype = ctypes.c_uint16
@@ -144,6 +146,15 @@ class Oracle:
         self.lib.mo_prefetch(R, E, B, _ptr(etc), HHp, c0, c1, _ptr(W))
         return W
 
+    def prefetch_bytes(self, R, E, B, etc, W, row_bytes, c0=0, c1=None):
+        """W [E + R*B, row_bytes] uint8 (packed MXFP4, block scales, any row
+        format seen as bytes), modified in place."""
+        c1 = row_bytes if c1 is None else c1
+        etc = np.ascontiguousarray(etc, dtype=np.int32)
+        assert W.dtype == np.uint8 and W.shape[-1] == row_bytes
+        self.lib.mo_prefetch_bytes(R, E, B, _ptr(etc), row_bytes, c0, c1, _ptr(W))
+        return W
+
     def reduce(self, R, E, B, etc, Gh, Gs, HHp, c0=0, c1=None):
         """Gh [E, HHp] fp32, Gs [R*B, HHp] fp32, modified in place."""
         c1 = HHp if c1 is None else c1
@@ -186,6 +197,10 @@ def combine(*a, **k):
 
 def prefetch(*a, **k):
     return _default().prefetch(*a, **k)
+
+
+def prefetch_bytes(*a, **k):
+    return _default().prefetch_bytes(*a, **k)
 
 
 def reduce(*a, **k):

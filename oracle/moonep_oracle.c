@@ -407,6 +407,23 @@ void mo_prefetch(int R, int E, int B, const int32_t *etc, int64_t HHp,
     }
 }
 
+/* Byte-row prefetch: the same slot fill for any row format, rows of
+ * row_bytes bytes, bytes [c0, c1) of each row.  Packed MXFP4 weights are
+ * uint8 (two 4-bit codes per byte) and their optional block-scale tensors
+ * share the leading E + B row convention, so a slot row receives its source
+ * row's bytes unchanged [API, Buffer.prefetch_weight: packed MXFP4 weights
+ * use uint8; block scales as a complete gate/up/down set]. */
+void mo_prefetch_bytes(int R, int E, int B, const int32_t *etc, int64_t row_bytes,
+                       int64_t c0, int64_t c1, uint8_t *W) {
+  for (int j = 0; j < R; j++)
+    for (int b = 0; b < B; b++) {
+      int e = etc[j * B + b];
+      if (e < 0) continue;
+      const int64_t dst_row = (int64_t)E + (int64_t)j * B + b;
+      for (int64_t c = c0; c < c1; c++) W[dst_row * row_bytes + c] = W[(int64_t)e * row_bytes + c];
+    }
+}
+
 /* -------------------------------------------------------------- reduce */
 
 /* For every expert with at least one slot copy: start from its own gradient,

@@ -82,6 +82,12 @@ void mo_combine(int R, int S, int K, int64_t NvS, int64_t H, int64_t c0,
 void mo_prefetch(int R, int E, int B, const int32_t *experts_to_copy,
                  int64_t HHp, int64_t c0, int64_t c1, uint16_t *W);
 
+/* Weight prefetch of rows of any format (packed MXFP4 uint8, block scales,
+ * bf16 seen as bytes): bytes [c0, c1) of rows of row_bytes bytes.
+ * W [E + R*B, row_bytes] bytes. */
+void mo_prefetch_bytes(int R, int E, int B, const int32_t *experts_to_copy,
+                       int64_t row_bytes, int64_t c0, int64_t c1, uint8_t *W);
+
 /* Gradient reduce, one projection, columns [c0, c1).
  * Gh [E, HHp] fp32, Gs [R*B, HHp] fp32. */
 void mo_reduce(int R, int E, int B, const int32_t *experts_to_copy,

@@ -44,6 +44,10 @@ MUTATIONS = {
     "reduce_keeps_slots": ("for (int64_t c = c0; c < c1; c++) Gs[(int64_t)i * HHp + c] = 0.0f;",
                            "for (int64_t c = c0; c < c1; c++) Gs[(int64_t)i * HHp + c] = Gs[(int64_t)i * HHp + c];"),
     "prefetch_skips_check": ("if (e < 0) continue;\n      int64_t slot", "if (e < 0) e = 0;\n      int64_t slot"),
+    "prefetch_bytes_wrong_slot": ("const int64_t dst_row = (int64_t)E + (int64_t)j * B + b;",
+                                  "const int64_t dst_row = (int64_t)E + (int64_t)b * R + j;"),
+    "prefetch_bytes_copies_unused": ("      if (e < 0) continue;\n      const int64_t dst_row",
+                                     "      if (e < 0) e = 0;\n      const int64_t dst_row"),
     "dispatch_no_weight_zero": ("if (w_out) w_out[g] = 0.0f;", "if (w_out) w_out[g] = w_out[g];"),
     "cu_exclusive": ("cu[(int64_t)j * EB + x] = (int32_t)end;", "cu[(int64_t)j * EB + x] = (int32_t)(end - padded);"),
     "slots_filled_from_end": ("etc[(int64_t)j * B + nslots] = e;", "etc[(int64_t)j * B + (B - 1 - nslots)] = e;"),
@@ -69,6 +73,8 @@ pins = [
     ("combine_bound", lambda: P.test_combine_within_one_ulp_of_exact_sum(o)),
     ("bf16_torch", lambda: P.test_bf16_rounding_matches_torch(o)),
     ("prefetch_copy", lambda: P.test_prefetch_copies_home_rows(o)),
+    ("prefetch_bytes", lambda: P.test_prefetch_bytes_copies_packed_rows(o)),
+    ("prefetch_bytes_window", lambda: P.test_prefetch_bytes_of_bf16_rows_is_the_bf16_prefetch(o)),
     ("reduce_const", lambda: P.test_reduce_constant_fill_counts_copies(o)),
     ("reduce_int", lambda: P.test_reduce_integer_values_exact(o)),
 ]

@@ -324,6 +324,61 @@ def test_prefetch_copies_home_rows(oracle_mod):
     assert np.array_equal(W[:sh.E], W0[:sh.E])
 
 
+def _mxfp4_set(sh, rng):
+    """A packed MXFP4 gate/up/down set with its E8M0 block scales: weights
+    [E + R*B, H, H'/2] uint8 (two 4-bit codes per byte), scales
+    [E + R*B, H, H'/32] uint8 (one exponent per 32 values)."""
+    rows = sh.E + sh.R * sh.B
+    w = [rng.integers(0, 256, (rows, sh.H * sh.Hp // 2), dtype=np.uint8) for _ in range(3)]
+    s = [rng.integers(0, 256, (rows, sh.H * sh.Hp // 32), dtype=np.uint8) for _ in range(3)]
+    return w + s
+
+
+def test_prefetch_bytes_copies_packed_rows(oracle_mod):
+    """Every used slot of every tensor of the set holds its source expert's
+    bytes, so its decoded 4-bit codes and scales are the source's; home rows
+    and unused slots keep theirs."""
+    sh, topk, p, x, w = _tiny_case(oracle_mod, 6)
+    etc = p["experts_to_copy"]
+    assert (etc >= 0).any() and (etc < 0).any()
+    rng = np.random.default_rng(2)
+    for T in _mxfp4_set(sh, rng):
+        T0 = T.copy()
+        oracle_mod.prefetch_bytes(sh.R, sh.E, sh.B, etc, T, T.shape[1])
+        for j in range(sh.R):
+            for b in range(sh.B):
+                row, src = sh.E + j * sh.B + b, etc[j, b]
+                assert np.array_equal(T[row], T0[src] if src >= 0 else T0[row])
+                if src >= 0:  # the two E2M1 codes of every byte
+                    assert np.array_equal(T[row] & 15, T0[src] & 15)
+                    assert np.array_equal(T[row] >> 4, T0[src] >> 4)
+        assert np.array_equal(T[:sh.E], T0[:sh.E])
+
+
+def test_prefetch_bytes_of_bf16_rows_is_the_bf16_prefetch(oracle_mod):
+    """bf16 rows seen as bytes: the byte copy and the element copy agree, and
+    a column window copies only its bytes."""
+    sh, topk, p, x, w = _tiny_case(oracle_mod, 4)
+    HHp = sh.H * sh.Hp
+    etc = p["experts_to_copy"]
+    rng = np.random.default_rng(5)
+    W = rng.integers(0, 65535, (sh.E + sh.R * sh.B, HHp)).astype(np.uint16)
+    Wb = W.copy().view(np.uint8)
+    oracle_mod.prefetch(sh.R, sh.E, sh.B, etc, W, HHp)
+    oracle_mod.prefetch_bytes(sh.R, sh.E, sh.B, etc, Wb, 2 * HHp)
+    assert np.array_equal(Wb.view(np.uint16), W)
+    Wc = rng.integers(0, 256, (sh.E + sh.R * sh.B, 64), dtype=np.uint8)
+    W0 = Wc.copy()
+    oracle_mod.prefetch_bytes(sh.R, sh.E, sh.B, etc, Wc, 64, c0=16, c1=40)
+    for j in range(sh.R):
+        for b in range(sh.B):
+            row, src = sh.E + j * sh.B + b, etc[j, b]
+            want = W0[row].copy()
+            if src >= 0:
+                want[16:40] = W0[src, 16:40]
+            assert np.array_equal(Wc[row], want)
+
+
 def test_reduce_constant_fill_counts_copies(oracle_mod):
     sh, topk, p, x, w = _tiny_case(oracle_mod, 5)
     etc = p["experts_to_copy"].reshape(-1)
