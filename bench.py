@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-mxfp4", action="store_true",
+                    help="skip the packed-MXFP4 weight prefetch measurement")
     ap.add_argument("--sweep-steps", type=int, default=30)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--graph", action="store_true",
@@ -248,6 +250,40 @@ def max_over_ranks(x, dist):
     t = torch.tensor([x], dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def run_mxfp4_prefetch(buf, step, sh, steps, torch, peak):
+    """The packed-MXFP4 form of the weight prefetch on the step's plan: a
+    gate/up/down set [E + R*B, H, H'/2] uint8 (two 4-bit codes per byte) with
+    its E8M0 block scales [E + R*B, H, H'/32] uint8, all six tensors moved by
+    one launch per call."""
+    rows = sh.E + sh.R * sh.B
+    g = torch.Generator(device="cuda")
+    g.manual_seed(17)
+    ts = [torch.randint(0, 256, (rows, sh.H, sh.Hp // 2), generator=g, dtype=torch.uint8,
+                        device="cuda") for _ in range(3)]
+    ts += [torch.randint(0, 256, (rows, sh.H, sh.Hp // 32), generator=g, dtype=torch.uint8,
+                         device="cuda") for _ in range(3)]
+    for _ in range(3):
+        buf.prefetch_weight(step.plan, *ts[:3], scales=ts[3:])
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        buf.prefetch_weight(step.plan, *ts[:3], scales=ts[3:])
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    U = step.algorithmic_bytes()[1]["U"]
+    nbytes = 2 * U * 3 * (sh.H * sh.Hp // 2 + sh.H * sh.Hp // 32)
+    del ts
+    torch.cuda.empty_cache()
+    return {"set": "gate/up/down packed MXFP4 [E+R*B, H, H'/2] uint8 + E8M0 block scales "
+                   "[E+R*B, H, H'/32] uint8, one launch",
+            "ms": round(ms, 5), "GB": round(nbytes / 1e9, 4), "slots_used": U,
+            "GBps": round(nbytes / (ms / 1e3) / 1e9, 1) if ms > 0 else None,
+            "frac_of_peak": round(nbytes / (ms / 1e3) / 1e9 / peak, 4) if ms > 0 else None}
 
 
 def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
@@ -635,6 +671,10 @@ def main():
             del s2
         torch.cuda.synchronize()
 
+    mxfp4 = None
+    if not args.no_mxfp4:
+        mxfp4 = run_mxfp4_prefetch(buf, step, sh, max(10, min(args.steps, 50)), torch, peak)
+
     e2e = None
     if not args.no_e2e:
         ms_e2e, bi, bo = run_e2e(buf, sh, topk_np, seed, args.e2e_steps, torch, dist)
@@ -663,7 +703,7 @@ def main():
                      "peak_source": peak_src, "traffic": recorded_traffic(dom, sh.name)},
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
-        "clocks": clocks, "sweep": sweep, "device_status": status,
+        "clocks": clocks, "sweep": sweep, "mxfp4_prefetch": mxfp4, "device_status": status,
     }
     if graph_ms is not None:
         line["graph_replay"] = {"ms_per_step": graph_ms,

@@ -249,23 +249,52 @@ class Buffer:
         return out, weights_out
 
     # --------------------------------------------------- weights / grads
-    def prefetch_weight(self, plan: CommPlan, *weights: torch.Tensor) -> None:
-        """Fill the prefetch slots of every [E + R*B, H, H'] bf16 tensor given
-        (gate, up, down, ...; at most 4) [Buffer.prefetch_weight]."""
+    def prefetch_weight(self, plan: CommPlan, *weights: torch.Tensor, scales=None) -> None:
+        """Fill the prefetch slots of every [E + R*B, ...] weight tensor given
+        (gate, up, down, ...; at most 4) [Buffer.prefetch_weight].  bf16
+        tensors [E + R*B, H, H'], or packed MXFP4 uint8 [E + R*B, H, H'/2]; with
+        `scales`, the block-scale tensors [E + R*B, ...] of the same set, one
+        per weight tensor (a complete set), all copied by one launch."""
         if not weights or len(weights) > 4:
             raise ValueError("prefetch_weight takes 1 to 4 weight tensors")
         rows = self.E + self.R * self.B
-        HHp = None
-        ptrs = []
-        for i, w in enumerate(weights):
-            hh = w[0].numel() if w.dim() > 1 else 0
-            HHp = hh if HHp is None else HHp
-            if hh != HHp:
-                raise ValueError("all weight tensors must share H*H'")
-            ptrs.append(_check_tensor(w, f"weight[{i}]", torch.bfloat16, (rows, *w.shape[1:])))
-        check(_lib.load().moonep_prefetch_weight(self._ctx, plan.struct, len(ptrs),
-                                                  _lib.ptr_array(ptrs), HHp, _stream()),
-              "moonep_prefetch_weight")
+        if scales is None and all(w.dtype == torch.bfloat16 for w in weights):
+            HHp = None
+            ptrs = []
+            for i, w in enumerate(weights):
+                hh = w[0].numel() if w.dim() > 1 else 0
+                HHp = hh if HHp is None else HHp
+                if hh != HHp:
+                    raise ValueError("all weight tensors must share H*H'")
+                ptrs.append(_check_tensor(w, f"weight[{i}]", torch.bfloat16, (rows, *w.shape[1:])))
+            check(_lib.load().moonep_prefetch_weight(self._ctx, plan.struct, len(ptrs),
+                                                      _lib.ptr_array(ptrs), HHp, _stream()),
+                  "moonep_prefetch_weight")
+            return
+        tensors = list(weights)
+        if scales is not None:
+            scales = list(scales)
+            if len(scales) != len(weights):
+                raise ValueError("scales must be a complete set: one per weight tensor")
+            tensors += scales
+        self.prefetch_rows(plan, tensors)
+
+    def prefetch_rows(self, plan: CommPlan, tensors) -> None:
+        """Fill the prefetch slots of up to 8 [E + R*B, ...] tensors of any
+        dtype (rows copied byte for byte) in one launch [Buffer.prefetch_weight]."""
+        tensors = list(tensors)
+        if not tensors or len(tensors) > 8:
+            raise ValueError("prefetch_rows takes 1 to 8 tensors")
+        rows = self.E + self.R * self.B
+        ptrs, rb = [], []
+        for i, t in enumerate(tensors):
+            _check_tensor(t, f"tensor[{i}]", t.dtype, (rows, *t.shape[1:]))
+            ptrs.append(t.data_ptr())
+            rb.append(t[0].numel() * t.element_size() if t.dim() > 1 else t.element_size())
+        arr = (ctypes.c_int64 * len(rb))(*rb)
+        check(_lib.load().moonep_prefetch_rows(self._ctx, plan.struct, len(ptrs),
+                                                _lib.ptr_array(ptrs), arr, _stream()),
+              "moonep_prefetch_rows")
 
     def reduce_grad(self, plan: CommPlan, grads, reduce_buffers) -> None:
         """Add the slot gradients into their home experts and clear the used

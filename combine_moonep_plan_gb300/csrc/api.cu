@@ -287,7 +287,24 @@ int moonep_prefetch_weight(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_
   if (!W || n_proj < 1 || n_proj > 4 || HHp < 0 || HHp % 8 != 0) return MOONEP_ERR_INVALID_ARG;
   for (int p = 0; p < n_proj; p++)
     if (!W[p] || !aligned16(W[p])) return MOONEP_ERR_INVALID_ARG;
-  return launch_prefetch(ctx, plan, n_proj, W, HHp, (cudaStream_t)stream);
+  void *T[4];
+  int64_t rb[4];
+  for (int p = 0; p < n_proj; p++) {
+    T[p] = W[p];
+    rb[p] = HHp * 2;
+  }
+  return launch_prefetch(ctx, plan, n_proj, T, rb, (cudaStream_t)stream);
+}
+
+int moonep_prefetch_rows(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_tensors,
+                         void *const *tensors, const int64_t *row_bytes, void *stream) {
+  int st = check_ctx(ctx);
+  if (st) return st;
+  if ((st = check_plan(ctx, plan))) return st;
+  if (!tensors || !row_bytes || n_tensors < 1 || n_tensors > 8) return MOONEP_ERR_INVALID_ARG;
+  for (int t = 0; t < n_tensors; t++)
+    if (row_bytes[t] < 0 || (row_bytes[t] > 0 && !tensors[t])) return MOONEP_ERR_INVALID_ARG;
+  return launch_prefetch(ctx, plan, n_tensors, tensors, row_bytes, (cudaStream_t)stream);
 }
 
 int moonep_reduce_redundant_grad(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj,

@@ -110,8 +110,8 @@ int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_
                     const float *w_sk, uint16_t *out, float *w_out, cudaStream_t st);
 int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *y,
                    const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st);
-int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj,
-                    uint16_t *const *W, int64_t HHp, cudaStream_t st);
+int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n, void *const *T,
+                    const int64_t *row_bytes, cudaStream_t st);
 int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, float *const *Gh,
                   float *const *Gs, int64_t HHp, cudaStream_t st);
 // Opt the planner kernels into the dynamic shared memory E experts need.

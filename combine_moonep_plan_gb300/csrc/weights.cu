@@ -15,7 +15,9 @@
 // rows that move.  Work units are 64 KB chunks of a row, strided over a
 // persistent grid.  Reduce reads each slot element once, adds it, and zeroes
 // it in the same thread, so no barrier separates the reduce and the clear.
-// HBM bytes: prefetch 2*U*HHp*2 per projection; reduce (2*D + 2*U)*HHp*4.
+// HBM bytes: prefetch 2*U*row_bytes per tensor (row_bytes = H*H'*2 for bf16,
+// H*H'/2 for packed MXFP4, H*H'/32 for its block scales); reduce
+// (2*D + 2*U)*HHp*4.
 #include "copy_common.cuh"
 #include "moonep_internal.cuh"
 
@@ -24,40 +26,60 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxProj = 4;
+constexpr int kMaxTensors = 8;   // prefetch: e.g. gate/up/down and their block scales
 constexpr int kChunkVec = 4096;  // 16-byte vectors per unit (64 KB)
 constexpr int kPU = 4;           // vectors per thread per step (prefetch)
 
+// Prefetch of n tensors whose expert rows have row_bytes[t] bytes each
+// (bf16 weights, packed MXFP4 bytes, block scales, ...).  A tensor whose
+// rows are 16-byte multiples on a 16-byte aligned base moves 16-byte vectors;
+// any other moves single bytes.
 struct PrefetchArgs {
-  uint4 *W[kMaxProj];
+  uint8_t *T[kMaxTensors];
+  int64_t row_bytes[kMaxTensors];
+  int64_t nchunk[kMaxTensors];  // 64 KB units per row
+  unsigned vec_mask;            // bit t: tensor t moves 16-byte vectors
   const int32_t *meta, *copy_slot, *copy_expert;
-  int n_proj, E;
-  int64_t vec_per_row;  // HHp / 8
-  int64_t nchunk;
+  int n, E;
 };
 
 __global__ void __launch_bounds__(kThreads) prefetch_kernel(PrefetchArgs a) {
   const int64_t U = a.meta[kMetaU];
-  const int64_t per_proj = U * a.nchunk;
-  const int64_t units = per_proj * a.n_proj;
+  int64_t units = 0;
+  for (int t = 0; t < a.n; t++) units += U * a.nchunk[t];
   for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
-    const int p = (int)(unit / per_proj);
-    const int64_t rem = unit - p * per_proj;
-    const int64_t s = rem / a.nchunk;
-    const int64_t c = rem - s * a.nchunk;
+    // unit -> (tensor, used slot, chunk); tensors in order, each U * nchunk units
+    int t = 0;
+    int64_t rem = unit;
+    while (t + 1 < a.n && rem >= U * a.nchunk[t]) {
+      rem -= U * a.nchunk[t];
+      t++;
+    }
+    const int64_t s = rem / a.nchunk[t];
+    const int64_t c = rem - s * a.nchunk[t];
     const int slot = a.copy_slot[s];
     const int e = a.copy_expert[s];
-    const uint4 *src = a.W[p] + (int64_t)e * a.vec_per_row;
-    uint4 *dst = a.W[p] + ((int64_t)a.E + slot) * a.vec_per_row;
-    const int64_t v_begin = c * kChunkVec;
-    const int64_t v_end = min(v_begin + kChunkVec, a.vec_per_row);
-    for (int64_t v = v_begin + threadIdx.x; v < v_end; v += kThreads * kPU) {
-      uint4 x[kPU];
+    const int64_t rb = a.row_bytes[t];
+    const uint8_t *src = a.T[t] + (int64_t)e * rb;
+    uint8_t *dst = a.T[t] + ((int64_t)a.E + slot) * rb;
+    if ((a.vec_mask >> t) & 1u) {
+      const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+      const int64_t v_begin = c * kChunkVec;
+      const int64_t v_end = min(v_begin + kChunkVec, rb / 16);
+      for (int64_t v = v_begin + threadIdx.x; v < v_end; v += kThreads * kPU) {
+        uint4 x[kPU];
 #pragma unroll
-      for (int i = 0; i < kPU; i++)
-        if (v + i * kThreads < v_end) x[i] = ld_stream(src + v + i * kThreads);
+        for (int i = 0; i < kPU; i++)
+          if (v + i * kThreads < v_end) x[i] = ld_stream(s4 + v + i * kThreads);
 #pragma unroll
-      for (int i = 0; i < kPU; i++)
-        if (v + i * kThreads < v_end) st_global(dst + v + i * kThreads, x[i]);
+        for (int i = 0; i < kPU; i++)
+          if (v + i * kThreads < v_end) st_global(d4 + v + i * kThreads, x[i]);
+      }
+    } else {
+      const int64_t b_begin = c * kChunkVec * 16;
+      const int64_t b_end = min(b_begin + (int64_t)kChunkVec * 16, rb);
+      for (int64_t v = b_begin + threadIdx.x; v < b_end; v += kThreads) dst[v] = src[v];
     }
   }
 }
@@ -167,22 +189,28 @@ int occupancy_reduce() {
   return n > 0 ? n : 1;
 }
 
-int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, uint16_t *const *W,
-                    int64_t HHp, cudaStream_t st) {
+int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n, void *const *T,
+                    const int64_t *row_bytes, cudaStream_t st) {
   const moonep_config &c = ctx->cfg;
-  if (n_proj < 1 || n_proj > kMaxProj) return MOONEP_ERR_INVALID_ARG;
+  if (n < 1 || n > kMaxTensors) return MOONEP_ERR_INVALID_ARG;
   PlanLayout lay = PlanLayout::make(c.R, c.E, c.B, ctx->NvS,
                                     (plan->flags & MOONEP_PLAN_DUP_RECORDS) != 0);
   PrefetchArgs a{};
-  for (int p = 0; p < n_proj; p++) a.W[p] = reinterpret_cast<uint4 *>(W[p]);
+  bool any = false;
+  for (int t = 0; t < n; t++) {
+    const int64_t rb = row_bytes[t];
+    a.T[t] = static_cast<uint8_t *>(T[t]);
+    a.row_bytes[t] = rb;
+    if (rb % 16 == 0 && aligned16(T[t])) a.vec_mask |= 1u << t;
+    a.nchunk[t] = (rb + (int64_t)kChunkVec * 16 - 1) / ((int64_t)kChunkVec * 16);
+    any = any || rb > 0;
+  }
   a.meta = plan->internal;
   a.copy_slot = plan->internal + lay.copy_slot;
   a.copy_expert = plan->internal + lay.copy_expert;
-  a.n_proj = n_proj;
+  a.n = n;
   a.E = c.E;
-  a.vec_per_row = HHp / 8;
-  a.nchunk = (a.vec_per_row + kChunkVec - 1) / kChunkVec;
-  if (a.vec_per_row == 0 || c.B == 0) return MOONEP_OK;
+  if (!any || c.B == 0) return MOONEP_OK;
   const int grid = ctx->sms * ctx->blocks_copy;
   prefetch_kernel<<<grid, kThreads, 0, st>>>(a);
   return cuda_status(cudaGetLastError());

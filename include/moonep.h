@@ -227,6 +227,23 @@ int moonep_prefetch_weight(moonep_ctx *ctx, const moonep_comm_plan *plan,
                            int n_proj, uint16_t *const *W, int64_t HHp,
                            void *stream);
 
+/* Weight prefetch of any row format [API, Buffer.prefetch_weight: packed
+ * MXFP4 weights are uint8; optional block-scale tensors follow the same
+ * leading E + B row convention and come as a complete gate/up/down set].
+ * tensors[t] (t < n_tensors <= 8) is a device pointer to an [E + R*B] array
+ * of rows of row_bytes[t] bytes each (packed MXFP4 [H, H'/2] bytes, E8M0
+ * block scales [H, H'/32] bytes, bf16 [H, H'] as 2*H*H' bytes, ...).  For
+ * every slot with experts_to_copy[j][b] = e >= 0 and every tensor: row
+ * E + j*B + b = row e, byte for byte.  Unused slots are not touched.  A
+ * tensor whose rows are 16-byte multiples on a 16-byte aligned base moves
+ * 16-byte vectors, any other single bytes (correct, slower).  Pass the whole
+ * set in one call: one launch covers every tensor.  `tensors` and
+ * `row_bytes` are host arrays; a tensor with row_bytes 0 is skipped (its
+ * pointer may be NULL). */
+int moonep_prefetch_rows(moonep_ctx *ctx, const moonep_comm_plan *plan,
+                         int n_tensors, void *const *tensors,
+                         const int64_t *row_bytes, void *stream);
+
 /* Gradient reduce of the redundant experts [API, Buffer.reduce_grad; README,
  * Weight buffer].  Gh[p] -> [E, HHp] fp32 home-expert gradients, Gs[p] ->
  * [R*B, HHp] fp32 slot gradients (the [R, B, H, H'] reduce buffer).  For

@@ -154,3 +154,49 @@ def test_full_size_parity(name, point):
         assert np.array_equal(Gs.view(R * B, -1)[:, a:b].cpu().numpy().view(np.uint32),
                               gs.view(np.uint32))
     buf.destroy()
+
+
+@pytest.mark.parametrize("name,point", [("deepseek_v3", 2.0), ("kimi_k2", "hot30")])
+def test_full_size_mxfp4_prefetch(name, point):
+    """A full-size packed MXFP4 gate/up/down set with its E8M0 block scales
+    ([E + R*B, H, H'/2] and [E + R*B, H, H'/32] uint8), one launch: every used
+    slot equals its source expert's row, every unused slot and home row keeps
+    its checksum."""
+    from combine_moonep_plan_gb300.api import Buffer
+    sh = wl.SHAPES[name]
+    R, E, B, H, Hp = sh.R, sh.E, sh.B, sh.H, sh.Hp
+    seed = wl.seed_for(name, 9)
+    topk = _routing(sh, point, seed)
+    st, op = oracle.plan(R, E, sh.K, sh.S, B, sh.tp, topk, wl.tokens_per_expert(topk, E),
+                         dup_records=False)
+    assert st == 0
+    etc = op["experts_to_copy"]
+    buf = Buffer(S=sh.S, H=H, K=sh.K, E=E, num_ep_ranks=R, B=B, token_padding=sh.tp,
+                 zero_copy_views=False)
+    plan = buf.plan(torch.from_numpy(topk).cuda())
+    rows = E + R * B
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    ts = [torch.randint(0, 256, (rows, H, Hp // 2), generator=g, device="cuda",
+                        dtype=torch.uint8) for _ in range(3)]
+    ts += [torch.randint(0, 256, (rows, H, Hp // 32), generator=g, device="cuda",
+                         dtype=torch.uint8) for _ in range(3)]
+
+    def sums(t):
+        return t.view(rows, -1).view(torch.int32).to(torch.int64).sum(dim=1).cpu()
+    before = [sums(t) for t in ts]
+    buf.prefetch_weight(plan, *ts[:3], scales=ts[3:])
+    assert buf.get_status() == 0
+    for t, b0 in zip(ts, before):
+        after = sums(t)
+        for j in range(R):
+            for b in range(B):
+                row = E + j * B + b
+                if etc[j, b] >= 0:
+                    assert torch.equal(t[row], t[etc[j, b]])
+                else:
+                    assert after[row] == b0[row]
+        assert torch.equal(after[:E], b0[:E])
+        del t
+    del ts
+    buf.destroy()

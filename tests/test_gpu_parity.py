@@ -310,6 +310,61 @@ def test_prefetch_and_reduce_parity(name, kind):
         assert np.array_equal(got_s.view(np.uint32), gs.view(np.uint32))
 
 
+@pytest.mark.parametrize("name,kind", [("tiny", "zipf"), ("deepseek_v3", "hot"),
+                                       ("kimi_k2", "hot")])
+def test_prefetch_mxfp4_set_parity(name, kind):
+    """A packed MXFP4 gate/up/down set with its E8M0 block scales, one launch:
+    every tensor byte-identical to the oracle's byte-row prefetch."""
+    sh = wl.SHAPES[name] if name == "tiny" else _small(name, 256)
+    cfg = _cfg_of(sh)
+    topk = _routing(sh, kind, 11)
+    st, op = _oracle_plan(cfg, topk)
+    assert st == 0
+    etc = op["experts_to_copy"]
+    assert (etc >= 0).any()
+    buf = _buffer(cfg, H=64)
+    plan = buf.plan(torch.from_numpy(topk).cuda())
+    H, Hp = 64, 2080                  # packed row 66,560 B: crosses a 64 KB unit
+    rows = sh.E + sh.R * sh.B
+    rng = np.random.default_rng(3)
+    packed = [rng.integers(0, 256, (rows, H * Hp // 2), dtype=np.uint8) for _ in range(3)]
+    scales = [rng.integers(0, 256, (rows, H * Hp // 32), dtype=np.uint8) for _ in range(3)]
+    pt = [torch.from_numpy(a).reshape(rows, H, Hp // 2).cuda() for a in packed]
+    stt = [torch.from_numpy(a).reshape(rows, H, Hp // 32).cuda() for a in scales]
+    buf.prefetch_weight(plan, *pt, scales=stt)
+    assert buf.get_status() == 0
+    for a, t in zip(packed + scales, pt + stt):
+        oracle.prefetch_bytes(sh.R, sh.E, sh.B, etc, a, a.shape[1])
+        assert np.array_equal(t.cpu().numpy().reshape(rows, -1), a)
+
+
+def test_prefetch_rows_odd_row_sizes():
+    """Rows that are not 16-byte multiples (and a tensor on an odd address)
+    take the byte path; a row size of 0 is skipped."""
+    sh = wl.SHAPES["tiny"]
+    cfg = _cfg_of(sh)
+    topk = _routing(sh, "zipf", 12)
+    st, op = _oracle_plan(cfg, topk)
+    etc = op["experts_to_copy"]
+    buf = _buffer(cfg, H=64)
+    plan = buf.plan(torch.from_numpy(topk).cuda())
+    rows = sh.E + sh.R * sh.B
+    rng = np.random.default_rng(4)
+    arrs = [rng.integers(0, 256, (rows, n), dtype=np.uint8) for n in (3, 40, 65537)]
+    ts = [torch.from_numpy(a).cuda() for a in arrs]
+    big = torch.from_numpy(rng.integers(0, 256, rows * 48 + 1, dtype=np.uint8)).cuda()
+    odd = big[1:].view(rows, 48)      # 48-byte rows on an odd base
+    odd_np = odd.cpu().numpy().copy()
+    empty = torch.empty((rows, 0), dtype=torch.uint8, device="cuda")
+    buf.prefetch_rows(plan, ts + [odd, empty])
+    assert buf.get_status() == 0
+    for a, t in zip(arrs + [odd_np], ts + [odd]):
+        oracle.prefetch_bytes(sh.R, sh.E, sh.B, etc, a, a.shape[1])
+        assert np.array_equal(t.cpu().numpy(), a)
+    with pytest.raises(ValueError):
+        buf.prefetch_weight(plan, ts[0], ts[1], scales=[ts[2]])
+
+
 # ------------------------------------------------------------- errors
 
 def test_device_errors_latch_status_without_faulting():
