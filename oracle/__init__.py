@@ -57,6 +57,8 @@ def _bind(path):
     lib.mo_combine.argtypes = [ci] * 3 + [i64] * 4 + [vp, vp, i64, vp, vp, vp, vp]
     lib.mo_prefetch.restype = None
     lib.mo_prefetch.argtypes = [ci] * 3 + [vp, i64, i64, i64, vp]
+    lib.mo_prepare.restype = None
+    lib.mo_prepare.argtypes = [ci] * 4 + [i64] + [vp] * 5
     lib.mo_prefetch_bytes.restype = None
     lib.mo_prefetch_bytes.argtypes = [ci] * 3 + [vp, i64, i64, i64, vp]
     lib.mo_reduce.restype = None
@@ -146,6 +148,17 @@ class Oracle:
         self.lib.mo_prefetch(R, E, B, _ptr(etc), HHp, c0, c1, _ptr(W))
         return W
 
+    def prepare(self, R, S, K, E, H, ntok, hidden, topk, w=None, want_tpe=True):
+        """Decode-path padding in place (hidden [R,S,H] uint16 or None, topk
+        [R,S,K] int32, w [R,S,K] fp32 or None); returns tokens_per_expert
+        [R,E] or None."""
+        nt = None if ntok is None else np.ascontiguousarray(ntok, dtype=np.int32)
+        tpe = np.zeros((R, E), np.int32) if want_tpe else None
+        assert topk.dtype == np.int32 and topk.flags["C_CONTIGUOUS"]
+        self.lib.mo_prepare(R, S, K, E, H, _ptr(nt), _ptr(hidden), _ptr(topk), _ptr(w),
+                            _ptr(tpe))
+        return tpe
+
     def prefetch_bytes(self, R, E, B, etc, W, row_bytes, c0=0, c1=None):
         """W [E + R*B, row_bytes] uint8 (packed MXFP4, block scales, any row
         format seen as bytes), modified in place."""
@@ -201,6 +214,10 @@ def prefetch(*a, **k):
 
 def prefetch_bytes(*a, **k):
     return _default().prefetch_bytes(*a, **k)
+
+
+def prepare(*a, **k):
+    return _default().prepare(*a, **k)
 
 
 def reduce(*a, **k):

@@ -331,6 +331,46 @@ out:
   return status;
 }
 
+/* ------------------------------------------------------------- prepare */
+
+/* Decode-path preparation, per rank r, following the padding step of the
+ * vLLM prepare/finalize page [vLLM, MoonEPPrepareAndFinalize._pad_to_capacity
+ * and prepare()]: (1) an invalid (negative) expert id becomes expert 0 with
+ * zero route weight; (2) the batch is padded to the static capacity S: rows
+ * s >= ntok[r] get a zero hidden row, expert 0 and zero weight; (3)
+ * tokens_per_expert is the per-rank count of the resulting ids (ids >= E are
+ * left for the planner to report and are not counted).  hidden, w and tpe
+ * may be NULL. */
+void mo_prepare(int R, int S, int K, int E, int64_t H, const int32_t *ntok,
+                uint16_t *hidden, int32_t *topk, float *w, int32_t *tpe) {
+  for (int r = 0; r < R; r++) {
+    const int n = ntok ? ntok[r] : S;
+    for (int s = 0; s < S; s++) {
+      const int64_t t = (int64_t)r * S + s;
+      for (int k = 0; k < K; k++) {
+        const int64_t i = t * K + k;
+        if (topk[i] < 0) {
+          topk[i] = 0;
+          if (w) w[i] = 0.0f;
+        }
+      }
+      if (s >= n) {
+        if (hidden)
+          for (int64_t c = 0; c < H; c++) hidden[t * H + c] = 0;
+        for (int k = 0; k < K; k++) {
+          topk[t * K + k] = 0;
+          if (w) w[t * K + k] = 0.0f;
+        }
+      }
+    }
+    if (tpe) {
+      for (int e = 0; e < E; e++) tpe[(int64_t)r * E + e] = 0;
+      for (int64_t i = (int64_t)r * S * K; i < (int64_t)(r + 1) * S * K; i++)
+        if (topk[i] < E) tpe[(int64_t)r * E + topk[i]]++;
+    }
+  }
+}
+
 /* ------------------------------------------------------------ dispatch */
 
 static int64_t decode_row(int32_t d) { return d >= 0 ? (int64_t)d : -(int64_t)d - 1; }

@@ -77,6 +77,13 @@ void mo_combine(int R, int S, int K, int64_t NvS, int64_t H, int64_t c0,
                 int64_t ntok, const uint16_t *y, const float *w_nvs,
                 uint16_t *out, float *w_out);
 
+/* Decode-path preparation, in place: ids < 0 -> expert 0 with weight 0;
+ * rows s >= ntok[r] (ntok NULL: none) -> zero hidden row, expert 0, weight 0;
+ * tpe [R,E] (optional) = per-rank counts of the resulting ids < E.
+ * hidden [R,S,H] bf16 bits or NULL, topk [R,S,K], w [R,S,K] or NULL. */
+void mo_prepare(int R, int S, int K, int E, int64_t H, const int32_t *ntok,
+                uint16_t *hidden, int32_t *topk, float *w, int32_t *tpe);
+
 /* Weight prefetch, one projection, columns [c0, c1) of rows of HHp elements.
  * W [E + R*B, HHp] bf16 bits. */
 void mo_prefetch(int R, int E, int B, const int32_t *experts_to_copy,

@@ -48,6 +48,10 @@ MUTATIONS = {
                                   "const int64_t dst_row = (int64_t)E + (int64_t)b * R + j;"),
     "prefetch_bytes_copies_unused": ("      if (e < 0) continue;\n      const int64_t dst_row",
                                      "      if (e < 0) e = 0;\n      const int64_t dst_row"),
+    "prepare_pad_off_by_one": ("      if (s >= n) {\n        if (hidden)", "      if (s > n) {\n        if (hidden)"),
+    "prepare_keeps_invalid_weight": ("          topk[i] = 0;\n          if (w) w[i] = 0.0f;", "          topk[i] = 0;"),
+    "prepare_counts_before_padding": ("    if (tpe) {\n      for (int e = 0; e < E; e++) tpe[(int64_t)r * E + e] = 0;",
+                                      "    if (tpe) {\n      for (int e = 0; e < E; e++) tpe[(int64_t)r * E + e] = (e == 0) ? -(S - n) * K : 0;"),
     "dispatch_no_weight_zero": ("if (w_out) w_out[g] = 0.0f;", "if (w_out) w_out[g] = w_out[g];"),
     "cu_exclusive": ("cu[(int64_t)j * EB + x] = (int32_t)end;", "cu[(int64_t)j * EB + x] = (int32_t)(end - padded);"),
     "slots_filled_from_end": ("etc[(int64_t)j * B + nslots] = e;", "etc[(int64_t)j * B + (B - 1 - nslots)] = e;"),
@@ -75,6 +79,8 @@ pins = [
     ("prefetch_copy", lambda: P.test_prefetch_copies_home_rows(o)),
     ("prefetch_bytes", lambda: P.test_prefetch_bytes_copies_packed_rows(o)),
     ("prefetch_bytes_window", lambda: P.test_prefetch_bytes_of_bf16_rows_is_the_bf16_prefetch(o)),
+    ("prepare_hand", lambda: P.test_prepare_hand_example(o)),
+    ("prepare_random", lambda: P.test_prepare_random_properties(o)),
     ("reduce_const", lambda: P.test_reduce_constant_fill_counts_copies(o)),
     ("reduce_int", lambda: P.test_reduce_integer_values_exact(o)),
 ]

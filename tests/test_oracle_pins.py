@@ -379,6 +379,57 @@ def test_prefetch_bytes_of_bf16_rows_is_the_bf16_prefetch(oracle_mod):
             assert np.array_equal(Wc[row], want)
 
 
+# ------------------------------------------------ decode-path preparation
+
+def test_prepare_hand_example(oracle_mod):
+    """Two ranks, capacity S = 4, K = 2, E = 4, H = 3, worked by hand from the
+    padding rule: a negative id becomes expert 0 with weight 0; rank 0 holds
+    2 valid tokens, so its rows 2 and 3 become zero rows routed to expert 0
+    with weight 0; rank 1 is full."""
+    R, S, K, E, H = 2, 4, 2, 4, 3
+    topk = np.array([[[1, -1], [3, 2], [2, 1], [0, 3]],
+                     [[-5, 2], [1, 1], [3, 0], [2, -1]]], np.int32)
+    w = np.array([[[.5, .5], [.3, .7], [.2, .8], [.9, .1]],
+                  [[.6, .4], [.5, .5], [.1, .9], [.7, .3]]], np.float32)
+    hidden = np.arange(1, R * S * H + 1, dtype=np.uint16).reshape(R, S, H)
+    h0 = hidden.copy()
+    tpe = oracle_mod.prepare(R, S, K, E, H, [2, 4], hidden, topk, w)
+    assert topk.tolist() == [[[1, 0], [3, 2], [0, 0], [0, 0]],
+                             [[0, 2], [1, 1], [3, 0], [2, 0]]]
+    assert np.array_equal(w, np.array([[[.5, 0], [.3, .7], [0, 0], [0, 0]],
+                                       [[0, .4], [.5, .5], [.1, .9], [.7, 0]]], np.float32))
+    assert np.array_equal(hidden[0, :2], h0[0, :2]) and np.all(hidden[0, 2:] == 0)
+    assert np.array_equal(hidden[1], h0[1])
+    # rank 0 ids 1,0,3,2,0,0,0,0; rank 1 ids 0,2,1,1,3,0,2,0
+    assert tpe.tolist() == [[5, 1, 1, 1], [3, 2, 2, 1]]
+
+
+def test_prepare_random_properties(oracle_mod):
+    """Random batches: valid rows with valid ids are untouched; a weight is
+    zeroed exactly where the id was negative or the row is padding; the
+    per-rank counts are numpy's bincount of the prepared ids; ids >= E stay
+    for the planner to report."""
+    rng = np.random.default_rng(8)
+    R, S, K, E, H = 3, 37, 4, 12, 5
+    topk = rng.integers(-3, E + 1, (R, S, K)).astype(np.int32)
+    w = rng.random((R, S, K)).astype(np.float32) + 0.5
+    hidden = rng.integers(1, 65535, (R, S, H)).astype(np.uint16)
+    n = np.array([0, 20, S], np.int32)
+    t0, w0, h0 = topk.copy(), w.copy(), hidden.copy()
+    tpe = oracle_mod.prepare(R, S, K, E, H, n, hidden, topk, w)
+    pad = np.arange(S)[None, :, None] >= n[:, None, None]
+    zero = (t0 < 0) | np.broadcast_to(pad, t0.shape)
+    assert np.array_equal(w == 0, zero)
+    assert np.array_equal(topk[~zero], t0[~zero]) and np.all(topk[zero] == 0)
+    assert np.array_equal(w[~zero], w0[~zero])
+    rows_pad = np.arange(S)[None, :] >= n[:, None]
+    assert np.all(hidden[rows_pad] == 0) and np.array_equal(hidden[~rows_pad], h0[~rows_pad])
+    for r in range(R):
+        ids = topk[r].reshape(-1)
+        assert np.array_equal(tpe[r], np.bincount(ids[ids < E], minlength=E))
+    assert (topk == E).any()
+
+
 def test_reduce_constant_fill_counts_copies(oracle_mod):
     sh, topk, p, x, w = _tiny_case(oracle_mod, 5)
     etc = p["experts_to_copy"].reshape(-1)
