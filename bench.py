@@ -286,6 +286,35 @@ def run_mxfp4_prefetch(buf, step, sh, steps, torch, peak):
             "frac_of_peak": round(nbytes / (ms / 1e3) / 1e9 / peak, 4) if ms > 0 else None}
 
 
+def run_prepare(buf, sh, steps, torch):
+    """The decode-path preparation on this shape: every rank holds 3/4 of the
+    capacity as real tokens (about 4 % of their ids invalid); the call pads
+    the rest in place and counts tokens_per_expert."""
+    R, S, K, E, H = sh.R, sh.S, sh.K, sh.E, sh.H
+    g = torch.Generator(device="cuda")
+    g.manual_seed(23)
+    n = [S - S // 4] * R
+    topk = torch.randint(0, E, (R, S, K), generator=g, device="cuda", dtype=torch.int32)
+    topk[torch.rand((R, S, K), generator=g, device="cuda") < 0.04] = -1
+    w = torch.rand((R, S, K), generator=g, device="cuda")
+    hidden = torch.randn((R, S, H), generator=g, device="cuda").to(torch.bfloat16)
+    for _ in range(3):
+        buf.prepare(hidden, topk, w, num_tokens=n)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        buf.prepare(hidden, topk, w, num_tokens=n)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / steps * 1e3
+    nbytes = R * S * K * 8 + R * E * 4 + R * (S // 4) * H * 2
+    del topk, w, hidden
+    return {"us": round(us, 2), "num_tokens_per_rank": n[0], "capacity": S,
+            "bytes": nbytes, "GBps": round(nbytes / (us / 1e6) / 1e9, 1)}
+
+
 def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
     """The same step through the public API with inputs in pinned host memory:
     every step copies its inputs host->device and reads the combined result
@@ -671,6 +700,8 @@ def main():
             del s2
         torch.cuda.synchronize()
 
+    prep = run_prepare(buf, sh, 50, torch)
+
     mxfp4 = None
     if not args.no_mxfp4:
         mxfp4 = run_mxfp4_prefetch(buf, step, sh, max(10, min(args.steps, 50)), torch, peak)
@@ -703,7 +734,8 @@ def main():
                      "peak_source": peak_src, "traffic": recorded_traffic(dom, sh.name)},
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
-        "clocks": clocks, "sweep": sweep, "mxfp4_prefetch": mxfp4, "device_status": status,
+        "clocks": clocks, "sweep": sweep, "mxfp4_prefetch": mxfp4, "decode_prepare": prep,
+        "device_status": status,
     }
     if graph_ms is not None:
         line["graph_replay"] = {"ms_per_step": graph_ms,

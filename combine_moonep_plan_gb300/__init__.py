@@ -16,7 +16,7 @@ def load_library():
 
 
 def __getattr__(name):
-    if name in ("Buffer", "CommPlan"):
+    if name in ("Buffer", "CommPlan", "BufferPool"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -31,7 +31,7 @@ EXPORTS = (
     "moonep_plan_clone", "moonep_plan", "moonep_dispatch", "moonep_combine",
     "moonep_prefetch_weight", "moonep_prefetch_rows", "moonep_reduce_redundant_grad", "moonep_hidden_view",
     "moonep_weight_view", "moonep_get_status", "moonep_strerror", "moonep_num_sms",
-    "moonep_plan_noalloc",
+    "moonep_plan_noalloc", "moonep_prepare",
 )
 
 
@@ -92,6 +92,7 @@ def load(path: str = LIB_PATH):
         "moonep_combine": (ci, [vp, planp, vp, vp, vp, vp, vp]),
         "moonep_prefetch_weight": (ci, [vp, planp, ci, ctypes.POINTER(vp), i64, vp]),
         "moonep_prefetch_rows": (ci, [vp, planp, ci, ctypes.POINTER(vp), ctypes.POINTER(i64), vp]),
+        "moonep_prepare": (ci, [vp, ctypes.POINTER(ctypes.c_int32), vp, vp, vp, vp, vp]),
         "moonep_reduce_redundant_grad": (ci, [vp, planp, ci, ctypes.POINTER(vp),
                                               ctypes.POINTER(vp), i64, vp]),
         "moonep_hidden_view": (vp, [vp, ci]),

@@ -296,6 +296,32 @@ class Buffer:
                                                 _lib.ptr_array(ptrs), arr, _stream()),
               "moonep_prefetch_rows")
 
+    def prepare(self, hidden: torch.Tensor | None, topk: torch.Tensor,
+                weights: torch.Tensor | None = None, num_tokens=None,
+                tokens_per_expert: bool = True) -> torch.Tensor | None:
+        """Pad this step's batch to the static capacity S and map invalid
+        (negative) expert ids to expert 0 with zero weight, in place
+        [vLLM MoonEPPrepareAndFinalize.prepare / _pad_to_capacity].  hidden
+        [R, S, H] bf16 (or None), topk [R, S, K] int32, weights [R, S, K] fp32
+        (or None): rank r's first num_tokens[r] rows hold its batch.  Returns
+        tokens_per_expert [R, E] int32 of the prepared ids (or None)."""
+        R, S, K, H = self.R, self.S, self.K, self.H
+        hp = _check_tensor(hidden, "hidden", torch.bfloat16, (R, S, H)) if hidden is not None else None
+        tp = _check_tensor(topk, "topk", torch.int32, (R, S, K))
+        wp = _check_tensor(weights, "weights", torch.float32, (R, S, K)) if weights is not None else None
+        nt = None
+        if num_tokens is not None:
+            vals = [int(v) for v in (num_tokens.tolist() if torch.is_tensor(num_tokens)
+                                     else num_tokens)]
+            if len(vals) != R:
+                raise ValueError(f"num_tokens: expected {R} values")
+            nt = (ctypes.c_int32 * R)(*vals)
+        tpe = torch.empty((R, self.E), dtype=torch.int32, device="cuda") if tokens_per_expert else None
+        check(_lib.load().moonep_prepare(self._ctx, nt, hp, tp, wp,
+                                         tpe.data_ptr() if tpe is not None else None, _stream()),
+              "moonep_prepare")
+        return tpe
+
     def reduce_grad(self, plan: CommPlan, grads, reduce_buffers) -> None:
         """Add the slot gradients into their home experts and clear the used
         slots [Buffer.reduce_grad].  grads: [E, H, H'] fp32 tensors;
@@ -323,3 +349,45 @@ class Buffer:
         check(_lib.load().moonep_get_status(self._ctx, ctypes.byref(v), _stream()),
               "moonep_get_status")
         return v.value
+
+
+class BufferPool:
+    """Buffers at power-of-two token capacities, created on first use
+    [vLLM MoonEPBufferPool].  A Buffer fixes its capacity S, so one
+    full-capacity buffer would pad every step to max_tokens_per_rank; the
+    pool serves the smallest power of two that holds the step's token count
+    (at least min_tokens, at most max_tokens_per_rank).  Every caller that
+    must agree on the buffer (all ranks of a step) passes the same count."""
+
+    def __init__(self, max_tokens_per_rank: int, min_tokens: int = 1, **buffer_kwargs):
+        if max_tokens_per_rank < 1 or min_tokens < 1:
+            raise ValueError("max_tokens_per_rank and min_tokens must be >= 1")
+        buffer_kwargs.pop("S", None)
+        self.max_tokens_per_rank = max_tokens_per_rank
+        self.min_tokens = min_tokens
+        self._kwargs = buffer_kwargs
+        self._buffers: dict[int, Buffer] = {}
+
+    def capacity_for(self, num_tokens: int) -> int:
+        if num_tokens >= self.max_tokens_per_rank:
+            return self.max_tokens_per_rank
+        cap = 1 << max(num_tokens - 1, 0).bit_length()
+        return min(max(cap, self.min_tokens), self.max_tokens_per_rank)
+
+    def get(self, num_tokens: int) -> tuple[int, Buffer]:
+        """(capacity, buffer) for a step of num_tokens tokens per rank."""
+        cap = self.capacity_for(num_tokens)
+        buf = self._buffers.get(cap)
+        if buf is None:
+            buf = Buffer(S=cap, **self._kwargs)
+            self._buffers[cap] = buf
+        return cap, buf
+
+    @property
+    def capacities(self) -> list[int]:
+        return sorted(self._buffers)
+
+    def destroy(self) -> None:
+        for buf in self._buffers.values():
+            buf.destroy()
+        self._buffers.clear()

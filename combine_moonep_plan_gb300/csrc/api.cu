@@ -307,6 +307,21 @@ int moonep_prefetch_rows(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_te
   return launch_prefetch(ctx, plan, n_tensors, tensors, row_bytes, (cudaStream_t)stream);
 }
 
+int moonep_prepare(moonep_ctx *ctx, const int32_t *num_tokens, uint16_t *hidden,
+                   int32_t *topk, float *w_sk, int32_t *tokens_per_expert, void *stream) {
+  int st = check_ctx(ctx);
+  if (st) return st;
+  const moonep_config &c = ctx->cfg;
+  if ((int64_t)c.S * c.K > 0 && !topk) return MOONEP_ERR_INVALID_ARG;
+  if (hidden && !aligned16(hidden)) return MOONEP_ERR_INVALID_ARG;
+  if (num_tokens)
+    for (int r = 0; r < c.R; r++)
+      if (num_tokens[r] < 0 || num_tokens[r] > c.S) return MOONEP_ERR_INVALID_ARG;
+  if ((int64_t)c.R * c.S == 0) return MOONEP_OK;
+  return launch_prepare(ctx, num_tokens, hidden, topk, w_sk, tokens_per_expert,
+                        (cudaStream_t)stream);
+}
+
 int moonep_reduce_redundant_grad(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj,
                                  float *const *Gh, float *const *Gs, int64_t HHp,
                                  void *stream) {

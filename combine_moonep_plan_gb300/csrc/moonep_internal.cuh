@@ -112,6 +112,8 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
                    const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st);
 int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n, void *const *T,
                     const int64_t *row_bytes, cudaStream_t st);
+int launch_prepare(moonep_ctx *ctx, const int32_t *num_tokens, uint16_t *hidden,
+                   int32_t *topk, float *w, int32_t *tpe, cudaStream_t st);
 int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, float *const *Gh,
                   float *const *Gs, int64_t HHp, cudaStream_t st);
 // Opt the planner kernels into the dynamic shared memory E experts need.

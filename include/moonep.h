@@ -244,6 +244,24 @@ int moonep_prefetch_rows(moonep_ctx *ctx, const moonep_comm_plan *plan,
                          int n_tensors, void *const *tensors,
                          const int64_t *row_bytes, void *stream);
 
+/* Decode-path preparation [vLLM, MoonEPPrepareAndFinalize: prepare() and
+ * _pad_to_capacity]: the step's batch is padded to the context's static
+ * capacity S, and invalid (negative) expert ids become expert 0 with zero
+ * route weight (the planner has no sentinel for them), in place:
+ *   num_tokens  HOST array [R]: valid tokens of each rank, 0 <= n <= S
+ *               (NULL: S for every rank, only invalid ids are mapped)
+ *   hidden      [R, S, H] bf16 or NULL, 16-byte aligned: rows s >= n of rank
+ *               r are set to 0
+ *   topk        [R, S, K] int32: ids < 0, and every id of rows s >= n, set
+ *               to 0; ids >= E are left for the planner to report
+ *   w_sk        [R, S, K] fp32 or NULL: the weights of those routes set to 0
+ *   tokens_per_expert  [R, E] int32 out or NULL: per-rank counts of the
+ *               prepared ids below E (the planner's tokens_per_expert)
+ * Only padding rows and invalid routes are written. */
+int moonep_prepare(moonep_ctx *ctx, const int32_t *num_tokens, uint16_t *hidden,
+                   int32_t *topk, float *w_sk, int32_t *tokens_per_expert,
+                   void *stream);
+
 /* Gradient reduce of the redundant experts [API, Buffer.reduce_grad; README,
  * Weight buffer].  Gh[p] -> [E, HHp] fp32 home-expert gradients, Gs[p] ->
  * [R*B, HHp] fp32 slot gradients (the [R, B, H, H'] reduce buffer).  For

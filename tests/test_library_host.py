@@ -74,6 +74,23 @@ def test_null_arguments_rejected(lib):
     assert lib.moonep_ctx_destroy(None) == 0          # idempotent on NULL
     assert lib.moonep_hidden_view(None, 0) is None
     assert lib.moonep_plan_destroy(None) == 0
+    assert lib.moonep_prepare(None, None, None, None, None, None, None) == ERR_INVALID_ARG
+    assert lib.moonep_prefetch_rows(None, None, 1, None, None, None) == ERR_INVALID_ARG
+
+
+def test_buffer_pool_capacities():
+    """Smallest power of two holding the step's tokens, within [min, max]
+    [vLLM MoonEPBufferPool.capacity_for]; no buffer exists before get()."""
+    from combine_moonep_plan_gb300.api import BufferPool
+    pool = BufferPool(max_tokens_per_rank=4096, min_tokens=16, H=64, K=2, E=8, num_ep_ranks=2)
+    ns = (0, 1, 2, 3, 16, 17, 100, 128, 129, 4095, 4096, 5000)
+    assert [pool.capacity_for(n) for n in ns] == [16, 16, 16, 16, 16, 32, 128, 128, 256,
+                                                  4096, 4096, 4096]
+    pool2 = BufferPool(max_tokens_per_rank=100)
+    assert [pool2.capacity_for(n) for n in (0, 1, 2, 3, 64, 65, 99, 100, 101)] == \
+        [1, 1, 2, 4, 64, 100, 100, 100, 100]
+    assert pool.capacities == [] and pool2.capacities == []
+    pool.destroy()
 
 
 def test_strerror_texts(lib):
