@@ -488,3 +488,84 @@ def test_maxvio_closed_form():
     T = np.bincount(topk.reshape(-1), minlength=sh.E)
     assert abs(info["maxvio"] - (T.max() / (sh.N / sh.E) - 1)) < 1e-12
     assert abs(info["maxvio"] - 2.0) <= 0.02
+
+
+# ------------------------------------------------ brute force on tiny inputs
+
+def _balanced_count_matrices(T, R, L, C, B):
+    """Every [E, R] matrix x of route counts with row sums T_e (each expert's
+    routes all placed), column sums C (every rank holds exactly S*K) and at
+    most B experts with x > 0 on a rank outside its home group."""
+    E = len(T)
+    out = []
+    x = np.zeros((E, R), np.int64)
+
+    def place(e, left):
+        if e == E:
+            if all(v == 0 for v in left):
+                out.append(x.copy())
+            return
+
+        def split(j, rem):
+            if j == R - 1:
+                if rem <= left[j]:
+                    x[e, j] = rem
+                    left[j] -= rem
+                    place(e + 1, left)
+                    left[j] += rem
+                    x[e, j] = 0
+                return
+            for v in range(min(rem, left[j]) + 1):
+                x[e, j] = v
+                left[j] -= v
+                split(j + 1, rem - v)
+                left[j] += v
+            x[e, j] = 0
+
+        split(0, T[e])
+
+    place(0, [C] * R)
+    ok = []
+    for m in out:
+        remote = [sum(1 for e in range(E) if e // L != j and m[e, j] > 0) for j in range(R)]
+        if max(remote) <= B:
+            ok.append(m)
+    return ok
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_brute_force_tiny_balanced_assignments(oracle_mod, seed):
+    """R <= 3, E <= 6, C <= 4: enumerate every balanced assignment of route
+    counts with at most B remote experts per rank.  The oracle's plan is one
+    of them; with B >= E/R the chain rule always succeeds; its moved-route
+    count is never below the enumerated minimum, which is never below the
+    overload lower bound.  With B < E/R the chain may report too few slots
+    although some balanced assignment fits (seed 23: R=2, L=2, C=4, B=1):
+    the rule is not slot-optimal, which the reading for B < E/R accepts."""
+    rng = np.random.default_rng(1000 + seed)
+    R = int(rng.integers(2, 4))
+    L = int(rng.integers(1, 6 // R + 1))
+    E = R * L
+    K = int(rng.integers(1, 3))
+    S = int(rng.integers(1, 4 // K + 1))
+    C = S * K
+    B = int(rng.integers(0, L + 1))
+    skew = rng.random(E) ** 2 + 1e-3
+    topk = rng.choice(E, size=(R, S, K), p=skew / skew.sum()).astype(np.int32)
+    T = np.bincount(topk.reshape(-1), minlength=E)
+    feasible = _balanced_count_matrices(list(T), R, L, C, B)
+    cfg = dict(R=R, E=E, K=K, S=S, B=B, tp=1)
+    st, p = _plan(oracle_mod, cfg, topk)
+    if B >= L:
+        assert st == 0
+    if st != 0:  # B < E/R: the chain needs more slots than B
+        assert st == -4 and B < L
+        return
+    rank_of = decode(p["dst"]).reshape(-1) // p["NvS"]
+    x = np.zeros((E, R), np.int64)
+    np.add.at(x, (topk.reshape(-1), rank_of), 1)
+    assert any(np.array_equal(x, m) for m in feasible)
+    moved = lambda m: sum(int(m[e, j]) for e in range(E) for j in range(R) if e // L != j)
+    best = min(moved(m) for m in feasible)
+    G = [int(T[j * L:(j + 1) * L].sum()) for j in range(R)]
+    assert moved(x) >= best >= sum(max(0, g - C) for g in G)
