@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "plan+dispatch+combine tokens/s and effective HBM GB/s vs ~8 TB/s, per maxvio"
 SWEEPS = {"tiny": [1.0], "mixtral": [0.0, 0.5, 1.0, 2.0, 3.0],
           "deepseek_v3": [0.0, 1.0, 2.0, 4.0], "kimi_k2": ["hot30", "hot9"],
-          "qwen3_decode": ["uniform", "zipf1"]}
+          "qwen3_decode": ["uniform", "zipf1", "pad100"]}
 HEADLINE = {"tiny": 1.0, "mixtral": 1.0, "deepseek_v3": 1.0, "kimi_k2": "hot30",
             "qwen3_decode": "zipf1"}
 
@@ -76,6 +76,16 @@ def make_routing(sh, point, seed):
         return wl.routing(sh, "uniform", seed=seed)
     if point == "zipf1":
         return wl.routing(sh, "zipf", zipf_s=1.0, seed=seed)
+    if point == "pad100":
+        # 100 real tokens per rank, padded to the capacity: padding routes go
+        # to expert 0 (with zero weight), as the decode-path preparation does
+        topk, info = wl.routing(sh, "zipf", zipf_s=1.0, seed=seed)
+        topk = topk.copy()
+        topk[:, 100:, :] = 0
+        info = dict(info, padded_from=100,
+                    maxvio=float(np.bincount(topk.reshape(-1), minlength=sh.E).max()
+                                 / (sh.N / sh.E) - 1))
+        return topk, info
     mv = float(point)
     if mv == 0.0 and (sh.N % sh.E == 0):
         return wl.routing(sh, "exact0", seed=seed)
@@ -243,6 +253,41 @@ def timed_steps(step, steps, torch, dist=None):
     return total, per_op, (t0, t1)
 
 
+def time_chain(step, n, torch, graph=False):
+    """plan -> dispatch -> combine back to back, timed as one chain (no
+    events between the ops); ms per chain, eagerly issued or (graph=True)
+    replayed from a CUDA graph of the chain."""
+    b = step.buf
+
+    def chain():
+        b.plan(step.topk, step.tpe, plan=step.plan)
+        b.dispatch(step.hidden, step.w_sk, plan=step.plan, out=step.hid_nvsh,
+                   weights_out=step.w_nvs)
+        b.combine(step.plan, step.hid_nvsh, step.w_nvs, out=step.out, weights_out=step.w_back)
+    run = chain
+    if graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            chain()
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            chain()
+        run = g.replay
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
 def max_over_ranks(x, dist):
     if dist is None:
         return x
@@ -298,17 +343,28 @@ def run_prepare(buf, sh, steps, torch):
     topk[torch.rand((R, S, K), generator=g, device="cuda") < 0.04] = -1
     w = torch.rand((R, S, K), generator=g, device="cuda")
     hidden = torch.randn((R, S, H), generator=g, device="cuda").to(torch.bfloat16)
-    for _ in range(3):
-        buf.prepare(hidden, topk, w, num_tokens=n)
+    # timed as CUDA-graph replays: the GPU time of the call, not the Python
+    # wrapper's issue rate
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            buf.prepare(hidden, topk, w, num_tokens=n)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(10):
+            buf.prepare(hidden, topk, w, num_tokens=n)
+    graph.replay()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(steps):
-        buf.prepare(hidden, topk, w, num_tokens=n)
+        graph.replay()
     b.record()
     torch.cuda.synchronize()
-    us = a.elapsed_time(b) / steps * 1e3
+    us = a.elapsed_time(b) / (10 * steps) * 1e3
     nbytes = R * S * K * 8 + R * E * 4 + R * (S // 4) * H * 2
     del topk, w, hidden
     return {"us": round(us, 2), "num_tokens_per_rank": n[0], "capacity": S,
@@ -473,9 +529,33 @@ def reference_arm(args, sh, point, topk_np, seed, dist):
             "data": "synthetic", "impl": "reference",
             "config": workload_config(sh, point),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": sample, "wall_s": wall},
+                             "sample": sample, "wall_s": wall, "host": host_info()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def host_info():
+    """The host cores the CPU baseline runs on: count, model, memory."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware") and model is None:
+                    model = ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    ram = None
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemTotal:"):
+                    ram = round(int(ln.split()[1]) / 2**20, 1)
+    except OSError:
+        pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model, "machine": platform.machine(),
+            "ram_gib": ram}
 
 
 def recorded_traffic(op, config):
@@ -674,7 +754,12 @@ def main():
     ops = {o: {"ms": round(op_ms[o], 5), "GB": round(alg[o] / 1e9, 4),
                "GBps": round(alg[o] / (op_ms[o] / 1e3) / 1e9, 1) if op_ms[o] > 0 else None,
                "frac_of_peak": round(alg[o] / (op_ms[o] / 1e3) / 1e9 / peak, 4)
-               if op_ms[o] > 0 else None} for o in OPS}
+               if op_ms[o] > 0 else None,
+               "ms_p10_p50_p90": [round(float(np.percentile(per_op[o], q)), 5)
+                                  for q in (10, 50, 90)]} for o in OPS}
+    chain_ms = time_chain(step, max(20, min(args.steps, 200)), torch)
+    chain_graph_ms = (time_chain(step, max(20, min(args.steps, 200)), torch, graph=True)
+                      if args.graph else None)
     step_bytes = sum(alg.values())
 
     sweep = []
@@ -700,7 +785,7 @@ def main():
             del s2
         torch.cuda.synchronize()
 
-    prep = run_prepare(buf, sh, 50, torch)
+    prep = run_prepare(buf, sh, 20, torch)
 
     mxfp4 = None
     if not args.no_mxfp4:
@@ -716,7 +801,7 @@ def main():
     if not args.no_cpu_baseline and rank == 0:
         v, step_s, per, sample = cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20)
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
-               "step_s": step_s}
+               "step_s": step_s, "host": host_info()}
 
     status = buf.get_status()
     line = {
@@ -726,6 +811,9 @@ def main():
         "data": "synthetic", "config": workload_config(sh, point),
         "routing": {k: v for k, v in rinfo.items() if k != "hot"},
         "plan_dispatch_combine_tokens_per_s": R_S(sh) * world / (pdc_ms / 1e3),
+        "plan_dispatch_combine_chain": {
+            "ms": round(chain_ms, 5), "tokens_per_s": R_S(sh) * world / (chain_ms / 1e3),
+            "graph_ms": round(chain_graph_ms, 5) if chain_graph_ms else None},
         "plan_frac_of_dispatch": op_ms["plan"] / op_ms["dispatch"],
         "step_hbm_GBps": step_bytes / (ms_per_step / 1e3) / 1e9,
         "ops": ops, "plan_counts": counts,
