@@ -20,17 +20,23 @@
 //   is a local duplicate, encoded -(g+1).
 //
 // Kernels:
+//   plan_fused_kernel<IT>  the usual path, one cooperative launch: tile CTAs
+//                          count and order their routes, all CTAs meet once,
+//                          each runs the balance step's routing stage on its
+//                          own copy of the per-rank totals and assigns its
+//                          routes; one extra CTA writes the plan's tables.
+//   The tile path (K not dividing 32, or tables too large for one CTA):
 //   K1 plan_hist_kernel    per 2048-route tile: per-expert counts and each
 //                          route's ordinal among same-expert routes of the tile
-//                          (warp-aggregated with __match_any_sync, stable).
+//                          (warp-aggregated with one ballot per key bit, stable).
 //   K2 plan_balance_kernel one CTA: column scans of the tile counts (the
 //                          position of every tile inside every P_e), the chain
 //                          balance, slots, segments, cu_seqlens, padding and
 //                          the copy / reduce lists.
 //   K3 plan_assign_kernel  one thread per token: Q position -> (rank, row),
 //                          duplicate encoding, dup_counts.
-//   K4 plan_dup_kernel     (optional) one CTA per rank: compact duplicate
-//                          records in ascending primary row.
+//   K4 plan_dup_kernel     (optional, either path) one CTA per rank: compact
+//                          duplicate records in ascending primary row.
 #include "moonep_internal.cuh"
 
 namespace moonep {

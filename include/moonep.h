@@ -20,7 +20,9 @@
  *   - Arrays are dense, row-major, and live in device memory unless stated.
  *     bf16 tensors travel as uint16_t bit patterns.
  *   - Every device pointer must be 16-byte aligned; H % 8 == 0 and, for the
- *     weight entry points, HHp % 8 == 0 (16-byte rows).
+ *     weight entry points, HHp % 8 == 0 (16-byte rows).  moonep_prefetch_rows
+ *     takes any alignment and row size (other than 16-byte multiples on a
+ *     16-byte aligned base, rows move byte by byte).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
  *     is stream-ordered and asynchronous: nothing synchronises with the host
  *     except moonep_get_status, moonep_ctx_destroy and moonep_plan_destroy
@@ -283,8 +285,11 @@ void *moonep_hidden_view(moonep_ctx *ctx, int rank);
 void *moonep_weight_view(moonep_ctx *ctx, int rank);
 
 /* Synchronise `stream`, return the first error any kernel latched since the
- * last call in *device_status (0 if none) and clear it.  The return value is
- * the host-side status of the query itself. */
+ * last call in *device_status (0 if none) and clear it.  After
+ * MOONEP_ERR_TIMEOUT it also clears the planner's cross-block counters and
+ * accumulators (a wait that ran out may leave them out of step), so the
+ * context plans correctly again; re-plan before reusing a plan from that
+ * call.  The return value is the host-side status of the query itself. */
 int moonep_get_status(moonep_ctx *ctx, int *device_status, void *stream);
 
 /* Static text for a status code. */
