@@ -94,80 +94,90 @@ struct ReduceArgs {
 };
 
 constexpr int kRedChunk = 2048;  // float4 per unit (32 KB of the home row)
-constexpr int kRV = 2;           // float4 per thread per round
-constexpr int kNS = 7;           // slot rows loaded together with the home row
 constexpr int kMaxSlotsPerExpert = 256;
 
+// Columns [v_begin, v_end) of one expert: acc = home, then each slot in list
+// order (acc = acc + slot), slot elements zeroed, home = acc.  A thread holds
+// RV columns and loads the home element and up to NS slot elements of each
+// together (RV * (1 + NS) loads in flight), so one round trip to memory
+// covers several rows of the column.
+template <int RV, int NS>
+__device__ __forceinline__ void reduce_columns(float4 *home, float4 *const *slot, int n,
+                                               int64_t v_begin, int64_t v_end) {
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t v = v_begin + threadIdx.x; v < v_end; v += RV * kThreads) {
+    bool ok[RV];
+    float4 acc[RV];
+#pragma unroll
+    for (int i = 0; i < RV; i++) {
+      ok[i] = v + i * kThreads < v_end;
+      if (ok[i]) acc[i] = ld_once_f4(home + v + i * kThreads);
+    }
+    for (int f = 0; f < n; f += NS) {
+      float4 x[NS][RV];
+#pragma unroll
+      for (int q = 0; q < NS; q++) {
+        if (f + q < n) {
+#pragma unroll
+          for (int i = 0; i < RV; i++)
+            if (ok[i]) x[q][i] = ld_once_f4(slot[f + q] + v + i * kThreads);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NS; q++) {
+        if (f + q < n) {
+#pragma unroll
+          for (int i = 0; i < RV; i++) {
+            if (!ok[i]) continue;
+            acc[i].x = acc[i].x + x[q][i].x;
+            acc[i].y = acc[i].y + x[q][i].y;
+            acc[i].z = acc[i].z + x[q][i].z;
+            acc[i].w = acc[i].w + x[q][i].w;
+            st_global_f4(slot[f + q] + v + i * kThreads, zero);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < RV; i++)
+      if (ok[i]) st_global_f4(home + v + i * kThreads, acc[i]);
+  }
+}
+
 // One unit = one 32 KB chunk of one expert's row (and of its slot rows).  A
-// thread loads the home element and up to kNS slot elements together, adds
-// them in slot-list order, zeroes the slot elements and stores the sum, so a
-// round trip to memory covers the whole column instead of one row at a time.
-__global__ void __launch_bounds__(kThreads) reduce_kernel(ReduceArgs a) {
+// thread takes four columns and two slot rows at a time: 8 loads in flight
+// for an expert with one copy, 12 for more; within 64 registers, so four
+// blocks fit on an SM.  The slot list of the unit's expert is staged in
+// shared memory once per expert.
+__global__ void __launch_bounds__(kThreads, 4) reduce_kernel(ReduceArgs a) {
   __shared__ float4 *s_slot[kMaxSlotsPerExpert];
   __shared__ float4 *s_home;
   __shared__ int s_n;
   const int64_t D = a.meta[kMetaD];
   const int64_t per_proj = D * a.nchunk;
   const int64_t units = per_proj * a.n_proj;
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  int64_t staged = -1;  // p * D + di of the staged slot list
   for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
     const int p = (int)(unit / per_proj);
     const int64_t rem = unit - p * per_proj;
     const int64_t di = rem / a.nchunk;
     const int64_t c = rem - di * a.nchunk;
-    __syncthreads();  // the previous unit is done with the shared pointers
-    if (threadIdx.x == 0) {
+    if (p * D + di != staged) {
+      __syncthreads();  // the previous expert's list is no longer read
       const int f0 = a.red_first[di], f1 = a.red_first[di + 1];
-      s_n = min(f1 - f0, kMaxSlotsPerExpert);
-      s_home = a.Gh[p] + (int64_t)a.red_expert[di] * a.vec_per_row;
-    }
-    {
-      const int f0 = a.red_first[di], f1 = a.red_first[di + 1];
+      if (threadIdx.x == 0) {
+        s_n = min(f1 - f0, kMaxSlotsPerExpert);
+        s_home = a.Gh[p] + (int64_t)a.red_expert[di] * a.vec_per_row;
+      }
       for (int q = threadIdx.x; q < f1 - f0 && q < kMaxSlotsPerExpert; q += kThreads)
         s_slot[q] = a.Gs[p] + (int64_t)a.red_slot[f0 + q] * a.vec_per_row;
+      __syncthreads();
+      staged = p * D + di;
     }
-    __syncthreads();
     const int n = s_n;
-    float4 *home = s_home;
     const int64_t v_begin = c * kRedChunk;
     const int64_t v_end = min(v_begin + kRedChunk, a.vec_per_row);
-    for (int64_t v = v_begin + threadIdx.x; v < v_end; v += kRV * kThreads) {
-      bool ok[kRV];
-      float4 acc[kRV];
-#pragma unroll
-      for (int i = 0; i < kRV; i++) {
-        ok[i] = v + i * kThreads < v_end;
-        if (ok[i]) acc[i] = ld_once_f4(home + v + i * kThreads);
-      }
-      for (int f = 0; f < n; f += kNS) {
-        float4 x[kNS][kRV];
-#pragma unroll
-        for (int q = 0; q < kNS; q++) {
-          if (f + q < n) {
-#pragma unroll
-            for (int i = 0; i < kRV; i++)
-              if (ok[i]) x[q][i] = ld_once_f4(s_slot[f + q] + v + i * kThreads);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < kNS; q++) {
-          if (f + q < n) {
-#pragma unroll
-            for (int i = 0; i < kRV; i++) {
-              if (!ok[i]) continue;
-              acc[i].x = acc[i].x + x[q][i].x;
-              acc[i].y = acc[i].y + x[q][i].y;
-              acc[i].z = acc[i].z + x[q][i].z;
-              acc[i].w = acc[i].w + x[q][i].w;
-              st_global_f4(s_slot[f + q] + v + i * kThreads, zero);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kRV; i++)
-        if (ok[i]) st_global_f4(home + v + i * kThreads, acc[i]);
-    }
+    reduce_columns<4, 2>(s_home, s_slot, n, v_begin, v_end);
   }
 }
 
