@@ -8,8 +8,8 @@
 //
 // On one GPU every destination row is local HBM, so duplicates are expanded by
 // writing the row to every |dst| directly: each source row is read once and
-// written K times.  The work is cut into units of (token, 2 KB chunk of its
-// row) followed by (padding row, chunk), strided over every warp of a
+// written K times.  The work is cut into units of (token, 4 KB chunk of its
+// row) followed by whole padding rows, strided over every warp of a
 // persistent grid, so the tail is balanced whatever the token count.
 // HBM bytes per call: read R*S*H*2 + N*8 (dst, weights); write
 // (N + P)*(H*2 + 4), P = padding rows.
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
   const int K = KT > 0 ? KT : a.K;
   const int64_t tok_units = a.ntok * a.nchunk;
   const int64_t P = a.meta[kMetaP];
-  const int64_t units = tok_units + P * a.nchunk;
+  const int64_t units = tok_units + P;  // then one unit per padding row
   // The next token unit's dst entries are loaded one unit ahead.
   int32_t d_next = 0;
   if (wid < tok_units && lane < K) d_next = __ldg(a.dst + (wid / a.nchunk) * K + lane);
@@ -100,14 +100,18 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
         }
       }
     } else {
-      // padding row q: segment = last s with pad_prefix[s] <= q
-      const int64_t pu = u - tok_units;
-      const int64_t q = pu / a.nchunk;
-      const int c = (int)(pu - q * a.nchunk);
+      // padding row q: segment = last s with pad_prefix[s] <= q, found by a
+      // 32-way search (each round the lanes probe 32 points of the range:
+      // three dependent loads for a few thousand segments, not a dozen)
+      const int64_t q = u - tok_units;
       int lo = 0, hi = a.nseg;
       while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(a.pad_prefix + mid) <= q) lo = mid; else hi = mid;
+        const int step = (hi - lo + 31) >> 5;
+        const int idx = lo + lane * step;
+        const bool le = idx < hi && __ldg(a.pad_prefix + idx) <= q;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        lo += (31 - __clz(m)) * step;
+        hi = min(hi, lo + step);
       }
       const int j = lo / a.EB;
       const int64_t row = __ldg(a.zfr + 2 * lo) + (q - __ldg(a.pad_prefix + lo));
@@ -118,12 +122,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
       }
       uint4 *dp = a.out + g * a.H8;
       const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int i = 0; i < kU; i++) {
-        const int v = c * kChunk + lane + 32 * i;
-        if (v < a.H8) st_global(dp + v, z);
-      }
-      if (c == 0 && lane == 0 && a.w_out) a.w_out[g] = 0.0f;
+      for (int v = lane; v < a.H8; v += 32) st_global(dp + v, z);
+      if (lane == 0 && a.w_out) a.w_out[g] = 0.0f;
     }
   }
 }
