@@ -24,7 +24,8 @@
 //                          count and order their routes, all CTAs meet once,
 //                          each runs the balance step's routing stage on its
 //                          own copy of the per-rank totals and assigns its
-//                          routes; one extra CTA writes the plan's tables.
+//                          routes; two extra CTAs write the plan's tables
+//                          and the copy / reduce lists.
 //   The tile path (K not dividing 32, or tables too large for one CTA):
 //   K1 plan_hist_kernel    per 2048-route tile: per-expert counts and each
 //                          route's ordinal among same-expert routes of the tile
@@ -298,18 +299,48 @@ __device__ void balance_route(const PlanDims &d, const BalTables &t, BalSmall &s
   }
   __syncthreads();
 
-  // Phase C: the chain balance on one warp (lane j holds rank j and j + 32):
+  // Phase C: the chain balance on one warp (lane j holds rank j, and j + 32
+  // when R > 32):
   // each round fills the lowest-index rank below C from the lowest-index rank
   // above C; at most R rounds.
-  if (warp == 0) {
+  if (warp == 0 && R <= 32) {
+    // lane j holds rank j; the loop body is uniform (no branch around a
+    // warp vote), which keeps a round to a few votes
+    int rem = lane < R ? s.G[lane] : C, don = 0, np = 0;
+    for (int round = 0; round <= R; round++) {
+      const unsigned rb = __ballot_sync(0xffffffffu, rem < C);
+      if (!rb) break;
+      const unsigned db = __ballot_sync(0xffffffffu, rem > C);
+      if (!db || np >= R) {  // only reachable from a broken histogram
+        if (lane == 0) s.err |= kErrHist;
+        break;
+      }
+      const int recv = __ffs(rb) - 1, donor = __ffs(db) - 1;
+      const int dd = C - __shfl_sync(0xffffffffu, rem, recv);
+      if (lane == 0) {
+        s.donor[np] = donor;
+        s.recv[np] = recv;
+        s.len[np] = dd;
+        s.recv_piece[recv] = np;
+      }
+      np++;
+      if (lane == donor) {
+        rem -= dd;
+        don += dd;
+      }
+      if (lane == recv) rem = C;
+    }
+    if (lane < R) s.keep[lane] = s.G[lane] - don;
+    if (lane == 0) s.np = np;
+  } else if (warp == 0) {
     int rem0 = lane < R ? s.G[lane] : C, rem1 = lane + 32 < R ? s.G[lane + 32] : C;
     int don0 = 0, don1 = 0, np = 0;
     for (int round = 0; round <= R; round++) {
       const unsigned rb0 = __ballot_sync(0xffffffffu, rem0 < C);
-      const unsigned rb1 = R > 32 ? __ballot_sync(0xffffffffu, rem1 < C) : 0u;
+      const unsigned rb1 = __ballot_sync(0xffffffffu, rem1 < C);
       if (!rb0 && !rb1) break;
       const unsigned db0 = __ballot_sync(0xffffffffu, rem0 > C);
-      const unsigned db1 = R > 32 ? __ballot_sync(0xffffffffu, rem1 > C) : 0u;
+      const unsigned db1 = __ballot_sync(0xffffffffu, rem1 > C);
       if ((!db0 && !db1) || np >= R) {  // only reachable from a broken histogram
         if (lane == 0) s.err |= kErrHist;
         break;
@@ -430,13 +461,13 @@ __device__ void balance_route(const PlanDims &d, const BalTables &t, BalSmall &s
   __syncthreads();
 }
 
-// Stage 2 of the balance step: experts_to_copy, cu_seqlens,
-// zero_fill_ranges, remote_stats, the padding prefix, the copy and reduce
-// lists and the meta words; a neutral plan (every later kernel a no-op) when
-// the balance failed or `ok` is false.  Called by one whole block after
-// balance_route.
-__device__ void balance_outputs(const PlanDims &d, const BalTables &t, BalSmall &s, PlanOut o,
-                                int32_t *in, const PlanLayout &lay, int32_t *status, bool ok) {
+// Stage 2 of the balance step, in two parts that may run on two blocks.
+// balance_tables: experts_to_copy, cu_seqlens, zero_fill_ranges,
+// remote_stats, the padding prefix and the meta words P, U and valid; a
+// neutral plan (every later kernel a no-op) when the balance failed or `ok`
+// is false.  Called by one whole block after balance_route.
+__device__ void balance_tables(const PlanDims &d, const BalTables &t, BalSmall &s, PlanOut o,
+                               int32_t *in, const PlanLayout &lay, int32_t *status, bool ok) {
   const int tid = threadIdx.x;
   const int R = d.R, E = d.E, L = d.L, B = d.B, Bm = d.Bm, LB = L + Bm, EB = d.EB, tp = d.tp;
   const int err = s.err;
@@ -445,7 +476,6 @@ __device__ void balance_outputs(const PlanDims &d, const BalTables &t, BalSmall 
       in[kMetaValid] = 0;
       in[kMetaP] = 0;
       in[kMetaU] = 0;
-      in[kMetaD] = 0;
       if (ok)
         set_status(status, (err & kErrBadExpert) ? MOONEP_ERR_BAD_EXPERT
                            : (err & kErrHist)    ? MOONEP_ERR_HIST_MISMATCH
@@ -461,14 +491,6 @@ __device__ void balance_outputs(const PlanDims &d, const BalTables &t, BalSmall 
     for (int i = tid; i < 2 * R; i += kBalThreads) o.remote_stats[i] = 0;
     return;
   }
-  if (tid == 0) {
-    int u = 0;
-    for (int j = 0; j < R; j++) {
-      s.slot_off[j] = u;
-      u += s.nslots[j];
-    }
-    s.U = u;
-  }
   for (int i = tid; i < R * B; i += kBalThreads) {
     const int j = i / B, b = i - j * B;
     o.etc[i] = b < Bm ? t.etc[j * Bm + b] : -1;
@@ -477,17 +499,6 @@ __device__ void balance_outputs(const PlanDims &d, const BalTables &t, BalSmall 
     const int p = s.recv_piece[j];
     o.remote_stats[2 * j] = p >= 0 ? s.len[p] : 0;
     o.remote_stats[2 * j + 1] = s.nslots[j];
-  }
-  // slot copies per expert (a receiver holds an expert at most once)
-  for (int e = tid; e < E; e += kBalThreads) {
-    const int l = e / L, u = e - l * L;
-    int cnt = 0;
-    for (int j = 0; j < R; j++) {
-      const int p = s.recv_piece[j];
-      if (p >= 0 && s.donor[p] == l && t.slot_b[j * L + u] >= 0) cnt++;
-    }
-    t.rcnt[e] = cnt;
-    t.rhas[e] = cnt > 0;
   }
   // cu_seqlens, zero-fill ranges and the padding prefix of every (rank,
   // segment): a segment that is neither a home expert nor a usable slot of
@@ -516,8 +527,47 @@ __device__ void balance_outputs(const PlanDims &d, const BalTables &t, BalSmall 
     o.zfr[2 * i + 1] = end;
     in[lay.pad_prefix + i] = t.padx[c];
   }
+  if (tid == 0) {
+    int u = 0;
+    for (int j = 0; j < R; j++) u += s.nslots[j];
+    in[lay.pad_prefix + R * EB] = t.padx[R * LB];
+    in[kMetaP] = t.padx[R * LB];
+    in[kMetaU] = u;
+    in[kMetaValid] = 1;
+  }
+}
+
+// balance_lists: the copy list (every used slot, rank by rank), the reduce
+// list (experts with copies in ascending id, their slots in ascending rank)
+// and the meta word D; D = 0 when the balance failed or `ok` is false.
+// Called by one whole block after balance_route.
+__device__ void balance_lists(const PlanDims &d, const BalTables &t, BalSmall &s, int32_t *in,
+                              const PlanLayout &lay, bool ok) {
+  const int tid = threadIdx.x;
+  const int R = d.R, E = d.E, L = d.L, B = d.B, Bm = d.Bm;
+  if (!ok || s.err != 0) {
+    if (tid == 0) in[kMetaD] = 0;
+    return;
+  }
+  if (tid == 0) {
+    int u = 0;
+    for (int j = 0; j < R; j++) {
+      s.slot_off[j] = u;
+      u += s.nslots[j];
+    }
+  }
+  // slot copies per expert (a receiver holds an expert at most once)
+  for (int e = tid; e < E; e += kBalThreads) {
+    const int l = e / L, u = e - l * L;
+    int cnt = 0;
+    for (int j = 0; j < R; j++) {
+      const int p = s.recv_piece[j];
+      if (p >= 0 && s.donor[p] == l && t.slot_b[j * L + u] >= 0) cnt++;
+    }
+    t.rcnt[e] = cnt;
+    t.rhas[e] = cnt > 0;
+  }
   __syncthreads();
-  // copy list: every used slot, rank by rank
   for (int i = tid; i < R * B; i += kBalThreads) {
     const int j = i / B, b = i - j * B;
     if (b < s.nslots[j]) {
@@ -525,8 +575,6 @@ __device__ void balance_outputs(const PlanDims &d, const BalTables &t, BalSmall 
       in[lay.copy_expert + s.slot_off[j] + b] = t.etc[j * Bm + b];
     }
   }
-  // reduce list: experts with copies in ascending id; their slots in
-  // ascending rank
   block_scan2(t.rcnt, t.rhas, E, 0, true, s.part);
   const int ncopies = t.rcnt[E], nexperts = t.rhas[E];
   for (int e = tid; e < E; e += kBalThreads) {
@@ -544,12 +592,8 @@ __device__ void balance_outputs(const PlanDims &d, const BalTables &t, BalSmall 
     }
   }
   if (tid == 0) {
-    in[lay.pad_prefix + R * EB] = t.padx[R * LB];
     in[lay.red_first + nexperts] = ncopies;
     in[kMetaD] = nexperts;
-    in[kMetaP] = t.padx[R * LB];
-    in[kMetaU] = s.U;
-    in[kMetaValid] = 1;
   }
 }
 
@@ -618,7 +662,9 @@ plan_balance_kernel(PlanDims d, const int32_t *__restrict__ tpe, int32_t *hist, 
     in[lay.piece_recv + j] = bs.pr[j];
   }
   for (int i = tid; i < 2 * R; i += kBalThreads) o.dup_counts[i] = 0;
-  balance_outputs(d, t, bs, o, in, lay, status, true);
+  balance_tables(d, t, bs, o, in, lay, status, true);
+  __syncthreads();
+  balance_lists(d, t, bs, in, lay, true);
 }
 
 // ------------------------------------------------------------------ K3
@@ -722,7 +768,7 @@ plan_assign_kernel(PlanDims d, const int32_t *__restrict__ topk, const int32_t *
 //
 // The whole planner in one cooperative launch: G tile blocks of 1024
 // threads, R*ceil(S*K/(1024*IT)) of them, one per tile of a source rank, plus
-// one table block:
+// a table block and a list block:
 //   1. each warp of a tile block walks IT chunks of 32 consecutive routes and
 //      counts them per expert (warp-aggregated, stable ordinals kept in
 //      registers);
@@ -735,9 +781,10 @@ plan_assign_kernel(PlanDims d, const int32_t *__restrict__ topk, const int32_t *
 //   4. each tile block adds the earlier tiles of its rank to its offsets, maps
 //      its routes to (rank, row), marks duplicates with warp shuffles inside
 //      each token's K lanes, and writes dst; meanwhile the table block writes
-//      the plan's other outputs (cu_seqlens, padding, copy and reduce lists),
-//      then, once every tile block is done, the duplicate counts, and clears
-//      the cross-block accumulators for the next call.
+//      cu_seqlens, zero_fill_ranges, experts_to_copy, remote_stats and the
+//      padding prefix, then, once every tile block is done, the duplicate
+//      counts, and clears the cross-block accumulators for the next call;
+//      the list block writes the copy and reduce lists.
 // Used when K divides 32 (a token's routes then never straddle a 32-route
 // chunk), the blocks fit on the SMs at once and the tables fit in shared
 // memory; otherwise the three-kernel tile path runs.
@@ -756,7 +803,7 @@ struct FusedArgs {
   int32_t *in;
   PlanLayout lay;
   int32_t *status;
-  // [0] arrivals (G + 1 per call), [1] tile blocks done (G per call)
+  // [0] arrivals (G + 2 per call), [1] blocks done with the totals (G + 1 per call)
   unsigned long long *sync;
   int32_t *dupflag;
   int items;          // routes per thread; tile = 1024 * items routes
@@ -803,8 +850,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   const PlanDims d = a.d;
   const int R = d.R, E = d.E, L = d.L, C = d.C;
   const int g = blockIdx.x;
-  const bool table_block = g == a.G;
-  const int r = table_block ? 0 : g / a.tpr, t = table_block ? 0 : g % a.tpr;
+  const int nblk = a.G + 2;  // tile blocks, then the table block and the list block
+  const bool tile = g < a.G, table_block = g == a.G, list_block = g == a.G + 1;
+  const int r = tile ? g / a.tpr : 0, t = tile ? g % a.tpr : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int32_t *h = sm;                     // [warps][E]
   int32_t *sCnt = h + kFusedWarps * E;  // [R*E]
@@ -818,7 +866,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   const int wbase = t * kFusedThreads * items + warp * 32 * items;
   int e_reg[items], o_reg[items];
   if (tid == 0) s_bad = 0;
-  if (!table_block) {
+  if (tile) {
     for (int i = tid; i < kFusedWarps * E; i += kFusedThreads) h[i] = 0;
     __syncthreads();
 
@@ -869,7 +917,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   // 3. all blocks arrive; each waits for the rest
   if (tid == 0) {
     __threadfence();
-    const unsigned long long n = (unsigned long long)a.G + 1;
+    const unsigned long long n = (unsigned long long)nblk;
     const unsigned long long old = atomicAdd(a.sync, 1ull);
     const unsigned long long target = old - old % n + n;
     s_target = target;
@@ -895,18 +943,28 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     // tokens_per_expert against the recount, a slice per block: a mismatch
     // latches its error but the plan stands (it is built from the recount)
     if (a.tpe != nullptr)
-      for (int i = g * kFusedThreads + tid; i < R * E; i += (a.G + 1) * kFusedThreads)
+      for (int i = g * kFusedThreads + tid; i < R * E; i += nblk * kFusedThreads)
         if (sCnt[i] != __ldg(a.tpe + i)) set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
     __syncthreads();
-    balance_route(d, tb, bs, s_err);
   }
+  // the list block is done with the totals and the error word
+  if (list_block && tid == 0) {
+    __threadfence();
+    atomicAdd(a.sync + 1, 1ull);
+  }
+  if (ok) balance_route(d, tb, bs, s_err);
 
+  if (list_block) {
+    balance_lists(d, tb, bs, a.in, a.lay, ok);
+    return;
+  }
   if (table_block) {
-    balance_outputs(d, tb, bs, a.o, a.in, a.lay, a.status, ok);
-    // the duplicate counts once every tile block has added its own; then
-    // the accumulators start the next call at zero
+    balance_tables(d, tb, bs, a.o, a.in, a.lay, a.status, ok);
+    // the duplicate counts once every tile block has added its own (and the
+    // list block has read the totals); then the accumulators start the next
+    // call at zero
     if (tid == 0) {
-      const unsigned long long done = s_target / ((unsigned long long)a.G + 1) * a.G;
+      const unsigned long long done = s_target / (unsigned long long)nblk * (a.G + 1);
       s_done = wait_counter(a.sync + 1, done, a.wait_ns);
       if (!s_done) set_status(a.status, MOONEP_ERR_TIMEOUT);
     }
@@ -1067,12 +1125,12 @@ plan_dup_kernel(PlanDims d, const int32_t *__restrict__ dst, const int32_t *__re
 }  // namespace
 
 // Routes per thread of the single-launch planner: the fewest (most tiles,
-// most SMs at work) for which every tile block and the table block fit on
+// most SMs at work) for which every tile block and the two table blocks fit on
 // the SMs at once; 0 if none.
 int plan_fused_items(int R, int C, int sms) {
   for (int items = 1; items <= kFusedMaxItems; items *= 2) {
     const int tpr = (C + kFusedThreads * items - 1) / (kFusedThreads * items);
-    if ((int64_t)R * (tpr > 0 ? tpr : 1) + 1 <= sms) return items;
+    if ((int64_t)R * (tpr > 0 ? tpr : 1) + 2 <= sms) return items;
   }
   return 0;
 }
@@ -1197,7 +1255,7 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
                        : fa.items == 2 ? (const void *)plan_fused_kernel<2>
                        : fa.items == 4 ? (const void *)plan_fused_kernel<4>
                                        : (const void *)plan_fused_kernel<8>;
-    e = cudaLaunchCooperativeKernel(kern, dim3(fa.G + 1), dim3(kFusedThreads), args, smem, st);
+    e = cudaLaunchCooperativeKernel(kern, dim3(fa.G + 2), dim3(kFusedThreads), args, smem, st);
     if (e != cudaSuccess) return cuda_status(e);
   } else {
     e = cudaMemsetAsync(in, 0, kMetaWords * sizeof(int32_t), st);
