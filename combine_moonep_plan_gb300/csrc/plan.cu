@@ -806,7 +806,6 @@ struct FusedArgs {
   // [0] arrivals (G + 2 per call), [1] blocks done with the totals (G + 1 per call)
   unsigned long long *sync;
   int32_t *dupflag;
-  int items;          // routes per thread; tile = 1024 * items routes
   int tpr, G;         // tiles per rank, tile blocks (R * tpr)
   int unreachable;    // test hook: the arrival wait can never be satisfied
   long long wait_ns;  // limit of each wait
@@ -1236,8 +1235,8 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     fa.topk = topk;
     fa.tpe = tpe;
     fa.hist = ctx->d_hist;
-    fa.items = plan_fused_items(d.R, d.C, ctx->sms_device);
-    fa.tpr = plan_fused_tiles(d.C, fa.items);
+    const int items = plan_fused_items(d.R, d.C, ctx->sms_device);
+    fa.tpr = plan_fused_tiles(d.C, items);
     fa.G = d.R * fa.tpr;
     fa.totals = ctx->d_hist + plan_totals_offset(d.R, d.E, d.C, ctx->sms_device);
     fa.aux = fa.totals + (int64_t)d.R * d.E;
@@ -1251,9 +1250,9 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     fa.wait_ns = ctx->test_planner_timeout ? 200000000LL : 1000000000LL;
     void *args[] = {&fa};
     const size_t smem = fused_smem_words(d.R, d.E, d.B) * sizeof(int32_t);
-    const void *kern = fa.items == 1   ? (const void *)plan_fused_kernel<1>
-                       : fa.items == 2 ? (const void *)plan_fused_kernel<2>
-                       : fa.items == 4 ? (const void *)plan_fused_kernel<4>
+    const void *kern = items == 1   ? (const void *)plan_fused_kernel<1>
+                       : items == 2 ? (const void *)plan_fused_kernel<2>
+                       : items == 4 ? (const void *)plan_fused_kernel<4>
                                        : (const void *)plan_fused_kernel<8>;
     e = cudaLaunchCooperativeKernel(kern, dim3(fa.G + 2), dim3(kFusedThreads), args, smem, st);
     if (e != cudaSuccess) return cuda_status(e);
