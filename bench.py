@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mxfp4", action="store_true",
                     help="skip the packed-MXFP4 weight prefetch measurement")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the step and nothing else (no sweep, chain, preparation, MXFP4, "
+                         "end-to-end or CPU legs): a clean launch list for profilers")
     ap.add_argument("--sweep-steps", type=int, default=30)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--graph", action="store_true",
@@ -61,7 +64,11 @@ def parse():
                     help="comma list of ops (plan,dispatch,combine,prefetch,reduce): "
                          "allocate only what they need and run each --steps times "
                          "(a small, self-contained case for profilers; prints timings)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.step_only:
+        args.no_sweep = args.no_e2e = args.no_cpu_baseline = args.no_mxfp4 = True
+        args.graph = False
+    return args
 
 
 # ----------------------------------------------------------------- routing
@@ -757,7 +764,8 @@ def main():
                if op_ms[o] > 0 else None,
                "ms_p10_p50_p90": [round(float(np.percentile(per_op[o], q)), 5)
                                   for q in (10, 50, 90)]} for o in OPS}
-    chain_ms = time_chain(step, max(20, min(args.steps, 200)), torch)
+    chain_ms = (time_chain(step, max(20, min(args.steps, 200)), torch)
+                if not args.step_only else None)
     chain_graph_ms = (time_chain(step, max(20, min(args.steps, 200)), torch, graph=True)
                       if args.graph else None)
     step_bytes = sum(alg.values())
@@ -785,7 +793,7 @@ def main():
             del s2
         torch.cuda.synchronize()
 
-    prep = run_prepare(buf, sh, 20, torch)
+    prep = run_prepare(buf, sh, 20, torch) if not args.step_only else None
 
     mxfp4 = None
     if not args.no_mxfp4:
@@ -813,7 +821,7 @@ def main():
         "plan_dispatch_combine_tokens_per_s": R_S(sh) * world / (pdc_ms / 1e3),
         "plan_dispatch_combine_chain": {
             "ms": round(chain_ms, 5), "tokens_per_s": R_S(sh) * world / (chain_ms / 1e3),
-            "graph_ms": round(chain_graph_ms, 5) if chain_graph_ms else None},
+            "graph_ms": round(chain_graph_ms, 5) if chain_graph_ms else None} if chain_ms else None,
         "plan_frac_of_dispatch": op_ms["plan"] / op_ms["dispatch"],
         "step_hbm_GBps": step_bytes / (ms_per_step / 1e3) / 1e9,
         "ops": ops, "plan_counts": counts,
