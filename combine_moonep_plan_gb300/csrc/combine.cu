@@ -71,6 +71,8 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 // (K = 8 reads 2 KB of each row per unit, in two batches of four rows).
 template <int KT, int U, int BT, int KB>
 __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t wid = ((int64_t)blockIdx.x * BT + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * BT) >> 5;
@@ -141,8 +143,8 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
 }
 
 template <int KT, int U, int BT, int KB>
-void launch(const Args &a, int grid, cudaStream_t st) {
-  combine_kernel<KT, U, BT, KB><<<grid, BT, 0, st>>>(a);
+cudaError_t launch(const Args &a, int grid, cudaStream_t st) {
+  return launch_pdl(combine_kernel<KT, U, BT, KB>, grid, BT, 0, st, false, a);
 }
 
 }  // namespace
@@ -177,14 +179,15 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
   a.nchunk = (a.H8 + 32 * U - 1) / (32 * U);
   if (a.ntok == 0 || a.H8 == 0) return MOONEP_OK;
   const int grid = ctx->sms * ctx->blocks_combine;
+  cudaError_t e;
   switch (c.K) {
-    case 1: launch<1, 4, 256, 1>(a, grid, st); break;
-    case 2: launch<2, 4, 256, 2>(a, grid, st); break;
-    case 4: launch<4, 4, 256, 4>(a, grid, st); break;
-    case 8: launch<8, 4, 128, 4>(a, grid, st); break;
-    default: launch<0, 2, 256, 1>(a, grid, st); break;
+    case 1: e = launch<1, 4, 256, 1>(a, grid, st); break;
+    case 2: e = launch<2, 4, 256, 2>(a, grid, st); break;
+    case 4: e = launch<4, 4, 256, 4>(a, grid, st); break;
+    case 8: e = launch<8, 4, 128, 4>(a, grid, st); break;
+    default: e = launch<0, 2, 256, 1>(a, grid, st); break;
   }
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
 
 }  // namespace moonep

@@ -40,6 +40,8 @@ struct Args {
 
 template <int KT>
 __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t wid = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * kThreads) >> 5;
@@ -168,14 +170,15 @@ int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_
   a.EB = ctx->EB;
   if (a.H8 == 0) return MOONEP_OK;
   const int grid = ctx->sms * ctx->blocks_dispatch;
+  cudaError_t e;
   switch (c.K) {
-    case 1: dispatch_kernel<1><<<grid, kThreads, 0, st>>>(a); break;
-    case 2: dispatch_kernel<2><<<grid, kThreads, 0, st>>>(a); break;
-    case 4: dispatch_kernel<4><<<grid, kThreads, 0, st>>>(a); break;
-    case 8: dispatch_kernel<8><<<grid, kThreads, 0, st>>>(a); break;
-    default: dispatch_kernel<0><<<grid, kThreads, 0, st>>>(a); break;
+    case 1: e = launch_pdl(dispatch_kernel<1>, grid, kThreads, 0, st, false, a); break;
+    case 2: e = launch_pdl(dispatch_kernel<2>, grid, kThreads, 0, st, false, a); break;
+    case 4: e = launch_pdl(dispatch_kernel<4>, grid, kThreads, 0, st, false, a); break;
+    case 8: e = launch_pdl(dispatch_kernel<8>, grid, kThreads, 0, st, false, a); break;
+    default: e = launch_pdl(dispatch_kernel<0>, grid, kThreads, 0, st, false, a); break;
   }
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
 
 }  // namespace moonep

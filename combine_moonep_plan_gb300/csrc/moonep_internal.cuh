@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moonep.h"
 
 namespace moonep {
@@ -131,6 +133,42 @@ int occupancy_dispatch(int K);
 int occupancy_combine(int K);
 int occupancy_copy();
 int occupancy_reduce();
+
+// Programmatic dependent launch: every kernel of the library is launched
+// with launch_pdl, so it may be scheduled while the kernel before it on the
+// stream is still running.  Its first statement is pdl_wait(): it waits until
+// that kernel has completed and its memory is visible, before touching any
+// memory; then pdl_launch_dependents() lets the next kernel be scheduled.
+// Back-to-back launches (the decode path's plan -> dispatch -> combine) then
+// overlap one kernel's launch latency with the previous one's tail.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, bool cooperative, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  n++;
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    n++;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Latch the first error code into the status word.
 __device__ __forceinline__ void set_status(int32_t *status, int code) {

@@ -842,6 +842,8 @@ size_t fused_smem_words(int R, int E, int B) {
 // count keeps only the routes' registers live across the balance step.
 template <int IT>
 __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int32_t sm[];
   __shared__ BalSmall bs;
   __shared__ int s_bad, s_ok, s_err, s_done;
@@ -1248,13 +1250,12 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     fa.dupflag = dupflag;
     fa.unreachable = ctx->test_planner_timeout;
     fa.wait_ns = ctx->test_planner_timeout ? 200000000LL : 1000000000LL;
-    void *args[] = {&fa};
     const size_t smem = fused_smem_words(d.R, d.E, d.B) * sizeof(int32_t);
-    const void *kern = items == 1   ? (const void *)plan_fused_kernel<1>
-                       : items == 2 ? (const void *)plan_fused_kernel<2>
-                       : items == 4 ? (const void *)plan_fused_kernel<4>
-                                       : (const void *)plan_fused_kernel<8>;
-    e = cudaLaunchCooperativeKernel(kern, dim3(fa.G + 2), dim3(kFusedThreads), args, smem, st);
+    const dim3 grid(fa.G + 2), block(kFusedThreads);
+    e = items == 1   ? launch_pdl(plan_fused_kernel<1>, grid, block, smem, st, true, fa)
+        : items == 2 ? launch_pdl(plan_fused_kernel<2>, grid, block, smem, st, true, fa)
+        : items == 4 ? launch_pdl(plan_fused_kernel<4>, grid, block, smem, st, true, fa)
+                     : launch_pdl(plan_fused_kernel<8>, grid, block, smem, st, true, fa);
     if (e != cudaSuccess) return cuda_status(e);
   } else {
     e = cudaMemsetAsync(in, 0, kMetaWords * sizeof(int32_t), st);

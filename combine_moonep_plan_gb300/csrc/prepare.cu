@@ -34,6 +34,8 @@ struct PrepArgs {
 };
 
 __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int32_t hist[];  // [E], route blocks only
   const int tid = threadIdx.x;
   if ((int)blockIdx.x < a.R) {
@@ -112,8 +114,8 @@ int launch_prepare(moonep_ctx *ctx, const int32_t *num_tokens, uint16_t *hidden,
   if (zb > cap) zb = cap;
   if (!hidden) a.pad_first[c.R] = 0;
   const size_t smem = tpe ? (size_t)c.E * sizeof(int32_t) : 0;
-  prepare_kernel<<<(unsigned)(c.R + zb), kThreads, smem, st>>>(a);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(
+      launch_pdl(prepare_kernel, dim3((unsigned)(c.R + zb)), dim3(kThreads), smem, st, false, a));
 }
 
 }  // namespace moonep

@@ -44,6 +44,8 @@ struct PrefetchArgs {
 };
 
 __global__ void __launch_bounds__(kThreads) prefetch_kernel(PrefetchArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t U = a.meta[kMetaU];
   int64_t units = 0;
   for (int t = 0; t < a.n; t++) units += U * a.nchunk[t];
@@ -150,6 +152,8 @@ __device__ __forceinline__ void reduce_columns(float4 *home, float4 *const *slot
 // blocks fit on an SM.  The slot list of the unit's expert is staged in
 // shared memory once per expert.
 __global__ void __launch_bounds__(kThreads, 4) reduce_kernel(ReduceArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float4 *s_slot[kMaxSlotsPerExpert];
   __shared__ float4 *s_home;
   __shared__ int s_n;
@@ -222,8 +226,7 @@ int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n, void *
   a.E = c.E;
   if (!any || c.B == 0) return MOONEP_OK;
   const int grid = ctx->sms * ctx->blocks_copy;
-  prefetch_kernel<<<grid, kThreads, 0, st>>>(a);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_pdl(prefetch_kernel, grid, kThreads, 0, st, false, a));
 }
 
 int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, float *const *Gh,
@@ -245,8 +248,8 @@ int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, flo
   a.vec_per_row = HHp / 4;
   a.nchunk = (a.vec_per_row + kRedChunk - 1) / kRedChunk;
   if (a.vec_per_row == 0 || c.B == 0) return MOONEP_OK;
-  reduce_kernel<<<ctx->sms * ctx->blocks_reduce, kThreads, 0, st>>>(a);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(
+      launch_pdl(reduce_kernel, ctx->sms * ctx->blocks_reduce, kThreads, 0, st, false, a));
 }
 
 }  // namespace moonep
