@@ -71,6 +71,9 @@ pins = [
     ("invariants_tiny_zipf", lambda: P.test_oracle_plan_invariants(o, "tiny", wl.SHAPES["tiny"], "zipf3")),
     ("invariants_kimi_hot", lambda: P.test_oracle_plan_invariants(o, "kimi", wl.Shape("k", R=8, E=384, K=8, S=64, H=8, Hp=8, B=48, tp=128, weights="sigmoid"), "hot")),
     ("stable_sort", lambda: P.test_balanced_routing_is_a_stable_sort(o, "tiny")),
+    ("restate_kimi", lambda: P.test_oracle_matches_sort_based_restatement(o, "kimi_k2", "hot30")),
+    ("restate_mixtral", lambda: P.test_oracle_matches_sort_based_restatement(o, "mixtral", 3.0)),
+    ("restate_small", lambda: [P.test_oracle_matches_restatement_random_small(o, i) for i in range(8)]),
     ("slots_error", lambda: P.test_slots_error_when_b_below_group_size(o)),
     ("dispatch_scatter", lambda: P.test_dispatch_is_a_scatter(o)),
     ("k_times_x", lambda: P.test_identity_expert_combine_is_k_times_x(o)),

@@ -569,3 +569,70 @@ def test_brute_force_tiny_balanced_assignments(oracle_mod, seed):
     best = min(moved(m) for m in feasible)
     G = [int(T[j * L:(j + 1) * L].sum()) for j in range(R)]
     assert moved(x) >= best >= sum(max(0, g - C) for g in G)
+
+
+# ------------------------------------------ independent sort-based restatement
+
+RESTATE_CASES = [
+    ("tiny", "zipf1.2"), ("mixtral", 0.0), ("mixtral", 1.0), ("mixtral", 3.0),
+    ("deepseek_v3", 1.0), ("deepseek_v3", 4.0), ("kimi_k2", "hot30"), ("kimi_k2", "hot9"),
+    ("qwen3_decode", "uniform"), ("qwen3_decode", "zipf1"),
+]
+
+
+@pytest.mark.parametrize("name,point", RESTATE_CASES, ids=[f"{n}-{p}" for n, p in RESTATE_CASES])
+def test_oracle_matches_sort_based_restatement(oracle_mod, name, point):
+    """The oracle's plan equals, field for field, a numpy restatement of the
+    rule built on a stable sort and prefix sums (tests/plan_restatement.py),
+    on every workload shape (S cut to 512 above that) and its routing sweep."""
+    from tests.plan_restatement import restate_plan
+    sh = wl.SHAPES[name]
+    if sh.S > 512:
+        sh = wl.Shape(name, R=sh.R, E=sh.E, K=sh.K, S=512, H=8, Hp=8, B=sh.B, tp=sh.tp,
+                      weights=sh.weights)
+    seed = wl.seed_for(name, 5)
+    if point == "zipf1.2":
+        topk, _ = wl.routing(sh, "zipf", zipf_s=1.2, seed=seed)
+    elif point == "zipf1":
+        topk, _ = wl.routing(sh, "zipf", zipf_s=1.0, seed=seed)
+    elif point == "uniform":
+        topk, _ = wl.routing(sh, "uniform", seed=seed)
+    elif point == "hot30":
+        topk, _ = wl.routing(sh, "hot", hot_share=0.30, seed=seed)
+    elif point == "hot9":
+        topk, _ = wl.routing(sh, "hot", hot_share=0.09375, seed=seed)
+    elif point == 0.0:
+        topk, _ = wl.routing(sh, "exact0", seed=seed)
+    else:
+        topk, _ = wl.routing(sh, "zipf", target_maxvio=float(point), seed=seed)
+    st, p = _plan(oracle_mod, _cfg(sh), topk)
+    rs, rp = restate_plan(sh.R, sh.E, sh.K, sh.S, sh.B, sh.tp, topk)
+    assert st == rs == 0
+    assert p["NvS"] == rp["NvS"]
+    for f in ("dst", "experts_to_copy", "cu_seqlens", "zero_fill_ranges", "remote_stats",
+              "dup_counts"):
+        assert np.array_equal(p[f], rp[f]), f
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_oracle_matches_restatement_random_small(oracle_mod, seed):
+    """Random small shapes with duplicate ids inside tokens and B anywhere in
+    [0, L + 1]: same plan, or the same too-few-slots status."""
+    from tests.plan_restatement import restate_plan
+    rng = np.random.default_rng(500 + seed)
+    R = int(rng.integers(1, 6))
+    L = int(rng.integers(1, 5))
+    E, K = R * L, int(rng.integers(1, 5))
+    S = int(rng.integers(1, 9))
+    B = int(rng.integers(0, L + 2))
+    tp = int(rng.integers(1, 6))
+    skew = rng.random(E) ** 3 + 1e-3
+    topk = rng.choice(E, size=(R, S, K), p=skew / skew.sum()).astype(np.int32)
+    cfg = dict(R=R, E=E, K=K, S=S, B=B, tp=tp)
+    st, p = _plan(oracle_mod, cfg, topk)
+    rs, rp = restate_plan(R, E, K, S, B, tp, topk)
+    assert st == rs
+    if st == 0:
+        for f in ("dst", "experts_to_copy", "cu_seqlens", "zero_fill_ranges", "remote_stats",
+                  "dup_counts"):
+            assert np.array_equal(p[f], rp[f]), f
