@@ -365,6 +365,83 @@ def test_prefetch_rows_odd_row_sizes():
         buf.prefetch_weight(plan, ts[0], ts[1], scales=[ts[2]])
 
 
+# ------------------------------------------------------------ canaries
+
+def test_guard_rows_around_every_output_stay_untouched():
+    """Every output buffer sits between guard rows holding a fixed bit
+    pattern; after prepare, plan, dispatch, combine, prefetch (bf16 and byte
+    rows) and reduce the guards still hold it."""
+    sh = wl.SHAPES["tiny"]
+    cfg = _cfg_of(sh)
+    R, S, K, E, H, B = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B
+    buf = _buffer(cfg, H=H, views=False)
+    NvS = buf.NvS
+    gr = 4
+    dev = "cuda"
+
+    def guarded(rows, cols, dtype, fill):
+        big = torch.empty((rows + 2 * gr, cols), dtype=dtype, device=dev)
+        big.view(torch.uint8).view(torch.int8).fill_(0x5A) if dtype == torch.uint8 else \
+            big.view(torch.int16).fill_(0x5A5A)
+        inner = big[gr:gr + rows]
+        if fill is not None:
+            inner.copy_(fill)
+        return big, inner
+
+    def guards_ok(big):
+        v = big.view(torch.uint8)
+        return bool((v[:gr] == 0x5A).all() and (v[-gr:] == 0x5A).all())
+
+    topk = _routing(sh, "zipf", 31)
+    g = torch.Generator(device=dev).manual_seed(31)
+    x_big, x = guarded(R * S, H, torch.bfloat16,
+                       torch.randn((R * S, H), generator=g, device=dev).bfloat16())
+    tk_big = torch.empty((R * S + 2 * gr, K), dtype=torch.int32, device=dev)
+    tk_big.view(torch.uint8).fill_(0x5A)
+    tk = tk_big[gr:gr + R * S]
+    tk.copy_(torch.from_numpy(topk.reshape(R * S, K)))
+    w_big = torch.empty((R * S + 2 * gr, K), dtype=torch.float32, device=dev)
+    w_big.view(torch.uint8).fill_(0x5A)
+    w = w_big[gr:gr + R * S]
+    w.copy_(torch.from_numpy(wl.route_weights(sh, 31).reshape(R * S, K)))
+    tpe = buf.prepare(x.view(R, S, H), tk.view(R, S, K), w.view(R, S, K), num_tokens=[S - 5, S])
+    out_big, out = guarded(R * NvS, H, torch.bfloat16, None)
+    wo_big = torch.empty(R * NvS + 2 * gr * 4, dtype=torch.float32, device=dev)
+    wo_big.view(torch.uint8).fill_(0x5A)
+    wo = wo_big[gr * 4:gr * 4 + R * NvS]
+    hid, wn, cu, plan = buf.dispatch(x.view(R, S, H), w.view(R, S, K), tk.view(R, S, K), tpe,
+                                     out=out, weights_out=wo)
+    c_big, c = guarded(R * S, H, torch.bfloat16, None)
+    cw_big = torch.empty((R * S + 2 * gr, K), dtype=torch.float32, device=dev)
+    cw_big.view(torch.uint8).fill_(0x5A)
+    cw = cw_big[gr:gr + R * S]
+    buf.combine(plan, hid, wn, out=c.view(R, S, H), weights_out=cw.view(R, S, K))
+    rows = E + R * B
+    W_big, W = guarded(rows, H * sh.Hp, torch.bfloat16,
+                       torch.randn((rows, H * sh.Hp), generator=g, device=dev).bfloat16())
+    buf.prefetch_weight(plan, W.view(rows, H, sh.Hp))
+    P_big, P = guarded(rows, 48, torch.uint8,
+                       torch.randint(0, 256, (rows, 48), generator=g, device=dev,
+                                     dtype=torch.uint8))
+    buf.prefetch_rows(plan, [P])
+    Gh_big = torch.empty((E + 2 * gr, H * sh.Hp), dtype=torch.float32, device=dev)
+    Gs_big = torch.empty((R * B + 2 * gr, H * sh.Hp), dtype=torch.float32, device=dev)
+    for t in (Gh_big, Gs_big):
+        t.view(torch.uint8).fill_(0x5A)
+    Gh_big[gr:gr + E].normal_(generator=g)
+    Gs_big[gr:gr + R * B].normal_(generator=g)
+    buf.reduce_grad(plan, [Gh_big[gr:gr + E].view(E, H, sh.Hp)],
+                    [Gs_big[gr:gr + R * B].view(R, B, H, sh.Hp)])
+    assert buf.get_status() == 0
+    for name, big in (("hidden", x_big), ("topk", tk_big), ("weights", w_big),
+                      ("dispatched rows", out_big), ("dispatched weights", wo_big),
+                      ("combined rows", c_big), ("combined weights", cw_big),
+                      ("bf16 weights", W_big), ("byte rows", P_big), ("grads", Gh_big),
+                      ("slot grads", Gs_big)):
+        assert guards_ok(big), f"guard rows around the {name} were written"
+    buf.destroy()
+
+
 # ------------------------------------------------------------- errors
 
 def test_device_errors_latch_status_without_faulting():
