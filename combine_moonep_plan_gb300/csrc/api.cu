@@ -88,7 +88,14 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
     free(ctx);
     return MOONEP_ERR_CUDA;
   }
-  ctx->sms = (c.num_sms > 0 && c.num_sms < sms) ? c.num_sms : sms;
+  // SM cap: the config's num_sms, else the MOONEP_NUM_SMS environment
+  // variable, else every SM
+  int cap = c.num_sms;
+  if (cap <= 0) {
+    const char *env = getenv("MOONEP_NUM_SMS");
+    cap = env ? atoi(env) : 0;
+  }
+  ctx->sms = (cap > 0 && cap < sms) ? cap : sms;
   ctx->sms_device = sms;
   ctx->L = c.E / c.R;
   ctx->C = c.S * c.K;

@@ -63,7 +63,8 @@ extern "C" {
  * rank (B = E/R is what training needs [README, How to set B]; smaller B is
  * allowed and reported as MOONEP_ERR_SLOTS when a plan needs more);
  * token_padding = row alignment of every non-empty segment; num_sms caps the
- * SMs the copy kernels use (<= 0: every SM). */
+ * SMs the copy kernels use (<= 0: the MOONEP_NUM_SMS environment variable
+ * when set to a positive count, else every SM). */
 typedef struct moonep_config {
   int R;             /* expert-parallel ranks (logical partitions), >= 1 */
   int E;             /* experts, multiple of R */
@@ -72,7 +73,7 @@ typedef struct moonep_config {
   int H;             /* hidden size, multiple of 8 */
   int B;             /* prefetch slots per rank, >= 0 */
   int token_padding; /* >= 1 */
-  int num_sms;       /* <= 0: all SMs */
+  int num_sms;       /* <= 0: MOONEP_NUM_SMS, else all SMs */
 } moonep_config;
 
 typedef struct moonep_ctx moonep_ctx;

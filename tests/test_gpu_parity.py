@@ -365,6 +365,39 @@ def test_prefetch_rows_odd_row_sizes():
         buf.prefetch_weight(plan, ts[0], ts[1], scales=[ts[2]])
 
 
+# ------------------------------------------------------------ SM cap
+
+def test_sm_cap_gives_identical_results(monkeypatch):
+    """A context capped to 16 SMs (by its config, or by MOONEP_NUM_SMS) moves
+    the same bytes to the same places as one using every SM."""
+    from combine_moonep_plan_gb300.api import Buffer
+    sh = _small("deepseek_v3", 128)
+    topk = torch.from_numpy(_routing(sh, "zipf_hard", 41)).cuda()
+    x = torch.randn((sh.R, sh.S, sh.H), device="cuda").bfloat16()
+    w = torch.rand((sh.R, sh.S, sh.K), device="cuda")
+    rows = sh.E + sh.R * sh.B
+    W = torch.randn((rows, sh.H, sh.Hp), device="cuda").bfloat16()
+    results = []
+    for how in ("all", "config", "env"):
+        if how == "env":
+            monkeypatch.setenv("MOONEP_NUM_SMS", "16")
+        buf = Buffer(S=sh.S, H=sh.H, K=sh.K, E=sh.E, num_ep_ranks=sh.R, B=sh.B,
+                     token_padding=sh.tp, zero_copy_views=False,
+                     num_sms=16 if how == "config" else None)
+        monkeypatch.delenv("MOONEP_NUM_SMS", raising=False)
+        assert buf.num_sms == (16 if how != "all" else torch.cuda.get_device_properties(0).multi_processor_count)
+        hid, wn, cu, plan = buf.dispatch(x, w, topk)
+        out, wb = buf.combine(plan, hid, wn)
+        Wc = W.clone()
+        buf.prefetch_weight(plan, Wc)
+        assert buf.get_status() == 0
+        results.append((hid.clone(), wn.clone(), out.clone(), wb.clone(), Wc))
+        buf.destroy()
+    for other in results[1:]:
+        for a, b in zip(results[0], other):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
 # ------------------------------------------------------------ canaries
 
 def test_guard_rows_around_every_output_stay_untouched():
