@@ -782,9 +782,9 @@ plan_assign_kernel(PlanDims d, const int32_t *__restrict__ topk, const int32_t *
 //      its routes to (rank, row), marks duplicates with warp shuffles inside
 //      each token's K lanes, and writes dst; meanwhile the table block writes
 //      cu_seqlens, zero_fill_ranges, experts_to_copy, remote_stats and the
-//      padding prefix, then, once every tile block is done, the duplicate
-//      counts, and clears the cross-block accumulators for the next call;
-//      the list block writes the copy and reduce lists.
+//      padding prefix, and the list block the copy and reduce lists;
+//   5. the last block to finish writes the duplicate counts and clears the
+//      cross-block accumulators for the next call.
 // Used when K divides 32 (a token's routes then never straddle a 32-route
 // chunk), the blocks fit on the SMs at once and the tables fit in shared
 // memory; otherwise the three-kernel tile path runs.
@@ -803,7 +803,7 @@ struct FusedArgs {
   int32_t *in;
   PlanLayout lay;
   int32_t *status;
-  // [0] arrivals (G + 2 per call), [1] blocks done with the totals (G + 1 per call)
+  // [0] arrivals, [1] blocks finished: each grows by G + 2 per call
   unsigned long long *sync;
   int32_t *dupflag;
   int tpr, G;         // tiles per rank, tile blocks (R * tpr)
@@ -834,6 +834,30 @@ __device__ bool wait_counter(const unsigned long long *p, unsigned long long tar
   return true;
 }
 
+// Every block counts itself finished once per call, after its last read of
+// the per-rank totals and its last add to the duplicate-count accumulators;
+// the last one writes the duplicate counts and clears the accumulators and
+// totals for the next call (no block waits for another here).
+__device__ void finish_call(const FusedArgs &a, int nblk, int *s_last) {
+  const int R = a.d.R, E = a.d.E, tid = threadIdx.x;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned long long old = atomicAdd(a.sync + 1, 1ull);
+    *s_last = old % (unsigned long long)nblk == (unsigned long long)(nblk - 1);
+    __threadfence();
+  }
+  __syncthreads();
+  if (*s_last) {
+    for (int i = tid; i < 2 * R; i += blockDim.x) {
+      a.o.dup_counts[i] = __ldcg(a.aux + i);
+      a.aux[i] = 0;
+    }
+    for (int i = tid; i < R * E; i += blockDim.x) a.totals[i] = 0;
+    if (tid == 0) a.aux[2 * R] = 0;
+  }
+}
+
 size_t fused_smem_words(int R, int E, int B) {
   return (size_t)kFusedWarps * E + (size_t)E * R + (size_t)E + bal_tables_words(R, E, B);
 }
@@ -846,8 +870,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   pdl_launch_dependents();
   extern __shared__ int32_t sm[];
   __shared__ BalSmall bs;
-  __shared__ int s_bad, s_ok, s_err, s_done;
-  __shared__ unsigned long long s_target;
+  __shared__ int s_bad, s_ok, s_err, s_last;
+  __shared__ int sDup[2 * kMaxR];  // duplicate counts of this block
   const PlanDims d = a.d;
   const int R = d.R, E = d.E, L = d.L, C = d.C;
   const int g = blockIdx.x;
@@ -921,7 +945,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     const unsigned long long n = (unsigned long long)nblk;
     const unsigned long long old = atomicAdd(a.sync, 1ull);
     const unsigned long long target = old - old % n + n;
-    s_target = target;
     s_ok = wait_counter(a.sync, target + (a.unreachable ? 1 : 0), a.wait_ns);
     if (!s_ok) set_status(a.status, MOONEP_ERR_TIMEOUT);
     s_err = s_ok ? __ldcg(a.aux + 2 * R) : 0;
@@ -948,34 +971,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
         if (sCnt[i] != __ldg(a.tpe + i)) set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
     __syncthreads();
   }
-  // the list block is done with the totals and the error word
-  if (list_block && tid == 0) {
-    __threadfence();
-    atomicAdd(a.sync + 1, 1ull);
-  }
   if (ok) balance_route(d, tb, bs, s_err);
 
   if (list_block) {
     balance_lists(d, tb, bs, a.in, a.lay, ok);
+    finish_call(a, nblk, &s_last);
     return;
   }
   if (table_block) {
     balance_tables(d, tb, bs, a.o, a.in, a.lay, a.status, ok);
-    // the duplicate counts once every tile block has added its own (and the
-    // list block has read the totals); then the accumulators start the next
-    // call at zero
-    if (tid == 0) {
-      const unsigned long long done = s_target / (unsigned long long)nblk * (a.G + 1);
-      s_done = wait_counter(a.sync + 1, done, a.wait_ns);
-      if (!s_done) set_status(a.status, MOONEP_ERR_TIMEOUT);
-    }
-    __syncthreads();
-    for (int i = tid; i < 2 * R; i += kFusedThreads) {
-      a.o.dup_counts[i] = s_done ? __ldcg(a.aux + i) : 0;
-      a.aux[i] = 0;
-    }
-    for (int i = tid; i < R * E; i += kFusedThreads) a.totals[i] = 0;
-    if (tid == 0) a.aux[2 * R] = 0;
+    finish_call(a, nblk, &s_last);
     return;
   }
 
@@ -988,7 +993,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     for (int tt = 0; tt < t; tt++) off += __ldcg(a.hist + (int64_t)(r * a.tpr + tt) * E + e);
     sSrc[e] = off;
   }
-  int32_t *sDup = bs.part[0];  // [2R] duplicate counts of this block (R <= 64: part has 64)
   for (int i = tid; i < 2 * R; i += kFusedThreads) sDup[i] = 0;
   __syncthreads();
   const bool valid = ok && bs.err == 0;
@@ -1049,9 +1053,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   __syncthreads();
   for (int i = tid; i < 2 * R; i += kFusedThreads)
     if (sDup[i]) atomicAdd(a.aux + i, sDup[i]);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) atomicAdd(a.sync + 1, 1ull);
+  finish_call(a, nblk, &s_last);
 }
 
 // ------------------------------------------------------------------ K4

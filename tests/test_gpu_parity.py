@@ -386,7 +386,10 @@ def test_sm_cap_gives_identical_results(monkeypatch):
                      num_sms=16 if how == "config" else None)
         monkeypatch.delenv("MOONEP_NUM_SMS", raising=False)
         assert buf.num_sms == (16 if how != "all" else torch.cuda.get_device_properties(0).multi_processor_count)
-        hid, wn, cu, plan = buf.dispatch(x, w, topk)
+        # the tail rows after the last segment are unspecified: start from zeros
+        hid0 = torch.zeros((sh.R * buf.NvS, sh.H), dtype=torch.bfloat16, device="cuda")
+        wn0 = torch.zeros((sh.R * buf.NvS,), dtype=torch.float32, device="cuda")
+        hid, wn, cu, plan = buf.dispatch(x, w, topk, out=hid0, weights_out=wn0)
         out, wb = buf.combine(plan, hid, wn)
         Wc = W.clone()
         buf.prefetch_weight(plan, Wc)
