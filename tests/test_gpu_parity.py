@@ -196,6 +196,18 @@ def test_random_small_configs(seed):
     _full_pipeline(sh, topk, seed)
 
 
+@pytest.mark.parametrize("K", [6, 7, 16, 32])
+def test_wide_and_odd_top_k(K):
+    """K that divides 32 (16, 32: a token's routes fill half or all of a warp
+    on the single-launch planner) and K that does not (6, 7: the tile path)."""
+    sh = wl.Shape("k", R=4, E=64, K=K, S=97, H=72, Hp=16, B=16, tp=8, weights="softmax")
+    rng = np.random.default_rng(K)
+    p = rng.random(sh.E) ** 3
+    topk = np.stack([np.stack([rng.choice(sh.E, K, replace=False, p=p / p.sum())
+                               for _ in range(sh.S)]) for _ in range(sh.R)]).astype(np.int32)
+    _full_pipeline(sh, topk, K)
+
+
 def test_all_routes_to_one_expert():
     sh = wl.Shape("one", R=4, E=8, K=2, S=300, H=64, Hp=16, B=2, tp=8, weights="softmax")
     topk = np.zeros((4, 300, 2), np.int32)
