@@ -208,6 +208,33 @@ def test_wide_and_odd_top_k(K):
     _full_pipeline(sh, topk, K)
 
 
+def test_largest_tables():
+    """The largest expert table the library takes (E = 4096, R = 64, B = 64,
+    K = 8): the planner's tables no longer fit in shared memory, so the tile
+    path runs with its balance tables in global memory."""
+    sh = wl.Shape("max", R=64, E=4096, K=8, S=16, H=16, Hp=8, B=64, tp=16, weights="softmax")
+    topk = _routing(sh, "zipf_hard", 51)
+    _full_pipeline(sh, topk, 51, dup=False, check_invariants=True)
+
+
+def test_zero_slots():
+    """B = 0: a routing that never overflows a home group plans without slots;
+    one that does reports MOONEP_ERR_SLOTS."""
+    from combine_moonep_plan_gb300 import _lib
+    sh = wl.Shape("b0", R=4, E=16, K=2, S=64, H=32, Hp=8, B=0, tp=4, weights="softmax")
+    topk, _ = wl.routing(sh, "exact0", seed=3)
+    buf, plan, op = _full_pipeline(sh, topk, 3)
+    assert plan.experts_to_copy.numel() == 0
+    buf.destroy()
+    skew = _routing(sh, "zipf_hard", 4)
+    st, _ = _oracle_plan(_cfg_of(sh), skew)
+    assert st == -4
+    buf = _buffer(_cfg_of(sh), H=32)
+    buf.plan(torch.from_numpy(skew).cuda())
+    assert buf.get_status() == _lib.ERR_SLOTS
+    buf.destroy()
+
+
 def test_all_routes_to_one_expert():
     sh = wl.Shape("one", R=4, E=8, K=2, S=300, H=64, Hp=16, B=2, tp=8, weights="softmax")
     topk = np.zeros((4, 300, 2), np.int32)
