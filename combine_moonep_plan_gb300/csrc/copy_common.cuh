@@ -15,14 +15,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   return v;
 }
 
-__device__ __forceinline__ float4 ld_stream_f4(const float4 *p) {
-  float4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // Read once through L2 from memory this kernel also writes (no .nc path).
 __device__ __forceinline__ float4 ld_once_f4(const float4 *p) {
   float4 v;
