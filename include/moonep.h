@@ -37,6 +37,14 @@
  *   - The caller owns every tensor argument.  The library owns the context's
  *     scratch and status word, the plan's arrays and the optional zero-copy
  *     buffers behind moonep_hidden_view / moonep_weight_view.
+ *   - One context plans one batch at a time: its planner scratch (counters,
+ *     per-rank totals) is shared by its moonep_plan calls, so two of them
+ *     must not overlap on the GPU (issue them on one stream, or order the
+ *     streams); use one context per concurrent stream.  The copy entry points
+ *     keep no state between calls and may overlap freely.
+ *   - Kernels are launched with programmatic dependent launch: each waits
+ *     for the previous kernel on its stream before touching memory, so
+ *     stream order is kept as with plain launches.
  */
 #ifndef MOONEP_H
 #define MOONEP_H
