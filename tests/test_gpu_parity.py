@@ -404,6 +404,41 @@ def test_prefetch_rows_odd_row_sizes():
         buf.prefetch_weight(plan, ts[0], ts[1], scales=[ts[2]])
 
 
+# --------------------------------------------------- concurrent contexts
+
+def test_two_contexts_on_two_streams():
+    """Two contexts plan and dispatch at the same time on two streams (their
+    single-launch planners overlap on the GPU); each result equals the
+    oracle's."""
+    from combine_moonep_plan_gb300.api import Buffer
+    shapes = [_small("deepseek_v3", 256), _small("kimi_k2", 192)]
+    runs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for i, sh in enumerate(shapes):
+        topk = _routing(sh, "zipf_hard", 60 + i)
+        buf = Buffer(S=sh.S, H=sh.H, K=sh.K, E=sh.E, num_ep_ranks=sh.R, B=sh.B,
+                     token_padding=sh.tp, zero_copy_views=False)
+        x = torch.randn((sh.R, sh.S, sh.H), device="cuda").bfloat16()
+        runs.append((sh, topk, buf, torch.from_numpy(topk).cuda(), x))
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(3):
+        outs = []
+        for (sh, topk, buf, tk, x), st in zip(runs, streams):
+            with torch.cuda.stream(st):
+                hid, wn, cu, plan = buf.dispatch(x, None, tk)
+                outs.append((plan, hid))
+    torch.cuda.synchronize()
+    for (sh, topk, buf, tk, x), (plan, hid) in zip(runs, outs):
+        assert buf.get_status() == 0
+        st_, op = _oracle_plan(_cfg_of(sh), topk)
+        _cmp_plan(plan, op, _cfg_of(sh))
+        g = torch.from_numpy(decode(op["dst"]).reshape(-1)).cuda()
+        tok = torch.arange(sh.R * sh.S, device="cuda").repeat_interleave(sh.K)
+        assert torch.equal(hid[g].view(torch.int16), x.reshape(-1, sh.H)[tok].view(torch.int16))
+        buf.destroy()
+
+
 # ------------------------------------------------------------ SM cap
 
 def test_sm_cap_gives_identical_results(monkeypatch):
