@@ -811,7 +811,7 @@ def main():
         a0 = time.perf_counter()
         cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20)
         one = time.perf_counter() - a0
-        reps = int(min(20, max(1, 15.0 / max(one, 1e-3))))
+        reps = int(min(100, max(1, 15.0 / max(one, 1e-3))))
         a0 = time.perf_counter()
         v, step_s, per, sample = cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20,
                                               repeats=reps)
