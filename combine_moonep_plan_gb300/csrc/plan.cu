@@ -971,7 +971,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
         if (sCnt[i] != __ldg(a.tpe + i)) set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
     __syncthreads();
   }
-  if (ok) balance_route(d, tb, bs, s_err);
+  if (ok) {
+    // where this tile's routes start inside P_e: sSrc holds the earlier
+    // ranks' routes; add the rank's earlier tiles (all loads in flight at
+    // once; balance_route's barriers order the adds before their use)
+    for (int i = tid; i < E * t; i += kFusedThreads) {
+      const int e = i % E, tt = i / E;
+      atomicAdd(&sSrc[e], __ldcg(a.hist + (int64_t)(r * a.tpr + tt) * E + e));
+    }
+    balance_route(d, tb, bs, s_err);
+  }
 
   if (list_block) {
     balance_lists(d, tb, bs, a.in, a.lay, ok);
@@ -985,14 +994,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   }
 
   // 4. this tile's routes -> (rank, row), duplicate marks, dst
-  for (int e = tid; e < E; e += kFusedThreads) {
-    // where this tile's routes start inside P_e: the earlier ranks, then the
-    // rank's earlier tiles
-    int off = sSrc[e];
-#pragma unroll 4
-    for (int tt = 0; tt < t; tt++) off += __ldcg(a.hist + (int64_t)(r * a.tpr + tt) * E + e);
-    sSrc[e] = off;
-  }
   for (int i = tid; i < 2 * R; i += kFusedThreads) sDup[i] = 0;
   __syncthreads();
   const bool valid = ok && bs.err == 0;
