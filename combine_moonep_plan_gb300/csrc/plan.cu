@@ -783,8 +783,9 @@ plan_assign_kernel(PlanDims d, const int32_t *__restrict__ topk, const int32_t *
 //      each token's K lanes, and writes dst; meanwhile the table block writes
 //      cu_seqlens, zero_fill_ranges, experts_to_copy, remote_stats and the
 //      padding prefix, and the list block the copy and reduce lists;
-//   5. the last block to finish writes the duplicate counts and clears the
-//      cross-block accumulators for the next call.
+//   5. the tile blocks add their duplicate counts straight into the plan
+//      (the table block zeroed them before the meeting); the table block
+//      clears the other set of per-rank totals, which the next call uses.
 // Used when K divides 32 (a token's routes then never straddle a 32-route
 // chunk), the blocks fit on the SMs at once and the tables fit in shared
 // memory; otherwise the three-kernel tile path runs.
@@ -797,13 +798,16 @@ struct FusedArgs {
   PlanDims d;
   const int32_t *topk, *tpe;
   int32_t *hist;    // [G, E] tile counts
-  int32_t *totals;  // [R, E] routes per (rank, expert): zero between calls
-  int32_t *aux;     // [2R] duplicate counts, [1] error bits: zero between calls
+  // Per-rank totals and error bits, two sets used by alternate calls (the
+  // parity of the call count): a call adds into its own set, which the
+  // previous call's table block left at zero, and clears the other set.
+  int32_t *totals;  // [2][R, E] routes per (rank, expert)
+  int32_t *errw;    // [2] error bits
   PlanOut o;
   int32_t *in;
   PlanLayout lay;
   int32_t *status;
-  // [0] arrivals, [1] blocks finished: each grows by G + 2 per call
+  // [0] arrivals: grows by G + 2 per call
   unsigned long long *sync;
   int32_t *dupflag;
   int tpr, G;         // tiles per rank, tile blocks (R * tpr)
@@ -834,30 +838,6 @@ __device__ bool wait_counter(const unsigned long long *p, unsigned long long tar
   return true;
 }
 
-// Every block counts itself finished once per call, after its last read of
-// the per-rank totals and its last add to the duplicate-count accumulators;
-// the last one writes the duplicate counts and clears the accumulators and
-// totals for the next call (no block waits for another here).
-__device__ void finish_call(const FusedArgs &a, int nblk, int *s_last) {
-  const int R = a.d.R, E = a.d.E, tid = threadIdx.x;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned long long old = atomicAdd(a.sync + 1, 1ull);
-    *s_last = old % (unsigned long long)nblk == (unsigned long long)(nblk - 1);
-    __threadfence();
-  }
-  __syncthreads();
-  if (*s_last) {
-    for (int i = tid; i < 2 * R; i += blockDim.x) {
-      a.o.dup_counts[i] = __ldcg(a.aux + i);
-      a.aux[i] = 0;
-    }
-    for (int i = tid; i < R * E; i += blockDim.x) a.totals[i] = 0;
-    if (tid == 0) a.aux[2 * R] = 0;
-  }
-}
-
 size_t fused_smem_words(int R, int E, int B) {
   return (size_t)kFusedWarps * E + (size_t)E * R + (size_t)E + bal_tables_words(R, E, B);
 }
@@ -870,7 +850,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   pdl_launch_dependents();
   extern __shared__ int32_t sm[];
   __shared__ BalSmall bs;
-  __shared__ int s_bad, s_ok, s_err, s_last;
+  __shared__ int s_bad, s_ok, s_err, s_par;
   __shared__ int sDup[2 * kMaxR];  // duplicate counts of this block
   const PlanDims d = a.d;
   const int R = d.R, E = d.E, L = d.L, C = d.C;
@@ -890,7 +870,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   constexpr int items = IT;
   const int wbase = t * kFusedThreads * items + warp * 32 * items;
   int e_reg[items], o_reg[items];
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) {
+    s_bad = 0;
+    // parity of this call: the arrival counter reads between this call's
+    // first and last arrival (no block of it has seen all arrive yet)
+    s_par = (int)((ld_acquire(a.sync) / (unsigned long long)nblk) & 1ull);
+  }
+  if (table_block) {
+    // the tile blocks add their duplicate counts after the meeting
+    for (int i = tid; i < 2 * R; i += kFusedThreads) a.o.dup_counts[i] = 0;
+    __threadfence();
+  }
   if (tile) {
     for (int i = tid; i < kFusedWarps * E; i += kFusedThreads) h[i] = 0;
     __syncthreads();
@@ -921,7 +911,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     if (bad) atomicOr(&s_bad, 1);
     __syncthreads();
     if (tid == 0 && s_bad) {
-      atomicOr(a.aux + 2 * R, kErrBadExpert);
+      atomicOr(a.errw + s_par, kErrBadExpert);
       set_status(a.status, MOONEP_ERR_BAD_EXPERT);
     }
     // 2. warp offsets per expert; the tile's histogram; the rank's totals
@@ -933,7 +923,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
         run += v;
       }
       a.hist[(int64_t)g * E + e] = run;
-      if (run) atomicAdd(a.totals + (int64_t)r * E + e, run);
+      if (run) atomicAdd(a.totals + ((int64_t)s_par * R + r) * E + e, run);
     }
     __threadfence();  // this thread's histogram entries and totals, before the arrival
   }
@@ -947,12 +937,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     const unsigned long long target = old - old % n + n;
     s_ok = wait_counter(a.sync, target + (a.unreachable ? 1 : 0), a.wait_ns);
     if (!s_ok) set_status(a.status, MOONEP_ERR_TIMEOUT);
-    s_err = s_ok ? __ldcg(a.aux + 2 * R) : 0;
+    s_err = s_ok ? __ldcg(a.errw + s_par) : 0;
   }
   __syncthreads();
   const bool ok = s_ok;
   if (ok) {
-    for (int i = tid; i < R * E; i += kFusedThreads) sCnt[i] = __ldcg(a.totals + i);
+    const int32_t *tot_in = a.totals + (int64_t)s_par * R * E;
+    for (int i = tid; i < R * E; i += kFusedThreads) sCnt[i] = __ldcg(tot_in + i);
     __syncthreads();
     for (int e = tid; e < E; e += kFusedThreads) {
       int tot = 0, before = 0;
@@ -984,12 +975,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
 
   if (list_block) {
     balance_lists(d, tb, bs, a.in, a.lay, ok);
-    finish_call(a, nblk, &s_last);
     return;
   }
   if (table_block) {
     balance_tables(d, tb, bs, a.o, a.in, a.lay, a.status, ok);
-    finish_call(a, nblk, &s_last);
+    // the other set of totals and error bits, used by the next call, back to
+    // zero (the previous call, its last user, has completed)
+    int32_t *other = a.totals + (int64_t)(1 - s_par) * R * E;
+    for (int i = tid; i < R * E; i += kFusedThreads) other[i] = 0;
+    if (tid == 0) a.errw[1 - s_par] = 0;
     return;
   }
 
@@ -1053,8 +1047,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   }
   __syncthreads();
   for (int i = tid; i < 2 * R; i += kFusedThreads)
-    if (sDup[i]) atomicAdd(a.aux + i, sDup[i]);
-  finish_call(a, nblk, &s_last);
+    if (sDup[i]) atomicAdd(a.o.dup_counts + i, sDup[i]);
 }
 
 // ------------------------------------------------------------------ K4
@@ -1152,7 +1145,7 @@ int64_t plan_totals_offset(int R, int E, int C, int sms) {
 }
 
 int64_t plan_scratch_words(int R, int E, int C, int sms) {
-  return plan_totals_offset(R, E, C, sms) + (int64_t)R * E + 2 * R + 8;
+  return plan_totals_offset(R, E, C, sms) + 2 * (int64_t)R * E + 8;
 }
 
 int plan_fused_tiles(int C, int items) {
@@ -1244,7 +1237,7 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     fa.tpr = plan_fused_tiles(d.C, items);
     fa.G = d.R * fa.tpr;
     fa.totals = ctx->d_hist + plan_totals_offset(d.R, d.E, d.C, ctx->sms_device);
-    fa.aux = fa.totals + (int64_t)d.R * d.E;
+    fa.errw = fa.totals + 2 * (int64_t)d.R * d.E;
     fa.o = o;
     fa.in = in;
     fa.lay = lay;
