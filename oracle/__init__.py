@@ -57,6 +57,10 @@ def _bind(path):
     lib.mo_combine.argtypes = [ci] * 3 + [i64] * 4 + [vp, vp, i64, vp, vp, vp, vp]
     lib.mo_prefetch.restype = None
     lib.mo_prefetch.argtypes = [ci] * 3 + [vp, i64, i64, i64, vp]
+    lib.mo_fold_duplicates.restype = None
+    lib.mo_fold_duplicates.argtypes = [ci] * 3 + [i64] * 4 + [vp, vp]
+    lib.mo_combine_primaries.restype = None
+    lib.mo_combine_primaries.argtypes = [ci] * 3 + [i64] * 4 + [vp, vp, i64, vp, vp, vp, vp]
     lib.mo_prepare.restype = None
     lib.mo_prepare.argtypes = [ci] * 4 + [i64] + [vp] * 5
     lib.mo_prefetch_bytes.restype = None
@@ -148,6 +152,30 @@ class Oracle:
         self.lib.mo_prefetch(R, E, B, _ptr(etc), HHp, c0, c1, _ptr(W))
         return W
 
+    def fold_duplicates(self, R, S, K, NvS, H, dst, y, c0=0, c1=None):
+        """Duplicate prologue, in place on y [R*NvS, H] uint16."""
+        c1 = H if c1 is None else c1
+        dst = np.ascontiguousarray(dst, dtype=np.int32)
+        assert y.dtype == np.uint16 and y.flags["C_CONTIGUOUS"]
+        self.lib.mo_fold_duplicates(R, S, K, NvS, H, c0, c1, _ptr(dst), _ptr(y))
+        return y
+
+    def combine_primaries(self, R, S, K, NvS, H, dst, y, w_nvs=None, tokens=None, c0=0,
+                          c1=None):
+        """Combine over primary routes: (out [ntok, H] uint16, w_out [ntok, K])."""
+        c1 = H if c1 is None else c1
+        dst = np.ascontiguousarray(dst, dtype=np.int32)
+        if tokens is not None:
+            tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+            ntok = len(tokens)
+        else:
+            ntok = R * S
+        out = np.zeros((ntok, H), np.uint16)
+        w_out = np.zeros((ntok, K), np.float32) if w_nvs is not None else None
+        self.lib.mo_combine_primaries(R, S, K, NvS, H, c0, c1, _ptr(dst), _ptr(tokens), ntok,
+                                      _ptr(y), _ptr(w_nvs), _ptr(out), _ptr(w_out))
+        return out, w_out
+
     def prepare(self, R, S, K, E, H, ntok, hidden, topk, w=None, want_tpe=True):
         """Decode-path padding in place (hidden [R,S,H] uint16 or None, topk
         [R,S,K] int32, w [R,S,K] fp32 or None); returns tokens_per_expert
@@ -218,6 +246,14 @@ def prefetch_bytes(*a, **k):
 
 def prepare(*a, **k):
     return _default().prepare(*a, **k)
+
+
+def fold_duplicates(*a, **k):
+    return _default().fold_duplicates(*a, **k)
+
+
+def combine_primaries(*a, **k):
+    return _default().combine_primaries(*a, **k)
 
 
 def reduce(*a, **k):

@@ -431,6 +431,61 @@ void mo_combine(int R, int S, int K, int64_t NvS, int64_t H, int64_t c0,
   }
 }
 
+/* ------------------------------------------- deduplicated combine path */
+
+/* Duplicate prologue [API, Buffer.combine: a prologue accumulates duplicate
+ * physical rows into their primary rows in fp32, then the main kernel
+ * gathers and reduces]: for every token and every rank holding more than one
+ * of its routes, the primary row (the token's first route on that rank, the
+ * one with dst >= 0) becomes the bf16 RNE rounding of the fp32 sum, in k
+ * order, of the token's rows on that rank.  Duplicate rows are left as they
+ * are.  y [R*NvS, H] bf16 bits, modified in place; columns [c0, c1). */
+void mo_fold_duplicates(int R, int S, int K, int64_t NvS, int64_t H, int64_t c0, int64_t c1,
+                        const int32_t *dst, uint16_t *y) {
+  for (int64_t t = 0; t < (int64_t)R * S; t++) {
+    const int32_t *d = dst + t * K;
+    for (int k = 0; k < K; k++) {
+      if (d[k] < 0) continue;  /* primary route */
+      const int64_t g = d[k];
+      const int64_t j = g / NvS;
+      int dups = 0;
+      for (int k2 = k + 1; k2 < K; k2++)
+        if (d[k2] < 0 && decode_row(d[k2]) / NvS == j) dups++;
+      if (!dups) continue;
+      for (int64_t c = c0; c < c1; c++) {
+        float acc = bf16_to_f32(y[g * H + c]);
+        for (int k2 = k + 1; k2 < K; k2++)
+          if (d[k2] < 0 && decode_row(d[k2]) / NvS == j)
+            acc = acc + bf16_to_f32(y[decode_row(d[k2]) * H + c]);
+        y[g * H + c] = mo_f32_to_bf16(acc);
+      }
+    }
+  }
+}
+
+/* The main combine of the deduplicated path: out[t] = bf16 RNE of the fp32
+ * sum, in k order, over the token's primary routes only (each one already
+ * holds its rank's fold).  Weights are gathered for every route as in
+ * mo_combine.  out [ntok, H] for the tokens listed (all when tokens is NULL). */
+void mo_combine_primaries(int R, int S, int K, int64_t NvS, int64_t H, int64_t c0, int64_t c1,
+                          const int32_t *dst, const int64_t *tokens, int64_t ntok,
+                          const uint16_t *y, const float *w_nvs, uint16_t *out, float *w_out) {
+  (void)NvS;
+  if (!tokens) ntok = (int64_t)R * S;
+  for (int64_t i = 0; i < ntok; i++) {
+    const int64_t t = tokens ? tokens[i] : i;
+    const int32_t *d = dst + t * K;
+    for (int64_t c = c0; c < c1; c++) {
+      float acc = bf16_to_f32(y[(int64_t)d[0] * H + c]);  /* route 0 is always primary */
+      for (int k = 1; k < K; k++)
+        if (d[k] >= 0) acc = acc + bf16_to_f32(y[(int64_t)d[k] * H + c]);
+      out[i * H + c] = mo_f32_to_bf16(acc);
+    }
+    if (w_nvs && w_out)
+      for (int k = 0; k < K; k++) w_out[i * K + k] = w_nvs[decode_row(d[k])];
+  }
+}
+
 /* ------------------------------------------------------------ prefetch */
 
 /* Copy expert e's weight into every slot that names it; unused slots (-1) are

@@ -77,6 +77,15 @@ void mo_combine(int R, int S, int K, int64_t NvS, int64_t H, int64_t c0,
                 int64_t ntok, const uint16_t *y, const float *w_nvs,
                 uint16_t *out, float *w_out);
 
+/* Deduplicated combine path: the duplicate prologue (primary rows become the
+ * bf16 RNE of the fp32 k-order sum of the token's rows on their rank; y
+ * modified in place) and the combine over primary routes only. */
+void mo_fold_duplicates(int R, int S, int K, int64_t NvS, int64_t H, int64_t c0, int64_t c1,
+                        const int32_t *dst, uint16_t *y);
+void mo_combine_primaries(int R, int S, int K, int64_t NvS, int64_t H, int64_t c0, int64_t c1,
+                          const int32_t *dst, const int64_t *tokens, int64_t ntok,
+                          const uint16_t *y, const float *w_nvs, uint16_t *out, float *w_out);
+
 /* Decode-path preparation, in place: ids < 0 -> expert 0 with weight 0;
  * rows s >= ntok[r] (ntok NULL: none) -> zero hidden row, expert 0, weight 0;
  * tpe [R,E] (optional) = per-rank counts of the resulting ids < E.

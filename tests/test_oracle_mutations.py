@@ -52,6 +52,10 @@ MUTATIONS = {
     "prepare_keeps_invalid_weight": ("          topk[i] = 0;\n          if (w) w[i] = 0.0f;", "          topk[i] = 0;"),
     "prepare_counts_before_padding": ("    if (tpe) {\n      for (int e = 0; e < E; e++) tpe[(int64_t)r * E + e] = 0;",
                                       "    if (tpe) {\n      for (int e = 0; e < E; e++) tpe[(int64_t)r * E + e] = (e == 0) ? -(S - n) * K : 0;"),
+    "fold_takes_other_ranks": ("          if (d[k2] < 0 && decode_row(d[k2]) / NvS == j)\n            acc = acc",
+                               "          if (1)\n            acc = acc"),
+    "primaries_combine_adds_duplicates": ("        if (d[k] >= 0) acc = acc + bf16_to_f32(y[(int64_t)d[k] * H + c]);",
+                                          "        acc = acc + bf16_to_f32(y[decode_row(d[k]) * H + c]);"),
     "dispatch_no_weight_zero": ("if (w_out) w_out[g] = 0.0f;", "if (w_out) w_out[g] = w_out[g];"),
     "cu_exclusive": ("cu[(int64_t)j * EB + x] = (int32_t)end;", "cu[(int64_t)j * EB + x] = (int32_t)(end - padded);"),
     "slots_filled_from_end": ("etc[(int64_t)j * B + nslots] = e;", "etc[(int64_t)j * B + (B - 1 - nslots)] = e;"),
@@ -82,6 +86,10 @@ pins = [
     ("prefetch_copy", lambda: P.test_prefetch_copies_home_rows(o)),
     ("prefetch_bytes", lambda: P.test_prefetch_bytes_copies_packed_rows(o)),
     ("prefetch_bytes_window", lambda: P.test_prefetch_bytes_of_bf16_rows_is_the_bf16_prefetch(o)),
+    ("folded_hand", lambda: P.test_folded_combine_hand_example(o)),
+    ("folded_nodup", lambda: P.test_folded_combine_equals_direct_without_duplicates(o)),
+    ("folded_top2", lambda: P.test_folded_identity_combine_is_k_times_x_for_top2(o)),
+    ("folded_bound", lambda: P.test_folded_combine_error_bound(o)),
     ("prepare_hand", lambda: P.test_prepare_hand_example(o)),
     ("prepare_random", lambda: P.test_prepare_random_properties(o)),
     ("reduce_const", lambda: P.test_reduce_constant_fill_counts_copies(o)),

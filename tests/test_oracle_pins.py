@@ -636,3 +636,91 @@ def test_oracle_matches_restatement_random_small(oracle_mod, seed):
         for f in ("dst", "experts_to_copy", "cu_seqlens", "zero_fill_ranges", "remote_stats",
                   "dup_counts"):
             assert np.array_equal(p[f], rp[f]), f
+
+
+# ------------------------------------------ deduplicated combine (prologue)
+
+def test_folded_combine_hand_example(oracle_mod):
+    """One token, K = 3, routes on ranks A, A, B (route 1 a duplicate of route
+    0), bf16 rows 1.0, 2^-8, 2^-8 (NvS = 4, H = 1).  The prologue folds rank
+    A: bf16(1 + 2^-8) = 1.0 (a tie, to even); the combine then adds rank B's
+    row: bf16(1 + 2^-8) = 1.0.  The direct k-order sum gives (1 + 2^-8) +
+    2^-8 = 1 + 2^-7 exactly.  The duplicate row itself is untouched."""
+    f2b = lambda v: int(np.array([v], np.float32).view(np.uint32)[0] >> 16)
+    R, S, K, NvS, H = 2, 1, 3, 4, 1
+    # token 0 of rank 0: routes 0 and 1 on rank 0 (rows 0 and 1), route 2 on rank 1 (row 4)
+    dst = np.array([[0, -(1 + 1), 4], [5, 6, 7]], np.int32).reshape(R, S * K)
+    y = np.zeros((R * NvS, H), np.uint16)
+    y[0, 0], y[1, 0], y[4, 0] = f2b(1.0), f2b(2.0 ** -8), f2b(2.0 ** -8)
+    y[5, 0] = y[6, 0] = y[7, 0] = f2b(1.0)
+    direct, _ = oracle_mod.combine(R, S, K, NvS, H, dst, y)
+    assert direct[0, 0] == f2b(1.0 + 2.0 ** -7)
+    yf = y.copy()
+    oracle_mod.fold_duplicates(R, S, K, NvS, H, dst, yf)
+    assert yf[0, 0] == f2b(1.0) and yf[1, 0] == y[1, 0]
+    assert np.array_equal(np.delete(yf, 0, axis=0), np.delete(y, 0, axis=0))
+    folded, _ = oracle_mod.combine_primaries(R, S, K, NvS, H, dst, yf)
+    assert folded[0, 0] == f2b(1.0)
+    assert folded[1, 0] == f2b(3.0) == direct[1, 0]   # no duplicates: same as direct
+
+
+def test_folded_combine_equals_direct_without_duplicates(oracle_mod):
+    """When no token has two routes on one rank (E = R, distinct experts, nothing
+    moves) the prologue changes nothing and the two combines agree bit for bit."""
+    sh = wl.Shape("nodup", R=4, E=4, K=2, S=64, H=16, Hp=8, B=1, tp=4, weights="softmax")
+    topk, _ = wl.routing(sh, "exact0", seed=2)
+    st, p = _plan(oracle_mod, _cfg(sh), topk)
+    assert st == 0 and np.all(p["dup_counts"] == 0)
+    NvS = p["NvS"]
+    rng = np.random.default_rng(4)
+    y = wl.bf16_bits_from_f32(rng.standard_normal((sh.R * NvS, sh.H)).astype(np.float32))
+    yf = y.copy()
+    oracle_mod.fold_duplicates(sh.R, sh.S, sh.K, NvS, sh.H, p["dst"], yf)
+    assert np.array_equal(yf, y)
+    a, _ = oracle_mod.combine(sh.R, sh.S, sh.K, NvS, sh.H, p["dst"], y)
+    b, _ = oracle_mod.combine_primaries(sh.R, sh.S, sh.K, NvS, sh.H, p["dst"], yf)
+    assert np.array_equal(a, b)
+
+
+def test_folded_identity_combine_is_k_times_x_for_top2(oracle_mod):
+    """Identity experts with K = 2: a rank holds one or both of a token's
+    rows, every fold and sum is exact (x or 2x), so the deduplicated combine
+    of dispatch(x) is 2x bit for bit, like the direct one; duplicates exist."""
+    sh = wl.SHAPES["tiny"]
+    topk, _ = wl.routing(sh, "zipf", zipf_s=3.0, seed=7)
+    st, p = _plan(oracle_mod, _cfg(sh), topk)
+    assert st == 0 and p["dup_counts"][:, 0].sum() > 0
+    NvS = p["NvS"]
+    x = wl.hidden_bf16(sh, 7)
+    y = np.zeros((sh.R * NvS, sh.H), np.uint16)
+    oracle_mod.dispatch(sh.R, sh.S, sh.K, sh.E, sh.B, NvS, sh.H, p["dst"], p["zero_fill_ranges"],
+                        x, None, y)
+    oracle_mod.fold_duplicates(sh.R, sh.S, sh.K, NvS, sh.H, p["dst"], y)
+    out, _ = oracle_mod.combine_primaries(sh.R, sh.S, sh.K, NvS, sh.H, p["dst"], y)
+    assert np.array_equal(oracle_mod.bf16_to_f32(out), 2 * oracle_mod.bf16_to_f32(x))
+
+
+def test_folded_combine_error_bound(oracle_mod):
+    """Random rows, K = 8 with many duplicates: a bf16 rounding errs by at
+    most half an ulp, 2^-8 of the rounded value; the folds' values add up to
+    at most sum_k |y_k| and so does the result (the fp32 adds err far less),
+    so the deduplicated combine stays within 2^-7 * sum_k |y_k| of the exact
+    fp64 sum.  (Not within an ulp of the result: under cancellation a fold's
+    rounding is large next to it.)"""
+    sh = wl.Shape("f8", R=4, E=8, K=8, S=48, H=32, Hp=8, B=2, tp=4, weights="softmax")
+    rng = np.random.default_rng(9)
+    topk = rng.integers(0, sh.E, (sh.R, sh.S, sh.K)).astype(np.int32)
+    st, p = _plan(oracle_mod, _cfg(sh), topk)
+    assert st == 0 and p["dup_counts"][:, 0].sum() > 0
+    NvS = p["NvS"]
+    y = wl.bf16_bits_from_f32(rng.standard_normal((sh.R * NvS, sh.H)).astype(np.float32))
+    exact = oracle_mod.bf16_to_f32(y).astype(np.float64)[decode(p["dst"]).reshape(-1)]
+    exact = exact.reshape(sh.R * sh.S, sh.K, sh.H).sum(axis=1)
+    yf = y.copy()
+    oracle_mod.fold_duplicates(sh.R, sh.S, sh.K, NvS, sh.H, p["dst"], yf)
+    out, _ = oracle_mod.combine_primaries(sh.R, sh.S, sh.K, NvS, sh.H, p["dst"], yf)
+    got = oracle_mod.bf16_to_f32(out).astype(np.float64)
+    mag = np.abs(oracle_mod.bf16_to_f32(y).astype(np.float64)[decode(p["dst"]).reshape(-1)])
+    mag = mag.reshape(sh.R * sh.S, sh.K, sh.H).sum(axis=1)
+    assert np.all(np.abs(got - exact) <= 2.0 ** -7 * mag + 1e-30)
+    assert np.abs(got - exact).max() > 0   # the bound is not vacuous here
