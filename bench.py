@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mxfp4", action="store_true",
                     help="skip the packed-MXFP4 weight prefetch measurement")
+    ap.add_argument("--no-dedup", action="store_true",
+                    help="skip the deduplicated dispatch/combine measurement")
     ap.add_argument("--step-only", action="store_true",
                     help="time the step and nothing else (no sweep, chain, preparation, MXFP4, "
                          "end-to-end or CPU legs): a clean launch list for profilers")
@@ -336,6 +338,81 @@ def run_mxfp4_prefetch(buf, step, sh, steps, torch, peak):
             "ms": round(ms, 5), "GB": round(nbytes / 1e9, 4), "slots_used": U,
             "GBps": round(nbytes / (ms / 1e3) / 1e9, 1) if ms > 0 else None,
             "frac_of_peak": round(nbytes / (ms / 1e3) / 1e9 / peak, 4) if ms > 0 else None}
+
+
+def run_dedup(sh, step, steps, torch, peak):
+    """The deduplicated data flow on the step's routing: dispatch copies only
+    the primary rows and expands the duplicates in an epilogue; combine folds
+    every rank's duplicates into their primaries first and then sums the
+    primaries.  On one GPU both move more HBM bytes than the direct kernels;
+    what they save is the rows that would cross between ranks
+    (cross_rank_rows, direct vs deduplicated)."""
+    from combine_moonep_plan_gb300.api import Buffer
+    R, S, K, H = sh.R, sh.S, sh.K, sh.H
+    buf = Buffer(S=S, H=H, K=K, E=sh.E, num_ep_ranks=R, B=sh.B, token_padding=sh.tp,
+                 zero_copy_views=False, dup_records=True)
+    plan = buf.plan(step.topk, step.tpe)
+    y = step.hid_nvsh.clone()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+    ms = {
+        "plan_with_dup_records": timed(lambda: buf.plan(step.topk, step.tpe, plan=plan)),
+        "dispatch_dedup": timed(lambda: buf.dispatch(step.hidden, step.w_sk, plan=plan,
+                                                     out=step.hid_nvsh, weights_out=step.w_nvs,
+                                                     dedup=True)),
+        "dispatch": timed(lambda: buf.dispatch(step.hidden, step.w_sk, plan=plan,
+                                               out=step.hid_nvsh, weights_out=step.w_nvs)),
+        "combine_dedup": timed(lambda: buf.combine(plan, y, step.w_nvs, out=step.out,
+                                                   weights_out=step.w_back, dedup=True)),
+        "combine": timed(lambda: buf.combine(plan, y, step.w_nvs, out=step.out,
+                                             weights_out=step.w_back)),
+    }
+    status = buf.get_status()
+    dst = plan.dst.cpu().numpy().astype(np.int64).reshape(R, S * K)
+    g = np.where(dst >= 0, dst, -dst - 1)
+    dest_rank = g // buf.NvS
+    remote = dest_rank != np.arange(R)[:, None]
+    dc = plan.dup_counts.cpu().numpy().astype(np.int64)
+    D, Gr = int(dc[:, 0].sum()), int(dc[:, 1].sum())
+    N = R * S * K
+    zfr = plan.zero_fill_ranges.cpu().numpy().astype(np.int64)
+    P = int((zfr[..., 1] - zfr[..., 0]).sum())
+    row = H * 2
+    nbytes = {
+        # primaries + padding rows written, weights for every route; then the
+        # epilogue reads Gr primary rows and writes D duplicate rows
+        "dispatch_dedup": R * S * row + N * 8 + (N - D + P) * row + (N + P) * 4
+        + (Gr + D) * row,
+        "dispatch": R * S * row + N * 8 + (N + P) * (row + 4),
+        # the fold reads Gr + D rows and writes Gr; the sum reads N - D rows
+        "combine_dedup": (2 * Gr + D) * row + (N - D) * row + N * 12 + R * S * row,
+        "combine": N * row + N * 12 + R * S * row,
+    }
+    ops = {}
+    for k, v in ms.items():
+        e = {"ms": round(v, 5)}
+        if k in nbytes and v > 0:
+            e["GB"] = round(nbytes[k] / 1e9, 4)
+            e["frac_of_peak"] = round(nbytes[k] / (v / 1e3) / 1e9 / peak, 4)
+        ops[k] = e
+    buf.destroy()
+    del y
+    torch.cuda.empty_cache()
+    return {"ops": ops, "duplicate_routes": D, "duplicate_groups": Gr, "routes": N,
+            "cross_rank_rows": {"direct": int(remote.sum()),
+                                "deduplicated": int((remote & (dst >= 0)).sum())},
+            "device_status": status}
 
 
 def run_prepare(buf, sh, steps, torch):
@@ -794,6 +871,8 @@ def main():
         torch.cuda.synchronize()
 
     prep = run_prepare(buf, sh, 20, torch) if not args.step_only else None
+    dedup = (run_dedup(sh, step, max(10, min(args.steps, 50)), torch, peak)
+             if not args.step_only and not args.no_dedup else None)
 
     mxfp4 = None
     if not args.no_mxfp4:
@@ -840,6 +919,7 @@ def main():
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks, "sweep": sweep, "mxfp4_prefetch": mxfp4, "decode_prepare": prep,
+        "dedup_path": dedup,
         "device_status": status,
     }
     if graph_ms is not None:

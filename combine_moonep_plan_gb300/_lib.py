@@ -29,6 +29,7 @@ EXPORTS = (
     "moonep_query_sizes", "moonep_ctx_create", "moonep_ctx_destroy", "moonep_ctx_free",
     "moonep_ctx_destroyed", "moonep_plan_create", "moonep_plan_destroy",
     "moonep_plan_clone", "moonep_plan", "moonep_dispatch", "moonep_combine",
+    "moonep_dispatch_dedup", "moonep_combine_dedup",
     "moonep_prefetch_weight", "moonep_prefetch_rows", "moonep_reduce_redundant_grad", "moonep_hidden_view",
     "moonep_weight_view", "moonep_get_status", "moonep_strerror", "moonep_num_sms",
     "moonep_plan_noalloc", "moonep_prepare",
@@ -90,6 +91,8 @@ def load(path: str = LIB_PATH):
         "moonep_plan": (ci, [vp, vp, vp, planp, vp]),
         "moonep_dispatch": (ci, [vp, planp, vp, vp, vp, vp, vp]),
         "moonep_combine": (ci, [vp, planp, vp, vp, vp, vp, vp]),
+        "moonep_dispatch_dedup": (ci, [vp, planp, vp, vp, vp, vp, vp]),
+        "moonep_combine_dedup": (ci, [vp, planp, vp, vp, vp, vp, vp]),
         "moonep_prefetch_weight": (ci, [vp, planp, ci, ctypes.POINTER(vp), i64, vp]),
         "moonep_prefetch_rows": (ci, [vp, planp, ci, ctypes.POINTER(vp), ctypes.POINTER(i64), vp]),
         "moonep_prepare": (ci, [vp, ctypes.POINTER(ctypes.c_int32), vp, vp, vp, vp, vp]),

@@ -195,8 +195,11 @@ class Buffer:
                  topk_experts_sk: torch.Tensor | None = None,
                  tokens_per_expert: torch.Tensor | None = None, plan: CommPlan | None = None,
                  zero_copy: bool = False, router_weights_zero_copy: bool = False,
-                 out: torch.Tensor | None = None, weights_out: torch.Tensor | None = None):
+                 out: torch.Tensor | None = None, weights_out: torch.Tensor | None = None,
+                 dedup: bool = False):
         """Fresh dispatch (plan is None) or plan-reuse dispatch [Buffer.dispatch].
+        dedup=True copies only the primary rows and expands the duplicates in
+        an epilogue (same result; needs a Buffer made with dup_records=True).
 
         Returns (hidden_nvsh [R*NvS, H] bf16, route_weights_nvs [R*NvS] fp32 or
         None, cu_seqlens [R, E+B] int32 (None on plan reuse), plan)."""
@@ -220,15 +223,18 @@ class Buffer:
                     else torch.empty((R * NvS,), dtype=torch.float32, device=hidden_sh.device)
             wop = _check_tensor(weights_out, "route_weights_nvs", torch.float32, (R * NvS,))
             w_out = weights_out
-        check(_lib.load().moonep_dispatch(self._ctx, plan.struct, hp, wp, op, wop, _stream()),
-              "moonep_dispatch")
+        fn = "moonep_dispatch_dedup" if dedup else "moonep_dispatch"
+        check(getattr(_lib.load(), fn)(self._ctx, plan.struct, hp, wp, op, wop, _stream()), fn)
         return out, w_out, (plan.cu_seqlens if fresh else None), plan
 
     # ----------------------------------------------------------- combine
     def combine(self, plan: CommPlan, hidden_nvsh: torch.Tensor,
                 route_weights_nvs: torch.Tensor | None = None, out: torch.Tensor | None = None,
-                weights_out: torch.Tensor | None = None):
+                weights_out: torch.Tensor | None = None, dedup: bool = False):
         """Gather and K-sum back to token-major [Buffer.combine].
+        dedup=True first folds every rank's duplicate rows of a token into its
+        primary row (fp32, one bf16 rounding, IN PLACE on hidden_nvsh), then
+        sums the primaries only; needs a Buffer made with dup_records=True.
         Returns (hidden_sh [R, S, H] bf16, route_weights_sk [R, S, K] or None)."""
         R, S, H, K, NvS = self.R, self.S, self.H, self.K, self.NvS
         yp = _check_tensor(hidden_nvsh, "hidden_nvsh", torch.bfloat16, (R * NvS, H))
@@ -244,8 +250,8 @@ class Buffer:
             wop = _check_tensor(weights_out, "route_weights_sk", torch.float32, (R, S, K))
         else:
             weights_out = None
-        check(_lib.load().moonep_combine(self._ctx, plan.struct, yp, wp, op, wop, _stream()),
-              "moonep_combine")
+        fn = "moonep_combine_dedup" if dedup else "moonep_combine"
+        check(getattr(_lib.load(), fn)(self._ctx, plan.struct, yp, wp, op, wop, _stream()), fn)
         return out, weights_out
 
     # --------------------------------------------------- weights / grads

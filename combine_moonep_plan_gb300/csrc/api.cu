@@ -107,6 +107,8 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
   ctx->blocks_combine = occupancy_combine(c.K);
   ctx->blocks_copy = occupancy_copy();
   ctx->blocks_reduce = occupancy_reduce();
+  ctx->blocks_expand = occupancy_dedup(false);
+  ctx->blocks_fold = occupancy_dedup(true);
   const size_t hist =
       (size_t)plan_scratch_words(c.R, c.E, ctx->C, ctx->sms_device) * sizeof(int32_t);
   const size_t ord = (size_t)c.R * ctx->C * sizeof(int32_t);
@@ -284,6 +286,40 @@ int moonep_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
       ((uintptr_t)w_sk_out & 3))
     return MOONEP_ERR_INVALID_ARG;
   return launch_combine(ctx, plan, y_nvsh, w_nvs, out_sh, w_sk_out, (cudaStream_t)stream);
+}
+
+int moonep_dispatch_dedup(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *hidden,
+                          const float *w_sk, uint16_t *hidden_nvsh, float *w_nvs, void *stream) {
+  int st = check_ctx(ctx);
+  if (st) return st;
+  if ((st = check_plan(ctx, plan))) return st;
+  if (!(plan->flags & MOONEP_PLAN_DUP_RECORDS)) return MOONEP_ERR_INVALID_ARG;
+  const int64_t ntok = (int64_t)ctx->cfg.R * ctx->cfg.S;
+  if (!hidden_nvsh || (ntok > 0 && !hidden)) return MOONEP_ERR_INVALID_ARG;
+  if ((w_sk == nullptr) != (w_nvs == nullptr)) return MOONEP_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(hidden_nvsh) || ((uintptr_t)w_sk & 3) ||
+      ((uintptr_t)w_nvs & 3))
+    return MOONEP_ERR_INVALID_ARG;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if ((st = launch_dispatch(ctx, plan, hidden, w_sk, hidden_nvsh, w_nvs, s, true))) return st;
+  return launch_expand(ctx, plan, hidden_nvsh, s);
+}
+
+int moonep_combine_dedup(moonep_ctx *ctx, const moonep_comm_plan *plan, uint16_t *y_nvsh,
+                         const float *w_nvs, uint16_t *out_sh, float *w_sk_out, void *stream) {
+  int st = check_ctx(ctx);
+  if (st) return st;
+  if ((st = check_plan(ctx, plan))) return st;
+  if (!(plan->flags & MOONEP_PLAN_DUP_RECORDS)) return MOONEP_ERR_INVALID_ARG;
+  const int64_t ntok = (int64_t)ctx->cfg.R * ctx->cfg.S;
+  if (ntok > 0 && (!y_nvsh || !out_sh)) return MOONEP_ERR_INVALID_ARG;
+  if ((w_nvs == nullptr) != (w_sk_out == nullptr)) return MOONEP_ERR_INVALID_ARG;
+  if (!aligned16(y_nvsh) || !aligned16(out_sh) || ((uintptr_t)w_nvs & 3) ||
+      ((uintptr_t)w_sk_out & 3))
+    return MOONEP_ERR_INVALID_ARG;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if ((st = launch_fold(ctx, plan, y_nvsh, s))) return st;
+  return launch_combine(ctx, plan, y_nvsh, w_nvs, out_sh, w_sk_out, s, true);
 }
 
 int moonep_prefetch_weight(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj,

@@ -70,8 +70,10 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 // thread leave room for more resident warps in small blocks).  KB: rows
 // loaded per batch (K = 8 reads 2 KB of each row per unit, in two batches of
 // four rows; K = 2 reads 4 KB of both rows at once: 0.98 of the copy
-// bandwidth on the Mixtral shape, 0.95 with 2 KB).
-template <int KT, int U, int BT, int KB>
+// bandwidth on the Mixtral shape, 0.95 with 2 KB).  PRIM: sum the primary
+// routes only (dst >= 0; the duplicates were folded into them), a separate
+// instantiation so that the direct kernel carries none of its code.
+template <int KT, int U, int BT, int KB, bool PRIM>
 __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
   pdl_wait();
   pdl_launch_dependents();
@@ -90,6 +92,9 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
     const int32_t d_cur = d_next;
     if (u + nw < units && lane < K) d_next = __ldg(a.dst + ((u + nw) / a.nchunk) * K + lane);
     int64_t g = 0;
+    // duplicate routes that the prologue folded into their primaries (the
+    // same for every lane: route k's sign, broadcast)
+    const unsigned dupm = PRIM ? __ballot_sync(0xffffffffu, lane < K && d_cur < 0) : 0u;
     if (lane < K) {
       g = decode_row(d_cur);
       if (g >= a.total_rows) {
@@ -108,16 +113,18 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
 #pragma unroll
         for (int kk = 0; kk < KB; kk++) {
           const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k0 + kk) * a.H8;
+          const bool skip = (dupm >> (k0 + kk)) & 1u;
 #pragma unroll
           for (int i = 0; i < U; i++) {
             const int v = v0 + 32 * i;
-            if (v < a.H8) x[kk][i] = ld_stream(row + v);
+            if (v < a.H8 && !skip) x[kk][i] = ld_stream(row + v);
           }
         }
 #pragma unroll
         for (int i = 0; i < U; i++) {
 #pragma unroll
           for (int kk = 0; kk < KB; kk++) {
+            if ((dupm >> (k0 + kk)) & 1u) continue;
             if (k0 + kk == 0) set_bf16x8(acc[i], x[kk][i]);
             else add_bf16x8(acc[i], x[kk][i]);
           }
@@ -126,6 +133,7 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
     } else {
       for (int k = 0; k < K; k++) {
         const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k) * a.H8;
+        if ((dupm >> k) & 1u) continue;
 #pragma unroll
         for (int i = 0; i < U; i++) {
           const int v = v0 + 32 * i;
@@ -145,26 +153,28 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
 }
 
 template <int KT, int U, int BT, int KB>
-cudaError_t launch(const Args &a, int grid, cudaStream_t st) {
-  return launch_pdl(combine_kernel<KT, U, BT, KB>, grid, BT, 0, st, false, a);
+cudaError_t launch(const Args &a, bool prim, int grid, cudaStream_t st) {
+  return prim ? launch_pdl(combine_kernel<KT, U, BT, KB, true>, grid, BT, 0, st, false, a)
+              : launch_pdl(combine_kernel<KT, U, BT, KB, false>, grid, BT, 0, st, false, a);
 }
 
 }  // namespace
 
 int occupancy_combine(int K) {
   int n = 0;
-  void *f = K == 1 ? (void *)combine_kernel<1, 4, 256, 1>
-          : K == 2 ? (void *)combine_kernel<2, 8, 128, 2>
-          : K == 4 ? (void *)combine_kernel<4, 4, 256, 4>
-          : K == 8 ? (void *)combine_kernel<8, 4, 128, 4>
-                   : (void *)combine_kernel<0, 2, 256, 1>;
+  void *f = K == 1 ? (void *)combine_kernel<1, 4, 256, 1, false>
+          : K == 2 ? (void *)combine_kernel<2, 8, 128, 2, false>
+          : K == 4 ? (void *)combine_kernel<4, 4, 256, 4, false>
+          : K == 8 ? (void *)combine_kernel<8, 4, 128, 4, false>
+                   : (void *)combine_kernel<0, 2, 256, 1, false>;
   const int bt = (K == 8 || K == 2) ? 128 : 256;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, bt, 0) != cudaSuccess) n = 1;
   return n > 0 ? n : 1;
 }
 
 int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *y,
-                   const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st) {
+                   const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st,
+                   bool primaries_only) {
   const moonep_config &c = ctx->cfg;
   Args a;
   a.y = reinterpret_cast<const uint4 *>(y);
@@ -183,11 +193,11 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
   const int grid = ctx->sms * ctx->blocks_combine;
   cudaError_t e;
   switch (c.K) {
-    case 1: e = launch<1, 4, 256, 1>(a, grid, st); break;
-    case 2: e = launch<2, 8, 128, 2>(a, grid, st); break;
-    case 4: e = launch<4, 4, 256, 4>(a, grid, st); break;
-    case 8: e = launch<8, 4, 128, 4>(a, grid, st); break;
-    default: e = launch<0, 2, 256, 1>(a, grid, st); break;
+    case 1: e = launch<1, 4, 256, 1>(a, primaries_only, grid, st); break;
+    case 2: e = launch<2, 8, 128, 2>(a, primaries_only, grid, st); break;
+    case 4: e = launch<4, 4, 256, 4>(a, primaries_only, grid, st); break;
+    case 8: e = launch<8, 4, 128, 4>(a, primaries_only, grid, st); break;
+    default: e = launch<0, 2, 256, 1>(a, primaries_only, grid, st); break;
   }
   return cuda_status(e);
 }

@@ -36,6 +36,7 @@ struct Args {
   int64_t ntok;       // R*S
   int64_t total_rows; // R*NvS
   int K, H8, nchunk, NvS, nseg, EB;
+  int primaries_only;  // rows of duplicate routes are left for the expand epilogue
 };
 
 template <int KT>
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
           set_status(a.status, MOONEP_ERR_PLAN);
         }
         if (c == 0 && g >= 0 && a.w_out) a.w_out[g] = __ldg(a.w_sk + t * K + lane);
+        if (a.primaries_only && d_cur < 0) g = -1;
       }
       const uint4 *src = a.hidden + t * a.H8;
       const int v0 = c * kChunk + lane;
@@ -146,7 +148,8 @@ int occupancy_dispatch(int K) {
 }
 
 int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *hidden,
-                    const float *w_sk, uint16_t *out, float *w_out, cudaStream_t st) {
+                    const float *w_sk, uint16_t *out, float *w_out, cudaStream_t st,
+                    bool primaries_only) {
   const moonep_config &c = ctx->cfg;
   PlanLayout lay = PlanLayout::make(c.R, c.E, c.B, ctx->NvS,
                                     (plan->flags & MOONEP_PLAN_DUP_RECORDS) != 0);
@@ -168,6 +171,7 @@ int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_
   a.NvS = ctx->NvS;
   a.nseg = c.R * ctx->EB;
   a.EB = ctx->EB;
+  a.primaries_only = primaries_only ? 1 : 0;
   if (a.H8 == 0) return MOONEP_OK;
   const int grid = ctx->sms * ctx->blocks_dispatch;
   cudaError_t e;

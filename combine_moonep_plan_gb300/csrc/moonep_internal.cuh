@@ -95,7 +95,8 @@ struct moonep_ctx {
   float *d_weight_view;     // optional [R*NvS] fp32
   unsigned long long *d_sync;  // [2] planner counters: arrivals, tile blocks done
   int test_planner_timeout;    // test hook: the planner's arrival wait never completes
-  int blocks_dispatch, blocks_combine, blocks_copy, blocks_reduce;  // resident blocks per SM
+  int blocks_dispatch, blocks_combine, blocks_copy, blocks_reduce, blocks_expand,
+      blocks_fold;  // resident blocks per SM
 };
 
 namespace moonep {
@@ -109,9 +110,16 @@ int cuda_status(cudaError_t e);
 int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
                 moonep_comm_plan *plan, cudaStream_t st);
 int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *hidden,
-                    const float *w_sk, uint16_t *out, float *w_out, cudaStream_t st);
+                    const float *w_sk, uint16_t *out, float *w_out, cudaStream_t st,
+                    bool primaries_only = false);
 int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *y,
-                   const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st);
+                   const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st,
+                   bool primaries_only = false);
+// The deduplicated data flow's local steps: copy every primary row to its
+// duplicates (dispatch epilogue), or fold every rank's duplicate rows of a
+// token into its primary row (combine prologue).
+int launch_expand(moonep_ctx *ctx, const moonep_comm_plan *plan, uint16_t *rows, cudaStream_t st);
+int launch_fold(moonep_ctx *ctx, const moonep_comm_plan *plan, uint16_t *rows, cudaStream_t st);
 int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n, void *const *T,
                     const int64_t *row_bytes, cudaStream_t st);
 int launch_prepare(moonep_ctx *ctx, const int32_t *num_tokens, uint16_t *hidden,
@@ -133,6 +141,7 @@ int occupancy_dispatch(int K);
 int occupancy_combine(int K);
 int occupancy_copy();
 int occupancy_reduce();
+int occupancy_dedup(bool fold);
 
 // Programmatic dependent launch: every kernel of the library is launched
 // with launch_pdl, so it may be scheduled while the kernel before it on the

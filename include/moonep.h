@@ -228,6 +228,33 @@ int moonep_combine(moonep_ctx *ctx, const moonep_comm_plan *plan,
                    const uint16_t *y_nvsh, const float *w_nvs,
                    uint16_t *out_sh, float *w_sk_out, void *stream);
 
+/* Deduplicated dispatch [API, Buffer.dispatch: a token routed to several
+ * experts on one rank is transferred once and expanded locally in an
+ * epilogue].  Same arguments and results as moonep_dispatch, bit for bit,
+ * in two launches: the copy writes the primary rows (dst >= 0) and every
+ * route weight, then the expand epilogue copies each primary row to the
+ * duplicate rows that plan->dup_groups / dup_loffs list for it.  Requires a
+ * plan created with MOONEP_PLAN_DUP_RECORDS (else MOONEP_ERR_INVALID_ARG).
+ * A record that points outside its rank sets MOONEP_ERR_PLAN in the status
+ * word and is skipped. */
+int moonep_dispatch_dedup(moonep_ctx *ctx, const moonep_comm_plan *plan,
+                          const uint16_t *hidden, const float *w_sk,
+                          uint16_t *hidden_nvsh, float *w_nvs, void *stream);
+
+/* Deduplicated combine [API, Buffer.combine: duplicate rows are accumulated
+ * into their primaries in fp32 before the gather].  Two launches:
+ *   1. fold prologue, IN PLACE on y_nvsh: for every group of rank j,
+ *      y[primary] = bf16_rne(fp32 y[primary] + y[dup_1] + ... ) in k order;
+ *      the duplicate rows are left as they were;
+ *   2. out[r,s,:] = bf16_rne(fp32 sum, in k order, over the token's primary
+ *      routes only (dst >= 0; route 0 always is)); w_sk_out as moonep_combine.
+ * The result can differ from moonep_combine by the fold's extra rounding
+ * (at most 2^-7 * sum |y| per element).  Requires MOONEP_PLAN_DUP_RECORDS.
+ * y_nvsh is written: a second call on the same buffer folds twice. */
+int moonep_combine_dedup(moonep_ctx *ctx, const moonep_comm_plan *plan,
+                         uint16_t *y_nvsh, const float *w_nvs,
+                         uint16_t *out_sh, float *w_sk_out, void *stream);
+
 /* Redundant-expert weight prefetch [API, Buffer.prefetch_weight; README,
  * Weight buffer].  W[p] (p < n_proj <= 4) is a device pointer to one
  * [E + R*B, HHp] bf16 tensor: rows [0, E) are the experts, rows E + j*B + b

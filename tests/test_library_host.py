@@ -71,6 +71,8 @@ def test_null_arguments_rejected(lib):
     assert lib.moonep_plan(None, None, None, None, None) == ERR_INVALID_ARG
     assert lib.moonep_dispatch(None, None, None, None, None, None, None) == ERR_INVALID_ARG
     assert lib.moonep_combine(None, None, None, None, None, None, None) == ERR_INVALID_ARG
+    assert lib.moonep_dispatch_dedup(None, None, None, None, None, None, None) == ERR_INVALID_ARG
+    assert lib.moonep_combine_dedup(None, None, None, None, None, None, None) == ERR_INVALID_ARG
     assert lib.moonep_ctx_destroy(None) == 0          # idempotent on NULL
     assert lib.moonep_hidden_view(None, 0) is None
     assert lib.moonep_plan_destroy(None) == 0
