@@ -63,7 +63,8 @@ def parse():
     ap.add_argument("--hp", type=int, default=None, help="override H' (profiling case)")
     ap.add_argument("--s", type=int, default=None, help="override S (profiling case)")
     ap.add_argument("--profile-op", default=None,
-                    help="comma list of ops (plan,dispatch,combine,prefetch,reduce): "
+                    help="comma list of ops (plan,dispatch,combine,prefetch,reduce,"
+                         "dispatch_dedup,combine_dedup): "
                          "allocate only what they need and run each --steps times "
                          "(a small, self-contained case for profilers; prints timings)")
     args = ap.parse_args()
@@ -693,13 +694,14 @@ def profile_ops(args, sh, point, seed):
     ops = args.profile_op.split(",")
     R, S, K, E, H, B, Hp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.Hp
     topk_np, info = make_routing(sh, point, seed)
+    dedup = any(o.endswith("_dedup") for o in ops)
     buf = Buffer(S=S, H=H, K=K, E=E, num_ep_ranks=R, B=B, token_padding=sh.tp,
-                 zero_copy_views=False)
+                 zero_copy_views=False, dup_records=dedup)
     dev = "cuda"
     topk = torch.from_numpy(topk_np).to(dev)
     plan = buf.plan(topk)
     t = {}
-    if {"dispatch", "combine"} & set(ops):
+    if {"dispatch", "combine", "dispatch_dedup", "combine_dedup"} & set(ops):
         t["x"] = torch.randn((R, S, H), device=dev).to(torch.bfloat16)
         t["w"] = torch.from_numpy(wl.route_weights(sh, seed)).to(dev)
         t["y"] = torch.empty((R * buf.NvS, H), dtype=torch.bfloat16, device=dev)
@@ -717,6 +719,10 @@ def profile_ops(args, sh, point, seed):
                                             weights_out=t["wn"]),
            "combine": lambda: buf.combine(plan, t["y"], t["wn"], out=t["out"],
                                           weights_out=t["wb"]),
+           "dispatch_dedup": lambda: buf.dispatch(t["x"], t["w"], plan=plan, out=t["y"],
+                                                  weights_out=t["wn"], dedup=True),
+           "combine_dedup": lambda: buf.combine(plan, t["y"], t["wn"], out=t["out"],
+                                                weights_out=t["wb"], dedup=True),
            "prefetch": lambda: buf.prefetch_weight(plan, t["W"]),
            "reduce": lambda: buf.reduce_grad(plan, [t["Gh"]], [t["Gs"]])}
     res = {}

@@ -14,8 +14,9 @@
 // Units of (group, chunk of a row) are strided over the warps of a persistent
 // grid; the global group index is mapped to its rank through a per-warp prefix
 // over dup_counts[j][1].  Expand reads the primary chunk once and stores it to
-// every duplicate row; fold loads the primary and up to four duplicate chunks
-// per batch, adds them in k order in fp32 and stores one bf16 RNE result.
+// every duplicate row; fold loads the primary with the first two duplicate
+// chunks (then two at a time), adds them in k order in fp32 and stores one
+// bf16 RNE result.
 // HBM bytes per call (D duplicate routes, Gr groups, row = H*2 bytes):
 // expand reads Gr rows and writes D rows; fold reads Gr + D rows and writes Gr.
 #include "copy_common.cuh"
@@ -25,10 +26,10 @@ namespace moonep {
 namespace {
 
 constexpr int kExpandThreads = 256;
-constexpr int kFoldThreads = 128;  // about 160 registers a thread: small blocks pack better
+constexpr int kFoldThreads = 128;
 constexpr int kExpandU = 8;  // 16-byte vectors per lane per unit (4 KB)
 constexpr int kFoldU = 4;    // 2 KB per row per unit
-constexpr int kFoldBatch = 4;
+constexpr int kFoldBatch = 2;
 
 struct Args {
   uint4 *rows;                // [R*NvS, H8]
@@ -107,7 +108,8 @@ __device__ __forceinline__ bool load_group(const Args &a, int j, int i, Group &g
 }
 
 template <bool FOLD>
-__global__ void __launch_bounds__(FOLD ? kFoldThreads : kExpandThreads) dedup_kernel(Args a) {
+__global__ void __launch_bounds__(FOLD ? kFoldThreads : kExpandThreads, FOLD ? 4 : 3)
+dedup_kernel(Args a) {
   constexpr int kThreads = FOLD ? kFoldThreads : kExpandThreads;
   pdl_wait();
   pdl_launch_dependents();
@@ -126,17 +128,29 @@ __global__ void __launch_bounds__(FOLD ? kFoldThreads : kExpandThreads) dedup_ke
   const int p1 = warp_scan_incl(c1) + __shfl_sync(0xffffffffu, p0, 31);
   const int total = __shfl_sync(0xffffffffu, p1, 31);
   const int64_t units = (int64_t)total * a.nchunk;
-  for (int64_t u = wid; u < units; u += nw) {
+  // Each warp takes a contiguous run of units, so consecutive units share a
+  // group and its record (three dependent loads) is read once per group, not
+  // once per chunk.
+  const int64_t per = (units + nw - 1) / nw;
+  const int64_t ub = wid * per;
+  const int64_t ue = ub + per < units ? ub + per : units;
+  int cur = -1;
+  bool ok = false;
+  Group g;
+  for (int64_t u = ub; u < ue; u++) {
     const int gi = (int)(u / a.nchunk);
     const int c = (int)(u - (int64_t)gi * a.nchunk);
-    // rank of group gi = number of ranks whose inclusive prefix is <= gi
-    const int j = __popc(__ballot_sync(0xffffffffu, p0 <= gi)) +
-                  __popc(__ballot_sync(0xffffffffu, p1 <= gi));
-    const int jm = (j - 1) & 31;
-    const int e0 = __shfl_sync(0xffffffffu, p0, jm), e1 = __shfl_sync(0xffffffffu, p1, jm);
-    const int excl = j == 0 ? 0 : (j - 1 < 32 ? e0 : e1);
-    Group g;
-    if (!load_group(a, j, gi - excl, g)) continue;
+    if (gi != cur) {
+      cur = gi;
+      // rank of group gi = number of ranks whose inclusive prefix is <= gi
+      const int j = __popc(__ballot_sync(0xffffffffu, p0 <= gi)) +
+                    __popc(__ballot_sync(0xffffffffu, p1 <= gi));
+      const int jm = (j - 1) & 31;
+      const int e0 = __shfl_sync(0xffffffffu, p0, jm), e1 = __shfl_sync(0xffffffffu, p1, jm);
+      const int excl = j == 0 ? 0 : (j - 1 < 32 ? e0 : e1);
+      ok = load_group(a, j, gi - excl, g);
+    }
+    if (!ok) continue;
     const uint4 *prow = a.rows + (g.base + g.prim) * a.H8;
     if (!FOLD) {
       const int v0 = c * 32 * kExpandU + lane;
@@ -155,17 +169,19 @@ __global__ void __launch_bounds__(FOLD ? kFoldThreads : kExpandThreads) dedup_ke
         }
       }
     } else {
+      // primary and the first two duplicates are loaded together (most
+      // groups have one or two), later duplicates two at a time; the adds
+      // run in k order
       const int v0 = c * 32 * kFoldU + lane;
       float acc[kFoldU][8];
-      uint4 x[kFoldU];
-#pragma unroll
-      for (int i = 0; i < kFoldU; i++) {
-        const int v = v0 + 32 * i;
-        x[i] = make_uint4(0, 0, 0, 0);
-        if (v < a.H8) x[i] = ld_stream(prow + v);
-      }
       for (int k0 = 0; k0 < g.cnt; k0 += kFoldBatch) {
-        uint4 y[kFoldBatch][kFoldU];
+        uint4 x[kFoldU], y[kFoldBatch][kFoldU];
+#pragma unroll
+        for (int i = 0; i < kFoldU; i++) {
+          const int v = v0 + 32 * i;
+          x[i] = make_uint4(0, 0, 0, 0);
+          if (k0 == 0 && v < a.H8) x[i] = ld_stream(prow + v);
+        }
 #pragma unroll
         for (int kk = 0; kk < kFoldBatch; kk++) {
           const int dr = __shfl_sync(0xffffffffu, g.dup, (k0 + kk) & 31);

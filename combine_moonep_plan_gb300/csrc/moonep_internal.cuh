@@ -48,10 +48,14 @@ inline size_t bal_tables_words(int R, int E, int B) {
 }
 
 // Layout of plan->internal (int32 words after the meta words).
+// Rows of a rank handled by one block of the duplicate-record builder.
+constexpr int kDupTile = 1024;
+inline int dup_tiles_per_rank(int NvS) { return (NvS + kDupTile - 1) / kDupTile; }
+
 struct PlanLayout {
   int64_t qoff, home_rowbase, keep, piece_first, piece_count, piece_start, piece_len,
       piece_recv, slot_rowbase, bal, pad_prefix, copy_slot, copy_expert, red_expert, red_first,
-      red_slot, dupflag, total;
+      red_slot, dupflag, dup_tiles, total;
   static PlanLayout make(int R, int E, int B, int NvS, bool dup_records) {
     PlanLayout l;
     const int L = E / R, EB = E + B;
@@ -74,6 +78,8 @@ struct PlanLayout {
     l.red_first = take(E + 1);
     l.red_slot = take((int64_t)R * B);
     l.dupflag = dup_records ? take((int64_t)R * NvS) : -1;
+    // per rank and tile of kDupTile rows: {groups, duplicate routes}
+    l.dup_tiles = dup_records ? take((int64_t)R * dup_tiles_per_rank(NvS) * 2) : -1;
     l.total = o;
     return l;
   }

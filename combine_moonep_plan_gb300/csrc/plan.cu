@@ -1052,70 +1052,117 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
 
 // ------------------------------------------------------------------ K4
 
-constexpr int kDupThreads = 1024;
+constexpr int kDupThreads = kDupTile;
 
-__global__ void __launch_bounds__(kDupThreads)
-plan_dup_kernel(PlanDims d, const int32_t *__restrict__ dst, const int32_t *__restrict__ dupflag,
-                int32_t *__restrict__ dup_groups, int32_t *__restrict__ dup_loffs) {
+// The group of row w of rank j: has = 1 when w is a primary row with
+// duplicates on its rank (dupflag names its route), cnt = their number.
+__device__ __forceinline__ void dup_row(const PlanDims &d, const int32_t *__restrict__ dst,
+                                        const int32_t *__restrict__ dupflag, int j, int w,
+                                        int &has, int &cnt, int64_t &tb, int &k) {
+  has = cnt = 0;
+  tb = 0;
+  k = 0;
+  if (w >= d.NvS) return;
+  const int rid = dupflag[(int64_t)j * d.NvS + w] - 1;
+  if (rid < 0) return;
+  k = rid % d.K;
+  tb = rid - k;
+  for (int k2 = k + 1; k2 < d.K; k2++) {
+    const int v = dst[tb + k2];
+    const int64_t g = v >= 0 ? v : -(int64_t)v - 1;
+    if (g / d.NvS == j) cnt++;
+  }
+  has = 1;
+}
+
+// Block-wide exclusive scan of two counters (1024 threads); returns the
+// totals through tot.
+__device__ __forceinline__ void dup_block_scan(int has, int cnt, int &hx, int &cx, int (&tot)[2]) {
   __shared__ int wsum[2][32];
-  __shared__ int carry[2];
-  const int j = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t rowbase = (int64_t)j * d.NvS;
-  if (tid == 0) carry[0] = carry[1] = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hi = warp_incl_scan(has), ci = warp_incl_scan(cnt);
+  if (lane == 31) {
+    wsum[0][warp] = hi;
+    wsum[1][warp] = ci;
+  }
   __syncthreads();
-  for (int w0 = 0; w0 < d.NvS; w0 += kDupThreads) {
-    const int w = w0 + tid;
-    int has = 0, cnt = 0, rid = -1;
-    if (w < d.NvS) {
-      rid = dupflag[rowbase + w] - 1;
-      if (rid >= 0) {
-        const int k = rid % d.K;
-        const int64_t tb = rid - k;
-        for (int k2 = k + 1; k2 < d.K; k2++) {
-          const int v = dst[tb + k2];
-          const int64_t g = v >= 0 ? v : -(int64_t)v - 1;
-          if (g / d.NvS == j) cnt++;
-        }
-        has = 1;
-      }
-    }
-    // block exclusive scans of has and cnt
-    int hi = warp_incl_scan(has), ci = warp_incl_scan(cnt);
-    if (lane == 31) {
-      wsum[0][warp] = hi;
-      wsum[1][warp] = ci;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int a = warp_incl_scan(wsum[0][lane]);
-      const int b = warp_incl_scan(wsum[1][lane]);
-      wsum[0][lane] = a;
-      wsum[1][lane] = b;
-    }
-    __syncthreads();
-    const int gi = carry[0] + (warp ? wsum[0][warp - 1] : 0) + hi - has;
-    const int di = carry[1] + (warp ? wsum[1][warp - 1] : 0) + ci - cnt;
-    if (has) {
-      int32_t *rec = dup_groups + (rowbase + gi) * 3;
-      rec[0] = w;
-      rec[1] = di;
-      rec[2] = cnt;
-      const int k = rid % d.K;
-      const int64_t tb = rid - k;
-      int c = 0;
-      for (int k2 = k + 1; k2 < d.K; k2++) {
-        const int v = dst[tb + k2];
-        const int64_t g = v >= 0 ? v : -(int64_t)v - 1;
-        if (g / d.NvS == j) dup_loffs[rowbase + di + c++] = (int)(g - rowbase);
-      }
-    }
-    __syncthreads();
-    if (tid == 0) {
-      carry[0] += wsum[0][31];
-      carry[1] += wsum[1][31];
-    }
-    __syncthreads();
+  if (warp == 0) {
+    wsum[0][lane] = warp_incl_scan(wsum[0][lane]);
+    wsum[1][lane] = warp_incl_scan(wsum[1][lane]);
+  }
+  __syncthreads();
+  hx = (warp ? wsum[0][warp - 1] : 0) + hi - has;
+  cx = (warp ? wsum[1][warp - 1] : 0) + ci - cnt;
+  tot[0] = wsum[0][31];
+  tot[1] = wsum[1][31];
+}
+
+// Pass 1: per (tile, rank) block, the tile's group and duplicate counts.
+__global__ void __launch_bounds__(kDupThreads)
+plan_dup_count_kernel(PlanDims d, const int32_t *__restrict__ dst,
+                      const int32_t *__restrict__ dupflag, int32_t *__restrict__ tiles) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x, j = blockIdx.y, T = gridDim.x;
+  int has, cnt, k;
+  int64_t tb;
+  dup_row(d, dst, dupflag, j, t * kDupTile + threadIdx.x, has, cnt, tb, k);
+  int hx, cx, tot[2];
+  dup_block_scan(has, cnt, hx, cx, tot);
+  if (threadIdx.x == 0) {
+    tiles[((int64_t)j * T + t) * 2] = tot[0];
+    tiles[((int64_t)j * T + t) * 2 + 1] = tot[1];
+  }
+}
+
+// Pass 2: every block adds up the counts of the rank's earlier tiles, then
+// writes its groups (ascending primary row) and their duplicate rows (k order).
+__global__ void __launch_bounds__(kDupThreads)
+plan_dup_write_kernel(PlanDims d, const int32_t *__restrict__ dst,
+                      const int32_t *__restrict__ dupflag, const int32_t *__restrict__ tiles,
+                      int32_t *__restrict__ dup_groups, int32_t *__restrict__ dup_loffs) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ int base[2][32];
+  const int t = blockIdx.x, j = blockIdx.y, T = gridDim.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int sg = 0, sd = 0;
+  for (int i = tid; i < t; i += kDupThreads) {
+    sg += tiles[((int64_t)j * T + i) * 2];
+    sd += tiles[((int64_t)j * T + i) * 2 + 1];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sg += __shfl_xor_sync(0xffffffffu, sg, o);
+    sd += __shfl_xor_sync(0xffffffffu, sd, o);
+  }
+  if (lane == 0) {
+    base[0][warp] = sg;
+    base[1][warp] = sd;
+  }
+  const int w = t * kDupTile + tid;
+  int has, cnt, k;
+  int64_t tb;
+  dup_row(d, dst, dupflag, j, w, has, cnt, tb, k);
+  int hx, cx, tot[2];
+  dup_block_scan(has, cnt, hx, cx, tot);  // its barriers also publish base[][]
+  int g0 = 0, d0 = 0;
+  for (int i = 0; i < kDupThreads / 32; i++) {
+    g0 += base[0][i];
+    d0 += base[1][i];
+  }
+  if (!has) return;
+  const int64_t rowbase = (int64_t)j * d.NvS;
+  const int gi = g0 + hx, di = d0 + cx;
+  int32_t *rec = dup_groups + (rowbase + gi) * 3;
+  rec[0] = w;
+  rec[1] = di;
+  rec[2] = cnt;
+  int c = 0;
+  for (int k2 = k + 1; k2 < d.K; k2++) {
+    const int v = dst[tb + k2];
+    const int64_t g = v >= 0 ? v : -(int64_t)v - 1;
+    if (g / d.NvS == j) dup_loffs[rowbase + di + c++] = (int)(g - rowbase);
   }
 }
 
@@ -1285,9 +1332,17 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
 #undef MOONEP_ASSIGN
     }
   }
-  if (dup)
-    plan_dup_kernel<<<d.R, kDupThreads, 0, st>>>(d, plan->dst, in + lay.dupflag,
-                                                 plan->dup_groups, plan->dup_loffs);
+  if (dup && d.NvS > 0) {
+    const dim3 grid(dup_tiles_per_rank(d.NvS), d.R);
+    cudaError_t e2 = launch_pdl(plan_dup_count_kernel, grid, kDupThreads, 0, st, false, d,
+                                (const int32_t *)plan->dst, (const int32_t *)(in + lay.dupflag),
+                                in + lay.dup_tiles);
+    if (e2 == cudaSuccess)
+      e2 = launch_pdl(plan_dup_write_kernel, grid, kDupThreads, 0, st, false, d,
+                      (const int32_t *)plan->dst, (const int32_t *)(in + lay.dupflag),
+                      (const int32_t *)(in + lay.dup_tiles), plan->dup_groups, plan->dup_loffs);
+    if (e2 != cudaSuccess) return cuda_status(e2);
+  }
   return cuda_status(cudaGetLastError());
 }
 
