@@ -11,9 +11,9 @@
 // the rank-local rows of its duplicates (in k order) -- the work lists of both
 // steps.
 //
-// Units of (group, chunk of a row) are strided over the warps of a persistent
-// grid; the global group index is mapped to its rank through a per-warp prefix
-// over dup_counts[j][1].  Expand reads the primary chunk once and stores it to
+// Units of (group, chunk of a row) are split into one contiguous run per warp
+// of a persistent grid; the global group index is mapped to its rank through a
+// per-warp prefix over dup_counts[j][1].  Expand reads the primary chunk once and stores it to
 // every duplicate row; fold loads the primary with the first two duplicate
 // chunks (then two at a time), adds them in k order in fp32 and stores one
 // bf16 RNE result.

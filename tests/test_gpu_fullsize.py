@@ -200,3 +200,69 @@ def test_full_size_mxfp4_prefetch(name, point):
         del t
     del ts
     buf.destroy()
+
+
+def test_full_size_three_projections():
+    """The gate/up/down case at the DeepSeek-V3 shape's full size (three bf16
+    [E + R*B, H, H'] weight tensors, 15 GB each, in one prefetch call; three
+    projections of fp32 gradients in one reduce call): every used slot equals
+    its home row, unused slots keep their contents, and the reduce matches the
+    oracle on sampled column windows of every projection."""
+    from combine_moonep_plan_gb300.api import Buffer
+    sh = wl.SHAPES["deepseek_v3"]
+    R, E, B, H, Hp = sh.R, sh.E, sh.B, sh.H, sh.Hp
+    seed = wl.seed_for("deepseek_v3", 13)
+    topk = _routing(sh, 2.0, seed)
+    st, op = oracle.plan(R, E, sh.K, sh.S, B, sh.tp, topk, wl.tokens_per_expert(topk, E),
+                         dup_records=False)
+    assert st == 0
+    etc = op["experts_to_copy"]
+    buf = Buffer(S=sh.S, H=H, K=sh.K, E=E, num_ep_ranks=R, B=B, token_padding=sh.tp,
+                 zero_copy_views=False)
+    plan = buf.plan(torch.from_numpy(topk).cuda())
+    rows = E + R * B
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    Ws = []
+    for _ in range(3):
+        w = torch.empty((rows, H, Hp), dtype=torch.bfloat16, device="cuda")
+        w.normal_(generator=g)
+        Ws.append(w)
+    unused = [E + j * B + b for j in range(R) for b in range(B) if etc[j, b] < 0]
+    ui = torch.tensor(unused, dtype=torch.int64, device="cuda")
+
+    def unused_sums(w):
+        w32 = w.view(rows, -1).view(torch.int32)
+        return torch.stack([w32[i].to(torch.int64).sum() for i in unused]).cpu() \
+            if unused else torch.zeros(0, dtype=torch.int64)
+    before = [unused_sums(w) for w in Ws]
+    buf.prefetch_weight(plan, *Ws)
+    assert buf.get_status() == 0
+    for w, b0 in zip(Ws, before):
+        for j in range(R):
+            for b in range(B):
+                if etc[j, b] >= 0:
+                    assert torch.equal(w[E + j * B + b].view(torch.int16),
+                                       w[etc[j, b]].view(torch.int16))
+        assert torch.equal(unused_sums(w), b0)
+    del Ws, ui
+    torch.cuda.empty_cache()
+
+    HHp = H * Hp
+    Gh = [torch.empty((E, H, Hp), device="cuda").normal_(generator=g) for _ in range(3)]
+    Gs = [torch.empty((R, B, H, Hp), device="cuda").normal_(generator=g) for _ in range(3)]
+    wins = [(0, 2048), (HHp // 3, HHp // 3 + 2048), (HHp - 2048, HHp)]
+    gh0 = [[t.view(E, -1)[:, a:b].cpu().numpy().copy() for a, b in wins] for t in Gh]
+    gs0 = [[t.view(R * B, -1)[:, a:b].cpu().numpy().copy() for a, b in wins] for t in Gs]
+    buf.reduce_grad(plan, Gh, Gs)
+    assert buf.get_status() == 0
+    for p in range(3):
+        for (a, b), gh, gs in zip(wins, gh0[p], gs0[p]):
+            oracle.reduce(R, E, B, etc.reshape(-1), gh, gs, b - a)
+            assert np.array_equal(Gh[p].view(E, -1)[:, a:b].cpu().numpy().view(np.uint32),
+                                  gh.view(np.uint32))
+            assert np.array_equal(Gs[p].view(R * B, -1)[:, a:b].cpu().numpy().view(np.uint32),
+                                  gs.view(np.uint32))
+    del Gh, Gs
+    buf.destroy()
+    torch.cuda.empty_cache()
