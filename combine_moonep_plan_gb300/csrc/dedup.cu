@@ -13,10 +13,10 @@
 //
 // Units of (group, chunk of a row) are split into one contiguous run per warp
 // of a persistent grid; the global group index is mapped to its rank through a
-// per-warp prefix over dup_counts[j][1].  Expand reads the primary chunk once and stores it to
-// every duplicate row; fold loads the primary with the first two duplicate
-// chunks (then two at a time), adds them in k order in fp32 and stores one
-// bf16 RNE result.
+// per-warp prefix over dup_counts[j][1].  Expand reads the primary chunk once
+// and stores it to every duplicate row; fold loads the primary with the first
+// two duplicate chunks (then two at a time), adds them in k order in fp32 and
+// stores one bf16 RNE result.
 // HBM bytes per call (D duplicate routes, Gr groups, row = H*2 bytes):
 // expand reads Gr rows and writes D rows; fold reads Gr + D rows and writes Gr.
 #include "copy_common.cuh"
