@@ -9,8 +9,9 @@
 // On one GPU every destination row is local HBM, so duplicates are expanded by
 // writing the row to every |dst| directly: each source row is read once and
 // written K times.  The work is cut into units of (token, 4 KB chunk of its
-// row) followed by whole padding rows, strided over every warp of a
-// persistent grid, so the tail is balanced whatever the token count.
+// row; 2 KB when the batch is too small to occupy every warp) followed by
+// whole padding rows, strided over every warp of a persistent grid, so the
+// tail is balanced whatever the token count.
 // HBM bytes per call: read R*S*H*2 + N*8 (dst, weights); write
 // (N + P)*(H*2 + 4), P = padding rows.
 #include "copy_common.cuh"
@@ -20,8 +21,6 @@ namespace moonep {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kU = 8;                  // 16-byte vectors per lane per unit
-constexpr int kChunk = 32 * kU;        // vectors per unit (4 KB)
 
 struct Args {
   const uint4 *hidden;
@@ -39,8 +38,11 @@ struct Args {
   int primaries_only;  // rows of duplicate routes are left for the expand epilogue
 };
 
-template <int KT>
+// kU: 16-byte vectors per lane per unit (8: 4 KB units; 4: 2 KB units for
+// batches too small to give every warp of the grid a 4 KB unit).
+template <int KT, int kU>
 __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
+  constexpr int kChunk = 32 * kU;  // vectors per unit
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
@@ -134,7 +136,13 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a) {
 
 template <int KT>
 void *kernel_ptr() {
-  return (void *)dispatch_kernel<KT>;
+  return (void *)dispatch_kernel<KT, 8>;
+}
+
+template <int KT>
+cudaError_t launch(const Args &a, int u, int grid, cudaStream_t st) {
+  return u == 4 ? launch_pdl(dispatch_kernel<KT, 4>, grid, kThreads, 0, st, false, a)
+                : launch_pdl(dispatch_kernel<KT, 8>, grid, kThreads, 0, st, false, a);
 }
 
 }  // namespace
@@ -167,20 +175,25 @@ int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_
   a.total_rows = (int64_t)c.R * ctx->NvS;
   a.K = c.K;
   a.H8 = c.H / 8;
-  a.nchunk = (a.H8 + kChunk - 1) / kChunk;
+  const int grid = ctx->sms * ctx->blocks_dispatch;
+  // 2 KB units when 4 KB units would leave warps of the grid idle (decode-
+  // sized batches: 16.7 us instead of 21.5 us at 1024 tokens of 8 KB; at
+  // large batches 4 KB units are 2 % faster)
+  const int64_t warps = (int64_t)grid * (kThreads / 32);
+  const int u = (int64_t)c.R * c.S * ((a.H8 + 255) / 256) < warps ? 4 : 8;
+  a.nchunk = (a.H8 + 32 * u - 1) / (32 * u);
   a.NvS = ctx->NvS;
   a.nseg = c.R * ctx->EB;
   a.EB = ctx->EB;
   a.primaries_only = primaries_only ? 1 : 0;
   if (a.H8 == 0) return MOONEP_OK;
-  const int grid = ctx->sms * ctx->blocks_dispatch;
   cudaError_t e;
   switch (c.K) {
-    case 1: e = launch_pdl(dispatch_kernel<1>, grid, kThreads, 0, st, false, a); break;
-    case 2: e = launch_pdl(dispatch_kernel<2>, grid, kThreads, 0, st, false, a); break;
-    case 4: e = launch_pdl(dispatch_kernel<4>, grid, kThreads, 0, st, false, a); break;
-    case 8: e = launch_pdl(dispatch_kernel<8>, grid, kThreads, 0, st, false, a); break;
-    default: e = launch_pdl(dispatch_kernel<0>, grid, kThreads, 0, st, false, a); break;
+    case 1: e = launch<1>(a, u, grid, st); break;
+    case 2: e = launch<2>(a, u, grid, st); break;
+    case 4: e = launch<4>(a, u, grid, st); break;
+    case 8: e = launch<8>(a, u, grid, st); break;
+    default: e = launch<0>(a, u, grid, st); break;
   }
   return cuda_status(e);
 }

@@ -36,8 +36,10 @@
 //                          the copy / reduce lists.
 //   K3 plan_assign_kernel  one thread per token: Q position -> (rank, row),
 //                          duplicate encoding, dup_counts.
-//   K4 plan_dup_kernel     (optional, either path) one CTA per rank: compact
-//                          duplicate records in ascending primary row.
+//   K4 plan_dup_count_kernel, plan_dup_write_kernel (optional, either path)
+//                          one CTA per (1024-row tile, rank): the tile's group
+//                          and duplicate counts, then compact duplicate
+//                          records in ascending primary row.
 #include "moonep_internal.cuh"
 
 namespace moonep {
