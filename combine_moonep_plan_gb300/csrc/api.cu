@@ -267,7 +267,7 @@ int moonep_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_
   if ((st = check_plan(ctx, plan))) return st;
   const int64_t ntok = (int64_t)ctx->cfg.R * ctx->cfg.S;
   if (!hidden_nvsh || (ntok > 0 && !hidden)) return MOONEP_ERR_INVALID_ARG;
-  if ((w_sk == nullptr) != (w_nvs == nullptr)) return MOONEP_ERR_INVALID_ARG;
+  if (ntok > 0 && (w_sk == nullptr) != (w_nvs == nullptr)) return MOONEP_ERR_INVALID_ARG;
   if (!aligned16(hidden) || !aligned16(hidden_nvsh) || ((uintptr_t)w_sk & 3) ||
       ((uintptr_t)w_nvs & 3))
     return MOONEP_ERR_INVALID_ARG;
@@ -281,7 +281,7 @@ int moonep_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
   if ((st = check_plan(ctx, plan))) return st;
   const int64_t ntok = (int64_t)ctx->cfg.R * ctx->cfg.S;
   if (ntok > 0 && (!y_nvsh || !out_sh)) return MOONEP_ERR_INVALID_ARG;
-  if ((w_nvs == nullptr) != (w_sk_out == nullptr)) return MOONEP_ERR_INVALID_ARG;
+  if (ntok > 0 && (w_nvs == nullptr) != (w_sk_out == nullptr)) return MOONEP_ERR_INVALID_ARG;
   if (!aligned16(y_nvsh) || !aligned16(out_sh) || ((uintptr_t)w_nvs & 3) ||
       ((uintptr_t)w_sk_out & 3))
     return MOONEP_ERR_INVALID_ARG;
@@ -296,7 +296,7 @@ int moonep_dispatch_dedup(moonep_ctx *ctx, const moonep_comm_plan *plan, const u
   if (!(plan->flags & MOONEP_PLAN_DUP_RECORDS)) return MOONEP_ERR_INVALID_ARG;
   const int64_t ntok = (int64_t)ctx->cfg.R * ctx->cfg.S;
   if (!hidden_nvsh || (ntok > 0 && !hidden)) return MOONEP_ERR_INVALID_ARG;
-  if ((w_sk == nullptr) != (w_nvs == nullptr)) return MOONEP_ERR_INVALID_ARG;
+  if (ntok > 0 && (w_sk == nullptr) != (w_nvs == nullptr)) return MOONEP_ERR_INVALID_ARG;
   if (!aligned16(hidden) || !aligned16(hidden_nvsh) || ((uintptr_t)w_sk & 3) ||
       ((uintptr_t)w_nvs & 3))
     return MOONEP_ERR_INVALID_ARG;
@@ -313,7 +313,7 @@ int moonep_combine_dedup(moonep_ctx *ctx, const moonep_comm_plan *plan, uint16_t
   if (!(plan->flags & MOONEP_PLAN_DUP_RECORDS)) return MOONEP_ERR_INVALID_ARG;
   const int64_t ntok = (int64_t)ctx->cfg.R * ctx->cfg.S;
   if (ntok > 0 && (!y_nvsh || !out_sh)) return MOONEP_ERR_INVALID_ARG;
-  if ((w_nvs == nullptr) != (w_sk_out == nullptr)) return MOONEP_ERR_INVALID_ARG;
+  if (ntok > 0 && (w_nvs == nullptr) != (w_sk_out == nullptr)) return MOONEP_ERR_INVALID_ARG;
   if (!aligned16(y_nvsh) || !aligned16(out_sh) || ((uintptr_t)w_nvs & 3) ||
       ((uintptr_t)w_sk_out & 3))
     return MOONEP_ERR_INVALID_ARG;

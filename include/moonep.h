@@ -210,6 +210,9 @@ int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk,
  *   hidden_nvsh [R*NvS, H] bf16 out: row |dst| of every route = its token's
  *               row; padding rows zero; tail rows untouched
  *   w_nvs       [R*NvS] fp32 out, or NULL: route weight per row, 0 on padding
+ *               (w_sk and w_nvs are both given or both NULL, else
+ *               MOONEP_ERR_INVALID_ARG; an empty batch, R*S = 0, takes
+ *               either without complaint)
  * Passing a saved plan again is the plan-reuse path (combine-backward
  * dispatch of an [R, S, H] gradient, weights NULL) [API, Buffer.dispatch:
  * a saved plan skips planning and ignores the routing inputs]. */
@@ -222,7 +225,8 @@ int moonep_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan,
  *   w_nvs    [R*NvS] fp32 or NULL
  *   out_sh   [R, S, H] bf16 out: out[r,s,:] = bf16_rne(fp32 sum over
  *            k = 0..K-1, in k order, of y[|dst(r,s,k)|,:])
- *   w_sk_out [R, S, K] fp32 out or NULL: w_nvs[|dst|] (bit copy)
+ *   w_sk_out [R, S, K] fp32 out or NULL: w_nvs[|dst|] (bit copy); given
+ *            together with w_nvs or not at all (any pair for an empty batch)
  * Reads only rows that dst names (never padding or tail rows). */
 int moonep_combine(moonep_ctx *ctx, const moonep_comm_plan *plan,
                    const uint16_t *y_nvsh, const float *w_nvs,

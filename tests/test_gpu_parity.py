@@ -255,6 +255,14 @@ def test_empty_tokens():
     plan = buf.plan(tk)
     assert buf.get_status() == 0
     assert torch.all(plan.cu_seqlens == 0) and torch.all(plan.experts_to_copy == -1)
+    # every copy call, direct and deduplicated, takes the empty batch
+    x = torch.zeros((2, 0, 16), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((2, 0, 2), dtype=torch.float32, device="cuda")
+    for dedup in (False, True):
+        rows, wn, _, _ = buf.dispatch(x, w, plan=plan, dedup=dedup)
+        out, wb = buf.combine(plan, rows, wn, dedup=dedup)
+        assert out.shape == (2, 0, 16) and wb.shape == (2, 0, 2)
+    assert buf.get_status() == 0
 
 
 # ----------------------------------------------------- plan properties
