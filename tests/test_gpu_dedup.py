@@ -87,9 +87,32 @@ def _buffer(sh, dup=True):
                                                      for c in CASES])
 def test_dedup_parity(name, S, H, kind):
     sh = _shape(name, S, H)
-    R, K, E, B, tp = sh.R, sh.K, sh.E, sh.B, sh.tp
     seed = wl.seed_for(name, 31) + S
-    topk = _routing(sh, kind, seed)
+    _dedup_parity(sh, _routing(sh, kind, seed), seed)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_dedup_random_small_configs(seed):
+    """Random R, E, K (including K outside the specialised set, so the generic
+    combine runs in its primaries-only form), S, B, token_padding and H, with
+    repeated experts inside a token (many duplicates on one rank)."""
+    rng = np.random.default_rng(1000 + seed)
+    R = int(rng.integers(1, 9))
+    L = int(rng.integers(1, 9))
+    E = R * L
+    K = int(rng.choice([2, 3, 4, 5, 8, 12]))
+    S = int(rng.integers(1, 400))
+    B = L + int(rng.integers(0, 3))
+    tp = int(rng.choice([1, 2, 8, 16]))
+    H = int(rng.choice([8, 64, 136, 2056]))
+    sh = wl.Shape("rand", R=R, E=E, K=K, S=S, H=H, Hp=16, B=B, tp=tp, weights="softmax")
+    p = rng.random(E) ** 4
+    topk = rng.choice(E, size=(R, S, K), p=p / p.sum()).astype(np.int32)
+    _dedup_parity(sh, topk, seed)
+
+
+def _dedup_parity(sh, topk, seed):
+    R, S, K, E, B, tp, H = sh.R, sh.S, sh.K, sh.E, sh.B, sh.tp, sh.H
     tpe = wl.tokens_per_expert(topk, E)
     st, op = oracle.plan(R, E, K, S, B, tp, topk, tpe)
     assert st == 0
