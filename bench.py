@@ -233,7 +233,7 @@ class Step:
         return {
             "plan": N * 4 + R * E * 4 + N * 4 + R * (E + B) * 16,
             "dispatch": R * S * H * 2 + N * 8 + (N + P) * (H * 2 + 4),
-            "prefetch": 2 * U * HHp * 2,
+            "prefetch": (D + U) * HHp * 2,  # each expert's row read once, U slot rows written
             "combine": N * H * 2 + N * 8 + R * S * H * 2 + N * 4,
             "grad_dispatch": R * S * H * 2 + N * 4 + (N + P) * H * 2,
             "reduce": (2 * D + 2 * U) * HHp * 4,
@@ -333,8 +333,9 @@ def run_mxfp4_prefetch(buf, step, sh, steps, torch, peak):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    U = step.algorithmic_bytes()[1]["U"]
-    nbytes = 2 * U * 3 * (sh.H * sh.Hp // 2 + sh.H * sh.Hp // 32)
+    cnt = step.algorithmic_bytes()[1]
+    U, D = cnt["U"], cnt["D"]
+    nbytes = (D + U) * 3 * (sh.H * sh.Hp // 2 + sh.H * sh.Hp // 32)
     del ts
     torch.cuda.empty_cache()
     return {"set": "gate/up/down packed MXFP4 [E+R*B, H, H'/2] uint8 + E8M0 block scales "

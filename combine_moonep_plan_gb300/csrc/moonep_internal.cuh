@@ -54,7 +54,7 @@ inline int dup_tiles_per_rank(int NvS) { return (NvS + kDupTile - 1) / kDupTile;
 
 struct PlanLayout {
   int64_t qoff, home_rowbase, keep, piece_first, piece_count, piece_start, piece_len,
-      piece_recv, slot_rowbase, bal, pad_prefix, copy_slot, copy_expert, red_expert, red_first,
+      piece_recv, slot_rowbase, bal, pad_prefix, red_expert, red_first,
       red_slot, dupflag, dup_tiles, total;
   static PlanLayout make(int R, int E, int B, int NvS, bool dup_records) {
     PlanLayout l;
@@ -72,8 +72,6 @@ struct PlanLayout {
     l.slot_rowbase = take((int64_t)R * L);
     l.bal = take((int64_t)bal_tables_words(R, E, B));
     l.pad_prefix = take((int64_t)R * EB + 1);
-    l.copy_slot = take((int64_t)R * B);
-    l.copy_expert = take((int64_t)R * B);
     l.red_expert = take(E);
     l.red_first = take(E + 1);
     l.red_slot = take((int64_t)R * B);

@@ -25,7 +25,7 @@
 //                          each runs the balance step's routing stage on its
 //                          own copy of the per-rank totals and assigns its
 //                          routes; two extra CTAs write the plan's tables
-//                          and the copy / reduce lists.
+//                          and the experts-with-copies list.
 //   The tile path (K not dividing 32, or tables too large for one CTA):
 //   K1 plan_hist_kernel    per 2048-route tile: per-expert counts and each
 //                          route's ordinal among same-expert routes of the tile
@@ -33,7 +33,7 @@
 //   K2 plan_balance_kernel one CTA: column scans of the tile counts (the
 //                          position of every tile inside every P_e), the chain
 //                          balance, slots, segments, cu_seqlens, padding and
-//                          the copy / reduce lists.
+//                          the experts-with-copies list.
 //   K3 plan_assign_kernel  one thread per token: Q position -> (rank, row),
 //                          duplicate encoding, dup_counts.
 //   K4 plan_dup_count_kernel, plan_dup_write_kernel (optional, either path)
@@ -164,7 +164,6 @@ struct BalSmall {
   int keep[kMaxR];        // prefix of Q_j the home rank keeps
   int recv_piece[kMaxR];  // piece (chain order) rank j receives, -1 if none
   int nslots[kMaxR];      // slots rank j uses
-  int slot_off[kMaxR];    // rank j's first entry in the copy list
   int donor[kMaxR], recv[kMaxR], len[kMaxR], start[kMaxR];  // pieces, chain order
   int pf[kMaxR], pc[kMaxR];             // per donor: first entry and count below
   int ps[kMaxR], pl[kMaxR], pr[kMaxR];  // pieces grouped by donor: Q start, length, receiver
@@ -539,9 +538,9 @@ __device__ void balance_tables(const PlanDims &d, const BalTables &t, BalSmall &
   }
 }
 
-// balance_lists: the copy list (every used slot, rank by rank), the reduce
-// list (experts with copies in ascending id, their slots in ascending rank)
-// and the meta word D; D = 0 when the balance failed or `ok` is false.
+// balance_lists: the list the prefetch and the gradient reduce walk (experts
+// with copies in ascending id, their slots in ascending rank) and the meta
+// word D; D = 0 when the balance failed or `ok` is false.
 // Called by one whole block after balance_route.
 __device__ void balance_lists(const PlanDims &d, const BalTables &t, BalSmall &s, int32_t *in,
                               const PlanLayout &lay, bool ok) {
@@ -550,13 +549,6 @@ __device__ void balance_lists(const PlanDims &d, const BalTables &t, BalSmall &s
   if (!ok || s.err != 0) {
     if (tid == 0) in[kMetaD] = 0;
     return;
-  }
-  if (tid == 0) {
-    int u = 0;
-    for (int j = 0; j < R; j++) {
-      s.slot_off[j] = u;
-      u += s.nslots[j];
-    }
   }
   // slot copies per expert (a receiver holds an expert at most once)
   for (int e = tid; e < E; e += kBalThreads) {
@@ -570,13 +562,6 @@ __device__ void balance_lists(const PlanDims &d, const BalTables &t, BalSmall &s
     t.rhas[e] = cnt > 0;
   }
   __syncthreads();
-  for (int i = tid; i < R * B; i += kBalThreads) {
-    const int j = i / B, b = i - j * B;
-    if (b < s.nslots[j]) {
-      in[lay.copy_slot + s.slot_off[j] + b] = i;
-      in[lay.copy_expert + s.slot_off[j] + b] = t.etc[j * Bm + b];
-    }
-  }
   block_scan2(t.rcnt, t.rhas, E, 0, true, s.part);
   const int ncopies = t.rcnt[E], nexperts = t.rhas[E];
   for (int e = tid; e < E; e += kBalThreads) {
@@ -784,7 +769,7 @@ plan_assign_kernel(PlanDims d, const int32_t *__restrict__ topk, const int32_t *
 //      its routes to (rank, row), marks duplicates with warp shuffles inside
 //      each token's K lanes, and writes dst; meanwhile the table block writes
 //      cu_seqlens, zero_fill_ranges, experts_to_copy, remote_stats and the
-//      padding prefix, and the list block the copy and reduce lists;
+//      padding prefix, and the list block the experts-with-copies list;
 //   5. the tile blocks add their duplicate counts straight into the plan
 //      (the table block zeroed them before the meeting); the table block
 //      clears the other set of per-rank totals, which the next call uses.

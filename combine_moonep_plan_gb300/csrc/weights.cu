@@ -12,12 +12,14 @@
 // (rank j's slot b is row E + j*B + b) and the slot gradients are [R*B, HHp].
 // The planner leaves compact lists on the device (used slots; experts with
 // copies and their slots in (rank, slot) order), so both kernels walk only the
-// rows that move.  Work units are 64 KB chunks of a row, strided over a
-// persistent grid.  Reduce reads each slot element once, adds it, and zeroes
-// it in the same thread, so no barrier separates the reduce and the clear.
-// HBM bytes: prefetch 2*U*row_bytes per tensor (row_bytes = H*H'*2 for bf16,
-// H*H'/2 for packed MXFP4, H*H'/32 for its block scales); reduce
-// (2*D + 2*U)*HHp*4.
+// rows that move.  Work units are chunks of an expert's row, strided over a
+// persistent grid: prefetch reads the chunk once and writes it to every slot
+// holding the expert; reduce reads each slot element once, adds it, and
+// zeroes it in the same thread, so no barrier separates the reduce and the
+// clear.
+// HBM bytes (D experts with copies, U used slots): prefetch (D + U)*row_bytes
+// per tensor (row_bytes = H*H'*2 for bf16, H*H'/2 for packed MXFP4, H*H'/32
+// for its block scales); reduce (2*D + 2*U)*HHp*4.
 #include "copy_common.cuh"
 #include "moonep_internal.cuh"
 
@@ -27,46 +29,60 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxProj = 4;
 constexpr int kMaxTensors = 8;   // prefetch: e.g. gate/up/down and their block scales
-constexpr int kChunkVec = 4096;  // 16-byte vectors per unit (64 KB)
+constexpr int kChunkVec = 2048;  // 16-byte vectors per unit (32 KB)
 constexpr int kPU = 4;           // vectors per thread per step (prefetch)
 
 // Prefetch of n tensors whose expert rows have row_bytes[t] bytes each
 // (bf16 weights, packed MXFP4 bytes, block scales, ...).  A tensor whose
 // rows are 16-byte multiples on a 16-byte aligned base moves 16-byte vectors;
-// any other moves single bytes.
+// any other moves single bytes.  Units walk the experts that have copies (the
+// reduce list: expert, then its slots in (rank, slot) order): a chunk of the
+// expert's row is read once and stored to every slot holding it.
 struct PrefetchArgs {
   uint8_t *T[kMaxTensors];
   int64_t row_bytes[kMaxTensors];
-  int64_t nchunk[kMaxTensors];  // 64 KB units per row
+  int64_t nchunk[kMaxTensors];  // 32 KB units per row
   unsigned vec_mask;            // bit t: tensor t moves 16-byte vectors
-  const int32_t *meta, *copy_slot, *copy_expert;
+  const int32_t *meta, *red_expert, *red_first, *red_slot;
   int n, E;
 };
+
+constexpr int kMaxCopies = 64;  // slots holding one expert: at most one per rank
 
 __global__ void __launch_bounds__(kThreads) prefetch_kernel(PrefetchArgs a) {
   pdl_wait();
   pdl_launch_dependents();
-  const int64_t U = a.meta[kMetaU];
+  __shared__ int s_dst[kMaxCopies];  // slot rows of the staged expert
+  __shared__ int s_n;
+  const int64_t D = a.meta[kMetaD];
   int64_t units = 0;
-  for (int t = 0; t < a.n; t++) units += U * a.nchunk[t];
+  for (int t = 0; t < a.n; t++) units += D * a.nchunk[t];
+  int64_t staged = -1;  // expert index of the staged slot list
   for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
-    // unit -> (tensor, used slot, chunk); tensors in order, each U * nchunk units
+    // unit -> (tensor, expert with copies, chunk); tensors in order
     int t = 0;
     int64_t rem = unit;
-    while (t + 1 < a.n && rem >= U * a.nchunk[t]) {
-      rem -= U * a.nchunk[t];
+    while (t + 1 < a.n && rem >= D * a.nchunk[t]) {
+      rem -= D * a.nchunk[t];
       t++;
     }
-    const int64_t s = rem / a.nchunk[t];
-    const int64_t c = rem - s * a.nchunk[t];
-    const int slot = a.copy_slot[s];
-    const int e = a.copy_expert[s];
+    const int64_t di = rem / a.nchunk[t];
+    const int64_t c = rem - di * a.nchunk[t];
+    if (di != staged) {
+      __syncthreads();  // the previous list is no longer read
+      const int f0 = a.red_first[di], f1 = a.red_first[di + 1];
+      if (threadIdx.x == 0) s_n = min(f1 - f0, kMaxCopies);
+      for (int q = threadIdx.x; q < f1 - f0 && q < kMaxCopies; q += kThreads)
+        s_dst[q] = a.E + a.red_slot[f0 + q];
+      __syncthreads();
+      staged = di;
+    }
+    const int n = s_n;
     const int64_t rb = a.row_bytes[t];
-    const uint8_t *src = a.T[t] + (int64_t)e * rb;
-    uint8_t *dst = a.T[t] + ((int64_t)a.E + slot) * rb;
+    uint8_t *base = a.T[t];
+    const uint8_t *src = base + (int64_t)a.red_expert[di] * rb;
     if ((a.vec_mask >> t) & 1u) {
       const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-      uint4 *d4 = reinterpret_cast<uint4 *>(dst);
       const int64_t v_begin = c * kChunkVec;
       const int64_t v_end = min(v_begin + kChunkVec, rb / 16);
       for (int64_t v = v_begin + threadIdx.x; v < v_end; v += kThreads * kPU) {
@@ -74,14 +90,20 @@ __global__ void __launch_bounds__(kThreads) prefetch_kernel(PrefetchArgs a) {
 #pragma unroll
         for (int i = 0; i < kPU; i++)
           if (v + i * kThreads < v_end) x[i] = ld_stream(s4 + v + i * kThreads);
+        for (int q = 0; q < n; q++) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(base + (int64_t)s_dst[q] * rb);
 #pragma unroll
-        for (int i = 0; i < kPU; i++)
-          if (v + i * kThreads < v_end) st_global(d4 + v + i * kThreads, x[i]);
+          for (int i = 0; i < kPU; i++)
+            if (v + i * kThreads < v_end) st_global(d4 + v + i * kThreads, x[i]);
+        }
       }
     } else {
       const int64_t b_begin = c * kChunkVec * 16;
       const int64_t b_end = min(b_begin + (int64_t)kChunkVec * 16, rb);
-      for (int64_t v = b_begin + threadIdx.x; v < b_end; v += kThreads) dst[v] = src[v];
+      for (int64_t v = b_begin + threadIdx.x; v < b_end; v += kThreads) {
+        const uint8_t x = src[v];
+        for (int q = 0; q < n; q++) base[(int64_t)s_dst[q] * rb + v] = x;
+      }
     }
   }
 }
@@ -220,8 +242,9 @@ int launch_prefetch(moonep_ctx *ctx, const moonep_comm_plan *plan, int n, void *
     any = any || rb > 0;
   }
   a.meta = plan->internal;
-  a.copy_slot = plan->internal + lay.copy_slot;
-  a.copy_expert = plan->internal + lay.copy_expert;
+  a.red_expert = plan->internal + lay.red_expert;
+  a.red_first = plan->internal + lay.red_first;
+  a.red_slot = plan->internal + lay.red_slot;
   a.n = n;
   a.E = c.E;
   if (!any || c.B == 0) return MOONEP_OK;
