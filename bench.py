@@ -896,21 +896,24 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0:
-        # two single samples (the first also loads the oracle), then as many
-        # repeats as fit in about 15 s of CPU work
-        one = None
-        for _ in range(2):
-            a0 = time.perf_counter()
-            cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20)
-            one = time.perf_counter() - a0
-        reps = int(min(200, max(1, 15.0 / max(one, 1e-3))))
+        # the cost of one repeat (input generation excluded: one call with 3
+        # repeats minus one with 1), then as many repeats as fit in about 15 s
+        # of oracle work
+        a0 = time.perf_counter()
+        cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20)
+        t1 = time.perf_counter() - a0
+        a0 = time.perf_counter()
+        cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20, repeats=3)
+        t3 = time.perf_counter() - a0
+        per_rep = max((t3 - t1) / 2, 1e-3)
+        reps = int(min(400, max(1, 15.0 / per_rep)))
         a0 = time.perf_counter()
         v, step_s, per, sample = cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20,
                                               repeats=reps)
         wall = time.perf_counter() - a0
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{sample}; mean of {reps} repeats", "step_s": step_s,
-               "wall_s": round(one + wall, 2), "host": host_info()}
+               "wall_s": round(t1 + t3 + wall, 2), "host": host_info()}
 
     status = buf.get_status()
     line = {
