@@ -60,7 +60,7 @@ def parse():
                     help="time the step and nothing else (no sweep, chain, preparation, MXFP4, "
                          "end-to-end or CPU legs): a clean launch list for profilers")
     ap.add_argument("--sweep-steps", type=int, default=30)
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--graph", action="store_true",
                     help="capture one step in a CUDA graph and replay it in the timed region")
     ap.add_argument("--hp", type=int, default=None, help="override H' (profiling case)")
@@ -533,7 +533,7 @@ def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
         torch.cuda.synchronize()
         return start.elapsed_time(end) if timed else 0.0
 
-    run(3, False)
+    run(6, False)  # the host link reads slower for the first few hundred MB
     ms = max_over_ranks(run(steps, True), dist)
     del st
     return ms / steps, bi, bo
