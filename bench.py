@@ -533,7 +533,7 @@ def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
         torch.cuda.synchronize()
         return start.elapsed_time(end) if timed else 0.0
 
-    run(6, False)  # the host link reads slower for the first few hundred MB
+    run(6, False)  # warm-up: host copies and kernels
     ms = max_over_ranks(run(steps, True), dist)
     del st
     return ms / steps, bi, bo
