@@ -110,7 +110,7 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
   ctx->blocks_expand = occupancy_dedup(false);
   ctx->blocks_fold = occupancy_dedup(true);
   const size_t hist =
-      (size_t)plan_scratch_words(c.R, c.E, ctx->C, ctx->sms_device) * sizeof(int32_t);
+      (size_t)plan_scratch_words(c.R, c.E, ctx->C, c.K, ctx->sms_device) * sizeof(int32_t);
   const size_t ord = (size_t)c.R * ctx->C * sizeof(int32_t);
   e = cudaMalloc(&ctx->d_status, 256);
   if (e == cudaSuccess) e = cudaMemset(ctx->d_status, 0, 256);
@@ -401,8 +401,8 @@ int moonep_get_status(moonep_ctx *ctx, int *device_status, void *stream) {
   // out of step: start them again from zero.
   if (e == cudaSuccess && v == MOONEP_ERR_TIMEOUT) {
     const moonep_config &c = ctx->cfg;
-    const int64_t off = plan_totals_offset(c.R, c.E, ctx->C, ctx->sms_device);
-    const int64_t words = plan_scratch_words(c.R, c.E, ctx->C, ctx->sms_device) - off;
+    const int64_t off = plan_totals_offset(c.R, c.E, ctx->C, c.K, ctx->sms_device);
+    const int64_t words = plan_scratch_words(c.R, c.E, ctx->C, c.K, ctx->sms_device) - off;
     e = cudaMemset(ctx->d_sync, 0, 2 * sizeof(unsigned long long));
     if (e == cudaSuccess) e = cudaMemset(ctx->d_hist + off, 0, (size_t)words * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();

@@ -135,12 +135,12 @@ cudaError_t plan_configure(int R, int E, int B);
 // K when the single-launch planner handles this shape (0: the tile path).
 int plan_fused_choice(int R, int E, int K, int B, int C, int sms);
 // Tiles the histogram area must hold (either planner path).
-int plan_hist_tiles(int R, int C, int sms);
+int plan_hist_tiles(int R, int C, int K, int sms);
 // The planner's scratch (ctx->d_hist): E words per tile, then two sets of
 // [R, E] totals (at plan_totals_offset) and two error words, used by
 // alternate calls, zero before a call uses them.
-int64_t plan_totals_offset(int R, int E, int C, int sms);
-int64_t plan_scratch_words(int R, int E, int C, int sms);
+int64_t plan_totals_offset(int R, int E, int C, int K, int sms);
+int64_t plan_scratch_words(int R, int E, int C, int K, int sms);
 int occupancy_dispatch(int K);
 int occupancy_combine(int K);
 int occupancy_copy();

@@ -26,7 +26,8 @@
 //                          own copy of the per-rank totals and assigns its
 //                          routes; two extra CTAs write the plan's tables
 //                          and the experts-with-copies list.
-//   The tile path (K not dividing 32, or tables too large for one CTA):
+//   The tile path (tables too large for one CTA, more than 64 ranks, or more
+//   tiles than SMs):
 //   K1 plan_hist_kernel    per 2048-route tile: per-expert counts and each
 //                          route's ordinal among same-expert routes of the tile
 //                          (warp-aggregated with one ballot per key bit, stable).
@@ -754,9 +755,10 @@ plan_assign_kernel(PlanDims d, const int32_t *__restrict__ topk, const int32_t *
 // ------------------------------------------------------------- fused
 //
 // The whole planner in one cooperative launch: G tile blocks of 1024
-// threads, R*ceil(S*K/(1024*IT)) of them, one per tile of a source rank, plus
-// a table block and a list block:
-//   1. each warp of a tile block walks IT chunks of 32 consecutive routes and
+// threads, R*ceil(S*K/(32*IT*lpc)) of them (lpc = floor(32/K)*K routes per
+// warp chunk), one per tile of a source rank, plus a table block and a list
+// block:
+//   1. each warp of a tile block walks IT chunks of consecutive routes and
 //      counts them per expert (warp-aggregated, stable ordinals kept in
 //      registers);
 //   2. per-expert offsets of the warps; the tile's histogram to global; the
@@ -773,13 +775,16 @@ plan_assign_kernel(PlanDims d, const int32_t *__restrict__ topk, const int32_t *
 //   5. the tile blocks add their duplicate counts straight into the plan
 //      (the table block zeroed them before the meeting); the table block
 //      clears the other set of per-rank totals, which the next call uses.
-// Used when K divides 32 (a token's routes then never straddle a 32-route
-// chunk), the blocks fit on the SMs at once and the tables fit in shared
-// memory; otherwise the three-kernel tile path runs.
+// A warp's chunk holds floor(32 / K) whole tokens, so a token's routes never
+// straddle two chunks.  Used when the blocks fit on the SMs at once and the
+// tables fit in shared memory; otherwise the three-kernel tile path runs.
 
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedWarps = kFusedThreads / 32;
-constexpr int kFusedMaxItems = 8;  // routes per thread: 1, 2, 4 or 8 (tile = 1024 * items)
+constexpr int kFusedMaxItems = 8;  // routes per thread: 1, 2, 4 or 8
+
+// Routes per warp chunk: whole tokens only (floor(32 / K) * K).
+__host__ __device__ __forceinline__ int fused_lanes(int K) { return 32 - 32 % K; }
 
 struct FusedArgs {
   PlanDims d;
@@ -855,7 +860,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   const unsigned lt = lanemask_lt();
   const int nbits = key_bits(E);
   constexpr int items = IT;
-  const int wbase = t * kFusedThreads * items + warp * 32 * items;
+  // a warp's chunk holds whole tokens: lpc = floor(32 / K) * K routes (all 32
+  // lanes when K divides 32; the lanes past lpc carry no route)
+  const int lpc = fused_lanes(d.K);
+  const int wbase = t * kFusedWarps * items * lpc + warp * lpc * items;
   int e_reg[items], o_reg[items];
   if (tid == 0) {
     s_bad = 0;
@@ -877,15 +885,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     bool bad = false;
 #pragma unroll
     for (int c = 0; c < items; c++) {
-      const int i = wbase + c * 32 + lane;
-      e_reg[c] = i < C ? __ldg(src + i) : -1;
+      const int i = wbase + c * lpc + lane;
+      e_reg[c] = lane < lpc && i < C ? __ldg(src + i) : -1;
     }
 #pragma unroll
     for (int c = 0; c < items; c++) {
-      const int i = wbase + c * 32 + lane;
+      const int i = wbase + c * lpc + lane;
+      const bool route = lane < lpc && i < C;
       int e = e_reg[c];
-      if (i < C && (e < 0 || e >= E)) bad = true;
-      if (i >= C || e < 0 || e >= E) e = -1;
+      if (route && (e < 0 || e >= E)) bad = true;
+      if (!route || e < 0 || e >= E) e = -1;
       const unsigned m = match_key(e >= 0 ? e : E, nbits);
       int base = 0;
       if (e >= 0) base = hw[e];
@@ -980,14 +989,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   const bool valid = ok && bs.err == 0;
   const int K = d.K;
   // A token's K routes sit in K consecutive lanes.  Routes of one token that
-  // land on the same rank share the key (token lane group, rank).
-  const int dkey_bits = key_bits((32 / K) * (R + 1));
+  // land on the same rank share the key (token lane group, rank); the lanes
+  // past lpc form a group of their own.
+  const int dkey_bits = key_bits(((32 + K - 1) / K) * (R + 1));
   const int rkey_bits = key_bits(R);
   int32_t *dst = a.o.dst + (int64_t)r * C;
 #pragma unroll
   for (int c = 0; c < items; c++) {
-    const int i = wbase + c * 32 + lane;
-    const bool in_range = i < C;
+    const int i = wbase + c * lpc + lane;
+    const bool in_range = lane < lpc && i < C;
     int j = R, row = 0;
     if (in_range) {
       j = 0;
@@ -1158,40 +1168,39 @@ plan_dup_write_kernel(PlanDims d, const int32_t *__restrict__ dst,
 // Routes per thread of the single-launch planner: the fewest (most tiles,
 // most SMs at work) for which every tile block and the two table blocks fit on
 // the SMs at once; 0 if none.
-int plan_fused_items(int R, int C, int sms) {
-  for (int items = 1; items <= kFusedMaxItems; items *= 2) {
-    const int tpr = (C + kFusedThreads * items - 1) / (kFusedThreads * items);
-    if ((int64_t)R * (tpr > 0 ? tpr : 1) + 2 <= sms) return items;
-  }
+int plan_fused_tiles(int C, int K, int items) {
+  const int per_tile = kFusedWarps * items * fused_lanes(K);
+  const int tpr = (C + per_tile - 1) / per_tile;
+  return tpr > 0 ? tpr : 1;
+}
+
+int plan_fused_items(int R, int C, int K, int sms) {
+  for (int items = 1; items <= kFusedMaxItems; items *= 2)
+    if ((int64_t)R * plan_fused_tiles(C, K, items) + 2 <= sms) return items;
   return 0;
 }
 
 // Tiles of either planner path (the histogram area holds E words per tile).
-int plan_hist_tiles(int R, int C, int sms) {
+int plan_hist_tiles(int R, int C, int K, int sms) {
   const int tile_path = R * ((C + kTile - 1) / kTile);
-  const int items = plan_fused_items(R, C, sms);
-  const int fused = items ? R * ((C + kFusedThreads * items - 1) / (kFusedThreads * items)) : 0;
+  const int items = plan_fused_items(R, C, K, sms);
+  const int fused = items ? R * plan_fused_tiles(C, K, items) : 0;
   return tile_path > fused ? tile_path : fused;
 }
 
-int64_t plan_totals_offset(int R, int E, int C, int sms) {
-  return (int64_t)E * plan_hist_tiles(R, C, sms);
+int64_t plan_totals_offset(int R, int E, int C, int K, int sms) {
+  return (int64_t)E * plan_hist_tiles(R, C, K, sms);
 }
 
-int64_t plan_scratch_words(int R, int E, int C, int sms) {
-  return plan_totals_offset(R, E, C, sms) + 2 * (int64_t)R * E + 8;
-}
-
-int plan_fused_tiles(int C, int items) {
-  const int tpr = (C + kFusedThreads * items - 1) / (kFusedThreads * items);
-  return tpr > 0 ? tpr : 1;
+int64_t plan_scratch_words(int R, int E, int C, int K, int sms) {
+  return plan_totals_offset(R, E, C, K, sms) + 2 * (int64_t)R * E + 8;
 }
 
 // Shared memory the planner kernels may use.
 constexpr size_t kPlanSmemLimit = 200 * 1024;
 
 int plan_fused_choice(int R, int E, int K, int B, int C, int sms) {
-  if (32 % K != 0 || R > kMaxR || plan_fused_items(R, C, sms) == 0) return 0;
+  if (K < 1 || K > kMaxK || R > kMaxR || plan_fused_items(R, C, K, sms) == 0) return 0;
   return fused_smem_words(R, E, B) * sizeof(int32_t) <= kPlanSmemLimit ? K : 0;
 }
 
@@ -1267,10 +1276,10 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     fa.topk = topk;
     fa.tpe = tpe;
     fa.hist = ctx->d_hist;
-    const int items = plan_fused_items(d.R, d.C, ctx->sms_device);
-    fa.tpr = plan_fused_tiles(d.C, items);
+    const int items = plan_fused_items(d.R, d.C, d.K, ctx->sms_device);
+    fa.tpr = plan_fused_tiles(d.C, d.K, items);
     fa.G = d.R * fa.tpr;
-    fa.totals = ctx->d_hist + plan_totals_offset(d.R, d.E, d.C, ctx->sms_device);
+    fa.totals = ctx->d_hist + plan_totals_offset(d.R, d.E, d.C, d.K, ctx->sms_device);
     fa.errw = fa.totals + 2 * (int64_t)d.R * d.E;
     fa.o = o;
     fa.in = in;

@@ -90,8 +90,8 @@ extern "C" int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk
   // plan tables
   const int64_t tpr = (C + kTile - 1) / kTile;
   const int64_t sync_words = 64;
-  const int64_t totals_off = plan_totals_offset(c.R, c.E, (int)C, sms);
-  const int64_t hist_words = round_words(plan_scratch_words(c.R, c.E, (int)C, sms));
+  const int64_t totals_off = plan_totals_offset(c.R, c.E, (int)C, c.K, sms);
+  const int64_t hist_words = round_words(plan_scratch_words(c.R, c.E, (int)C, c.K, sms));
   const int64_t ord_words = round_words((int64_t)c.R * C);
   const PlanLayout lay = PlanLayout::make(c.R, c.E, c.B, (int)nvs, false);
   if (sync_words + hist_words + ord_words + lay.total > kNoAllocScratchWords)
@@ -108,7 +108,7 @@ extern "C" int moonep_plan_noalloc(const moonep_config *cfg, const int32_t *topk
   // shape).
   if (cudaMemsetAsync(scratch, 0, sync_words * sizeof(int32_t), s) != cudaSuccess ||
       cudaMemsetAsync(scratch + sync_words + totals_off, 0,
-                      (size_t)(plan_scratch_words(c.R, c.E, (int)C, sms) - totals_off) *
+                      (size_t)(plan_scratch_words(c.R, c.E, (int)C, c.K, sms) - totals_off) *
                           sizeof(int32_t),
                       s) != cudaSuccess)
     return MOONEP_ERR_CUDA;

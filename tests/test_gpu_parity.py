@@ -208,6 +208,15 @@ def test_wide_and_odd_top_k(K):
     _full_pipeline(sh, topk, K)
 
 
+@pytest.mark.parametrize("K", [2, 6, 8])
+def test_tile_path_planner(K):
+    """Tables too large for the single-launch planner's shared memory
+    (E = 1536) take the three-kernel tile path; it must give the same plan."""
+    sh = wl.Shape("tilepath", R=8, E=1536, K=K, S=96, H=64, Hp=8, B=192, tp=8,
+                  weights="softmax")
+    _full_pipeline(sh, _routing(sh, "zipf", 40 + K), 40 + K)
+
+
 def test_largest_tables():
     """The largest expert table the library takes (E = 4096, R = 64, B = 64,
     K = 8): the planner's tables no longer fit in shared memory, so the tile
