@@ -66,11 +66,14 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 }
 
 // KT: compile-time K (0 = runtime K, up to 32).  U: vectors per lane per unit.
-// BT: threads per block (128 for K = 8 and K = 2, whose 100+ registers per
-// thread leave room for more resident warps in small blocks).  KB: rows
-// loaded per batch (K = 8 reads 2 KB of each row per unit, in two batches of
-// four rows; K = 2 reads 4 KB of both rows at once: 0.98 of the copy
-// bandwidth on the Mixtral shape, 0.95 with 2 KB).  PRIM: sum the primary
+// BT: threads per block (128 for the specialised K: with 80-170 registers per
+// thread, small blocks leave room for more resident warps).  KB: rows loaded
+// per batch.  Per K, chosen by measurement: K = 8 reads 2 KB of each row per
+// unit in two batches of four rows; K = 2 reads 4 KB of both rows at once
+// (0.98 of the copy bandwidth on the Mixtral shape, 0.95 with 2 KB); K = 3
+// reads 4 KB of one row at a time, K = 4 2 KB of two rows, K = 6 2 KB of three
+// rows (1.00-1.04 of the copy bandwidth each, where the runtime-K kernel gave
+// 0.66-0.78).  PRIM: sum the primary
 // routes only (dst >= 0; the duplicates were folded into them), a separate
 // instantiation so that the direct kernel carries none of its code.
 template <int KT, int U, int BT, int KB, bool PRIM>
@@ -164,10 +167,12 @@ int occupancy_combine(int K) {
   int n = 0;
   void *f = K == 1 ? (void *)combine_kernel<1, 4, 256, 1, false>
           : K == 2 ? (void *)combine_kernel<2, 8, 128, 2, false>
-          : K == 4 ? (void *)combine_kernel<4, 4, 256, 4, false>
+          : K == 3 ? (void *)combine_kernel<3, 8, 128, 1, false>
+          : K == 4 ? (void *)combine_kernel<4, 4, 128, 2, false>
+          : K == 6 ? (void *)combine_kernel<6, 4, 128, 3, false>
           : K == 8 ? (void *)combine_kernel<8, 4, 128, 4, false>
                    : (void *)combine_kernel<0, 2, 256, 1, false>;
-  const int bt = (K == 8 || K == 2) ? 128 : 256;
+  const int bt = (K == 2 || K == 3 || K == 4 || K == 6 || K == 8) ? 128 : 256;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, bt, 0) != cudaSuccess) n = 1;
   return n > 0 ? n : 1;
 }
@@ -187,7 +192,7 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
   a.total_rows = (int64_t)c.R * ctx->NvS;
   a.K = c.K;
   a.H8 = c.H / 8;
-  const int U = c.K == 2 ? 8 : (c.K == 1 || c.K == 4 || c.K == 8) ? 4 : 2;
+  const int U = (c.K == 2 || c.K == 3) ? 8 : (c.K == 1 || c.K == 4 || c.K == 6 || c.K == 8) ? 4 : 2;
   a.nchunk = (a.H8 + 32 * U - 1) / (32 * U);
   if (a.ntok == 0 || a.H8 == 0) return MOONEP_OK;
   const int grid = ctx->sms * ctx->blocks_combine;
@@ -195,7 +200,9 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
   switch (c.K) {
     case 1: e = launch<1, 4, 256, 1>(a, primaries_only, grid, st); break;
     case 2: e = launch<2, 8, 128, 2>(a, primaries_only, grid, st); break;
-    case 4: e = launch<4, 4, 256, 4>(a, primaries_only, grid, st); break;
+    case 3: e = launch<3, 8, 128, 1>(a, primaries_only, grid, st); break;
+    case 4: e = launch<4, 4, 128, 2>(a, primaries_only, grid, st); break;
+    case 6: e = launch<6, 4, 128, 3>(a, primaries_only, grid, st); break;
     case 8: e = launch<8, 4, 128, 4>(a, primaries_only, grid, st); break;
     default: e = launch<0, 2, 256, 1>(a, primaries_only, grid, st); break;
   }

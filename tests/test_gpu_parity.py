@@ -185,7 +185,7 @@ def test_random_small_configs(seed):
     R = int(rng.integers(1, 9))
     L = int(rng.integers(1, 9))
     E = R * L
-    K = int(rng.choice([1, 2, 3, 4, 5, 8, 12]))
+    K = int(rng.choice([1, 2, 3, 4, 5, 6, 8, 12]))
     S = int(rng.integers(1, 700))
     B = L + int(rng.integers(0, 3))
     tp = int(rng.choice([1, 2, 3, 8, 16, 128]))
