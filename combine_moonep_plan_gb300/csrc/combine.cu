@@ -72,8 +72,9 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 // unit in two batches of four rows; K = 2 reads 4 KB of both rows at once
 // (0.98 of the copy bandwidth on the Mixtral shape, 0.95 with 2 KB); K = 3
 // reads 4 KB of one row at a time, K = 4 2 KB of two rows, K = 6 2 KB of three
-// rows (1.00-1.04 of the copy bandwidth each, where the runtime-K kernel gave
-// 0.66-0.78).  PRIM: sum the primary
+// rows (1.00-1.04 of the copy bandwidth each, where a runtime-K kernel gave
+// 0.66-0.78), K = 10 4 KB of one row at a time (0.85); any other K takes the
+// runtime-K kernel, four rows per batch.  PRIM: sum the primary
 // routes only (dst >= 0; the duplicates were folded into them), a separate
 // instantiation so that the direct kernel carries none of its code.
 template <int KT, int U, int BT, int KB, bool PRIM>
@@ -134,15 +135,29 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
         }
       }
     } else {
-      for (int k = 0; k < K; k++) {
-        const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k) * a.H8;
-        if ((dupm >> k) & 1u) continue;
+      // runtime K: batches of KB rows, the last one partial
+      for (int k0 = 0; k0 < K; k0 += KB) {
+        uint4 x[KB][U];
+#pragma unroll
+        for (int kk = 0; kk < KB; kk++) {
+          const int k = k0 + kk;
+          const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k & 31) * a.H8;
+          const bool use = k < K && !((dupm >> (k & 31)) & 1u);
+#pragma unroll
+          for (int i = 0; i < U; i++) {
+            const int v = v0 + 32 * i;
+            if (use && v < a.H8) x[kk][i] = ld_stream(row + v);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < U; i++) {
-          const int v = v0 + 32 * i;
-          uint4 xv = make_uint4(0, 0, 0, 0);
-          if (v < a.H8) xv = ld_stream(row + v);
-          if (k == 0) set_bf16x8(acc[i], xv); else add_bf16x8(acc[i], xv);
+#pragma unroll
+          for (int kk = 0; kk < KB; kk++) {
+            const int k = k0 + kk;
+            if (k >= K || ((dupm >> (k & 31)) & 1u)) continue;
+            if (k == 0) set_bf16x8(acc[i], x[kk][i]);
+            else add_bf16x8(acc[i], x[kk][i]);
+          }
         }
       }
     }
@@ -171,8 +186,9 @@ int occupancy_combine(int K) {
           : K == 4 ? (void *)combine_kernel<4, 4, 128, 2, false>
           : K == 6 ? (void *)combine_kernel<6, 4, 128, 3, false>
           : K == 8 ? (void *)combine_kernel<8, 4, 128, 4, false>
-                   : (void *)combine_kernel<0, 2, 256, 1, false>;
-  const int bt = (K == 2 || K == 3 || K == 4 || K == 6 || K == 8) ? 128 : 256;
+          : K == 10 ? (void *)combine_kernel<10, 8, 128, 1, false>
+                    : (void *)combine_kernel<0, 4, 128, 4, false>;
+  const int bt = K == 1 ? 256 : 128;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, bt, 0) != cudaSuccess) n = 1;
   return n > 0 ? n : 1;
 }
@@ -192,7 +208,7 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
   a.total_rows = (int64_t)c.R * ctx->NvS;
   a.K = c.K;
   a.H8 = c.H / 8;
-  const int U = (c.K == 2 || c.K == 3) ? 8 : (c.K == 1 || c.K == 4 || c.K == 6 || c.K == 8) ? 4 : 2;
+  const int U = (c.K == 2 || c.K == 3 || c.K == 10) ? 8 : 4;
   a.nchunk = (a.H8 + 32 * U - 1) / (32 * U);
   if (a.ntok == 0 || a.H8 == 0) return MOONEP_OK;
   const int grid = ctx->sms * ctx->blocks_combine;
@@ -204,7 +220,8 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
     case 4: e = launch<4, 4, 128, 2>(a, primaries_only, grid, st); break;
     case 6: e = launch<6, 4, 128, 3>(a, primaries_only, grid, st); break;
     case 8: e = launch<8, 4, 128, 4>(a, primaries_only, grid, st); break;
-    default: e = launch<0, 2, 256, 1>(a, primaries_only, grid, st); break;
+    case 10: e = launch<10, 8, 128, 1>(a, primaries_only, grid, st); break;
+    default: e = launch<0, 4, 128, 4>(a, primaries_only, grid, st); break;
   }
   return cuda_status(e);
 }
