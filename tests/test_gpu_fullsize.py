@@ -266,3 +266,40 @@ def test_full_size_three_projections():
     del Gh, Gs
     buf.destroy()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("R,E,K,S,B,H", [(8, 160, 6, 4096, 20, 5120), (8, 512, 10, 2048, 64, 2048),
+                                         (8, 128, 3, 8192, 16, 4096)])
+def test_full_size_other_top_k(R, E, K, S, B, H):
+    """Top-K values outside the five workload shapes (top-6 with 160 experts,
+    top-10 with 512, top-3), at full batch sizes: the single-launch planner
+    with whole-token warp chunks (several tiles per rank) against the oracle's
+    plan bit for bit, the dispatch scatter in full on the device, and the
+    combine by its closed form in fp32 (K copies of a row add exactly)."""
+    from combine_moonep_plan_gb300.api import Buffer
+    sh = wl.Shape("topk", R=R, E=E, K=K, S=S, H=H, Hp=64, B=B, tp=128, weights="softmax")
+    seed = 4242 + K
+    topk = wl.routing(sh, "zipf", target_maxvio=1.5, seed=seed)[0]
+    tpe = wl.tokens_per_expert(topk, E)
+    st, op = oracle.plan(R, E, K, S, B, 128, topk, tpe, dup_records=False)
+    assert st == 0
+    buf = Buffer(S=S, H=H, K=K, E=E, num_ep_ranks=R, B=B, token_padding=128,
+                 zero_copy_views=False)
+    dev = "cuda"
+    x = torch.randn((R, S, H), device=dev).to(torch.bfloat16)
+    hid, _, _, plan = buf.dispatch(x, None, torch.from_numpy(topk).to(dev),
+                                   torch.from_numpy(tpe).to(dev))
+    assert buf.get_status() == 0
+    for f in ("dst", "experts_to_copy", "cu_seqlens", "zero_fill_ranges", "remote_stats",
+              "dup_counts"):
+        assert np.array_equal(getattr(plan, f).cpu().numpy(), op[f]), f
+    gidx = torch.from_numpy(decode(op["dst"]).reshape(-1)).to(dev)
+    tok = torch.arange(R * S, device=dev).repeat_interleave(K)
+    xf = x.reshape(R * S, H)
+    for c0 in range(0, gidx.numel(), 1 << 16):
+        c1 = c0 + (1 << 16)
+        assert torch.equal(hid[gidx[c0:c1]].view(torch.int16), xf[tok[c0:c1]].view(torch.int16))
+    out, _ = buf.combine(plan, hid)
+    assert torch.equal(out.view(torch.int16), (x.float() * K).to(torch.bfloat16).view(torch.int16))
+    buf.destroy()
+    torch.cuda.empty_cache()
