@@ -10,10 +10,11 @@
 // Here the batch already sits in capacity-sized [R, S, ...] buffers (rank r's
 // first num_tokens[r] rows valid), and the preparation runs in place: only
 // padding rows and invalid routes are written, so a full batch costs one read
-// of the ids and weights.  Blocks [0, R) each take one rank's S*K routes
-// (sanitise, count per expert in shared memory, write tokens_per_expert);
-// the remaining blocks zero the padding rows of the hidden tensor with
-// 16-byte stores.
+// of the ids and weights.  Blocks [0, R) each take one rank's S*K routes,
+// eight per thread with their loads in flight together (sanitise, count per
+// expert in shared memory, write tokens_per_expert); the remaining blocks
+// zero the padding rows of the hidden tensor, one warp per 2 KB of a row
+// with 16-byte stores.
 #include "copy_common.cuh"
 #include "moonep_internal.cuh"
 
@@ -21,7 +22,9 @@ namespace moonep {
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kZeroVec = 128;  // 16-byte vectors per zeroing unit (2 KB of a row)
 constexpr int kMaxRanks = 64;
+constexpr int kBatch = 8;  // routes per thread whose loads are in flight together
 
 struct PrepArgs {
   int32_t ntok[kMaxRanks];  // valid tokens of each rank
@@ -37,7 +40,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepArgs a) {
   pdl_wait();
   pdl_launch_dependents();
   extern __shared__ int32_t hist[];  // [E], route blocks only
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   if ((int)blockIdx.x < a.R) {
     const int r = blockIdx.x;
     const int n = a.ntok[r];
@@ -47,22 +50,37 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepArgs a) {
     const int64_t C = (int64_t)a.S * a.K;
     int32_t *ids = a.topk + r * C;
     float *ws = a.w ? a.w + r * C : nullptr;
-    for (int64_t i = tid; i < C; i += kThreads) {
-      const int s = (int)(i / a.K);
-      int e = ids[i];
-      if (s >= n || e < 0) {
-        if (e != 0) ids[i] = 0;
-        if (ws) ws[i] = 0.0f;
-        e = 0;
+    // few experts: the routes of a warp share counters, so they are added
+    // once per distinct id (match), not once per route
+    const bool few = a.E <= 32;
+    for (int64_t i0 = 0; i0 < C; i0 += (int64_t)kThreads * kBatch) {
+      int ev[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; b++) {
+        const int64_t i = i0 + (int64_t)b * kThreads + tid;
+        ev[b] = i < C ? ids[i] : 0;
       }
-      if (a.tpe) {
-        // padding routes all land on expert 0: one shared add per warp for them
-        const unsigned act = __activemask();
-        const unsigned z0 = __ballot_sync(act, e == 0);
-        if (e == 0) {
-          if ((tid & 31) == __ffs(z0) - 1) atomicAdd(&hist[0], __popc(z0));
-        } else if (e < a.E) {
-          atomicAdd(&hist[e], 1);
+#pragma unroll
+      for (int b = 0; b < kBatch; b++) {
+        const int64_t i = i0 + (int64_t)b * kThreads + tid;
+        int e = ev[b];
+        if (i < C) {
+          const int s = (int)(i / a.K);
+          if (s >= n || e < 0) {
+            if (e != 0) ids[i] = 0;
+            if (ws) ws[i] = 0.0f;
+            e = 0;
+          }
+        } else {
+          e = -1;
+        }
+        if (a.tpe) {
+          if (few) {
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && e < a.E && lane == __ffs(m) - 1) atomicAdd(&hist[e], __popc(m));
+          } else if (e >= 0 && e < a.E) {
+            atomicAdd(&hist[e], 1);
+          }
         }
       }
     }
@@ -71,17 +89,21 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepArgs a) {
       for (int e = tid; e < a.E; e += kThreads) a.tpe[(int64_t)r * a.E + e] = hist[e];
     return;
   }
-  // zero the padding rows: vector v of the flattened padding rows
-  const int64_t total = (int64_t)a.pad_first[a.R] * a.H8;
-  const int64_t stride = (int64_t)(gridDim.x - a.R) * kThreads;
+  // zero the padding rows: one warp per 2 KB of a row (flattened over the
+  // ranks' padding rows)
+  const int nch = (a.H8 + kZeroVec - 1) / kZeroVec;
+  const int64_t units = (int64_t)a.pad_first[a.R] * nch;
+  const int64_t warps = ((int64_t)(gridDim.x - a.R) * kThreads) >> 5;
   const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int64_t v = (int64_t)(blockIdx.x - a.R) * kThreads + tid; v < total; v += stride) {
-    const int64_t q = v / a.H8;
-    const int c = (int)(v - q * a.H8);
+  for (int64_t u = ((int64_t)(blockIdx.x - a.R) * kThreads + tid) >> 5; u < units; u += warps) {
+    const int64_t q = u / nch;
+    const int c = (int)(u - q * nch);
     int r = 0;
     while (r + 1 < a.R && a.pad_first[r + 1] <= q) r++;
     const int64_t s = a.ntok[r] + (q - a.pad_first[r]);
-    st_global(a.hidden + ((int64_t)r * a.S + s) * a.H8 + c, z);
+    uint4 *row = a.hidden + ((int64_t)r * a.S + s) * a.H8;
+    const int v1 = min(a.H8, (c + 1) * kZeroVec);
+    for (int v = c * kZeroVec + lane; v < v1; v += 32) st_global(row + v, z);
   }
 }
 
@@ -108,8 +130,9 @@ int launch_prepare(moonep_ctx *ctx, const int32_t *num_tokens, uint16_t *hidden,
   a.K = c.K;
   a.E = c.E;
   a.H8 = c.H / 8;
-  const int64_t vecs = hidden ? pad_rows * a.H8 : 0;
-  int64_t zb = (vecs + kThreads - 1) / kThreads;
+  // one warp per 2 KB of a padding row, at most four blocks per SM
+  const int64_t zunits = hidden ? pad_rows * ((a.H8 + kZeroVec - 1) / kZeroVec) : 0;
+  int64_t zb = (zunits * 32 + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)ctx->sms * 4;
   if (zb > cap) zb = cap;
   if (!hidden) a.pad_first[c.R] = 0;
