@@ -41,6 +41,9 @@
 //                          one CTA per (1024-row tile, rank): the tile's group
 //                          and duplicate counts, then compact duplicate
 //                          records in ascending primary row.
+#include <map>
+#include <mutex>
+
 #include "moonep_internal.cuh"
 
 namespace moonep {
@@ -1208,35 +1211,42 @@ static bool bal_in_shared(int R, int E, int B) {
   return bal_tables_words(R, E, B) * sizeof(int32_t) <= kPlanSmemLimit;
 }
 
+// Raise a kernel's dynamic shared memory limit to at least `bytes` (never
+// lower it: contexts of different shapes share the kernels).  The default
+// limit is 48 KB minus the kernel's static shared memory, so any size is set
+// explicitly.
+static cudaError_t raise_dyn_smem(const void *f, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void *>, int> limit;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  int &cur = limit[{dev, f}];
+  if (bytes <= cur) return cudaSuccess;
+  e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
+}
+
 cudaError_t plan_configure(int R, int E, int B) {
   const int hist_smem = (kPlanThreads / 32) * E * (int)sizeof(int32_t);
   const int assign_smem = (3 * E + 8 * R) * (int)sizeof(int32_t);
   const int bal_smem =
       bal_in_shared(R, E, B) ? (int)(bal_tables_words(R, E, B) * sizeof(int32_t)) : 0;
-  cudaError_t e = cudaSuccess;
-  if (hist_smem > 48 * 1024)
-    e = cudaFuncSetAttribute(plan_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             hist_smem);
-  if (e == cudaSuccess && bal_smem > 48 * 1024)
-    e = cudaFuncSetAttribute(plan_balance_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bal_smem);
-  if (e == cudaSuccess && assign_smem > 48 * 1024) {
-    const void *fs[] = {(const void *)plan_assign_kernel<0>, (const void *)plan_assign_kernel<1>,
-                        (const void *)plan_assign_kernel<2>, (const void *)plan_assign_kernel<4>,
-                        (const void *)plan_assign_kernel<6>, (const void *)plan_assign_kernel<8>};
-    for (const void *f : fs)
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, assign_smem);
-  }
+  cudaError_t e = raise_dyn_smem((const void *)plan_hist_kernel, hist_smem);
+  if (e == cudaSuccess) e = raise_dyn_smem((const void *)plan_balance_kernel, bal_smem);
+  const void *as[] = {(const void *)plan_assign_kernel<0>, (const void *)plan_assign_kernel<1>,
+                      (const void *)plan_assign_kernel<2>, (const void *)plan_assign_kernel<4>,
+                      (const void *)plan_assign_kernel<6>, (const void *)plan_assign_kernel<8>};
+  for (const void *f : as)
+    if (e == cudaSuccess) e = raise_dyn_smem(f, assign_smem);
   if (e == cudaSuccess && plan_fused_choice(R, E, 1, B, 0, 1 << 30)) {
     const int fsmem = (int)(fused_smem_words(R, E, B) * sizeof(int32_t));
-    if (fsmem > 48 * 1024) {
-      const void *fs[] = {(const void *)plan_fused_kernel<1>, (const void *)plan_fused_kernel<2>,
-                          (const void *)plan_fused_kernel<4>, (const void *)plan_fused_kernel<8>};
-      for (const void *f : fs)
-        if (e == cudaSuccess)
-          e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, fsmem);
-    }
+    const void *fs[] = {(const void *)plan_fused_kernel<1>, (const void *)plan_fused_kernel<2>,
+                        (const void *)plan_fused_kernel<4>, (const void *)plan_fused_kernel<8>};
+    for (const void *f : fs)
+      if (e == cudaSuccess) e = raise_dyn_smem(f, fsmem);
   }
   return e;
 }

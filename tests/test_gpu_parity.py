@@ -208,6 +208,78 @@ def test_wide_and_odd_top_k(K):
     _full_pipeline(sh, topk, K)
 
 
+@pytest.mark.parametrize("block", range(4))
+def test_random_wide_configs(block):
+    """100 random shapes (up to 16 ranks, top-1..16, 1..12 experts per rank,
+    token_padding 1..128, rows of 16 bytes to 4 KB, mild to sharp skew): the
+    plan and its duplicate records bit for bit with the oracle, the whole
+    dispatch scatter and its deduplicated form, the route weights, and the
+    combine of the dispatched rows (K copies add exactly in fp32)."""
+    for seed in range(25 * block, 25 * (block + 1)):
+        rng = np.random.default_rng(777000 + seed)
+        R = int(rng.integers(1, 17))
+        L = int(rng.integers(1, 13))
+        E = R * L
+        K = int(rng.integers(1, 17))
+        S = int(rng.integers(1, 1500))
+        B = L + int(rng.integers(0, 3))
+        tp = int(rng.choice([1, 2, 4, 8, 16, 64, 128]))
+        H = int(rng.choice([8, 16, 64, 520, 1024, 2056]))
+        p = rng.random(E) ** float(rng.choice([1, 4, 8]))
+        topk = rng.choice(E, size=(R, S, K), p=p / p.sum()).astype(np.int32)
+        tpe = wl.tokens_per_expert(topk, E)
+        cfg = dict(R=R, E=E, K=K, S=S, B=B, tp=tp)
+        st, op = _oracle_plan(cfg, topk, tpe)
+        assert st == 0
+        buf = _buffer(cfg, H=H, views=False)
+        x = torch.from_numpy(rng.standard_normal((R, S, H)).astype(np.float32)).bfloat16().cuda()
+        w = torch.from_numpy(rng.random((R, S, K)).astype(np.float32)).cuda()
+        hid, wn, _, plan = buf.dispatch(x, w, torch.from_numpy(topk).cuda(),
+                                        torch.from_numpy(tpe).cuda())
+        assert buf.get_status() == 0, cfg
+        _cmp_plan(plan, op, cfg)
+        g = torch.from_numpy(decode(op["dst"]).reshape(-1)).cuda()
+        tok = torch.arange(R * S, device="cuda").repeat_interleave(K)
+        assert torch.equal(hid[g].view(torch.int16), x.reshape(-1, H)[tok].view(torch.int16)), cfg
+        assert torch.equal(wn[g], w.reshape(-1)), cfg
+        hd, _, _, _ = buf.dispatch(x, w, plan=plan, dedup=True)
+        assert torch.equal(hd[g].view(torch.int16), hid[g].view(torch.int16)), cfg
+        out, wb = buf.combine(plan, hid, wn)
+        assert torch.equal(out.view(torch.int16), (x.float() * K).bfloat16().view(torch.int16)), cfg
+        assert torch.equal(wb, w), cfg
+        assert buf.get_status() == 0, cfg
+        buf.destroy()
+
+
+def test_planner_tables_near_the_default_shared_memory_limit():
+    """Tables of 48,400 bytes: under 48 KB, but over 48 KB with the kernel's
+    static shared memory, so the limit must be raised explicitly (a launch
+    error before)."""
+    sh = wl.Shape("smem48", R=16, E=192, K=12, S=387, H=64, Hp=8, B=13, tp=4,
+                  weights="softmax")
+    buf, _, _ = _full_pipeline(sh, _routing(sh, "zipf", 114), 114)
+    buf.destroy()
+
+
+def test_contexts_of_different_table_sizes_coexist():
+    """The planner's shared-memory limit is per kernel and process-wide: a
+    context with smaller tables created later must not lower it under an
+    earlier context's need."""
+    big = wl.Shape("big", R=8, E=768, K=8, S=64, H=64, Hp=8, B=96, tp=8, weights="softmax")
+    mid = wl.Shape("mid", R=8, E=256, K=8, S=64, H=64, Hp=8, B=32, tp=8, weights="softmax")
+    tb, tm = _routing(big, "zipf", 5), _routing(mid, "zipf", 6)
+    bb, bm = _buffer(_cfg_of(big)), _buffer(_cfg_of(mid))
+    pb = bb.plan(torch.from_numpy(tb).cuda())
+    pm = bm.plan(torch.from_numpy(tm).cuda())
+    pb = bb.plan(torch.from_numpy(tb).cuda(), plan=pb)
+    assert bb.get_status() == 0 and bm.get_status() == 0
+    for sh, topk, p in ((big, tb, pb), (mid, tm, pm)):
+        st, op = _oracle_plan(_cfg_of(sh), topk)
+        assert st == 0 and np.array_equal(p.dst.cpu().numpy(), op["dst"])
+    bb.destroy()
+    bm.destroy()
+
+
 @pytest.mark.parametrize("K", [2, 6, 8])
 def test_tile_path_planner(K):
     """Tables too large for the single-launch planner's shared memory
