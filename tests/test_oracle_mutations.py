@@ -59,6 +59,25 @@ MUTATIONS = {
     "dispatch_no_weight_zero": ("if (w_out) w_out[g] = 0.0f;", "if (w_out) w_out[g] = w_out[g];"),
     "cu_exclusive": ("cu[(int64_t)j * EB + x] = (int32_t)end;", "cu[(int64_t)j * EB + x] = (int32_t)(end - padded);"),
     "slots_filled_from_end": ("etc[(int64_t)j * B + nslots] = e;", "etc[(int64_t)j * B + (B - 1 - nslots)] = e;"),
+    # summation orders
+    "combine_reversed_k": ("float acc = bf16_to_f32(y[decode_row(d[0]) * H + c]);\n      for (int k = 1; k < K; k++) acc = acc + bf16_to_f32(y[decode_row(d[k]) * H + c]);",
+                           "float acc = bf16_to_f32(y[decode_row(d[K - 1]) * H + c]);\n      for (int k = K - 2; k >= 0; k--) acc = acc + bf16_to_f32(y[decode_row(d[k]) * H + c]);"),
+    "combine_pairwise": ("float acc = bf16_to_f32(y[decode_row(d[0]) * H + c]);\n      for (int k = 1; k < K; k++) acc = acc + bf16_to_f32(y[decode_row(d[k]) * H + c]);",
+                         "float v[64];\n      for (int k = 0; k < K; k++) v[k] = bf16_to_f32(y[decode_row(d[k]) * H + c]);\n"
+                         "      for (int w = 1; w < K; w *= 2) for (int k = 0; k + w < K; k += 2 * w) v[k] = v[k] + v[k + w];\n"
+                         "      float acc = v[0];"),
+    "combine_fp64_accumulate": ("float acc = bf16_to_f32(y[decode_row(d[0]) * H + c]);\n      for (int k = 1; k < K; k++) acc = acc + bf16_to_f32(y[decode_row(d[k]) * H + c]);",
+                                "double acc = bf16_to_f32(y[decode_row(d[0]) * H + c]);\n      for (int k = 1; k < K; k++) acc = acc + bf16_to_f32(y[decode_row(d[k]) * H + c]);"),
+    "reduce_reversed_rank_slot": ("      for (int j = 0; j < R; j++)\n        for (int b = 0; b < B; b++)\n          if (etc[j * B + b] == e)",
+                                  "      for (int j = R - 1; j >= 0; j--)\n        for (int b = B - 1; b >= 0; b--)\n          if (etc[j * B + b] == e)"),
+    "reduce_slot_major": ("      for (int j = 0; j < R; j++)\n        for (int b = 0; b < B; b++)\n          if (etc[j * B + b] == e)",
+                          "      for (int b = 0; b < B; b++)\n        for (int j = 0; j < R; j++)\n          if (etc[j * B + b] == e)"),
+    "reduce_seed_last": ("float acc = Gh[(int64_t)e * HHp + c];\n      for (int j = 0; j < R; j++)\n        for (int b = 0; b < B; b++)\n          if (etc[j * B + b] == e) acc = acc + Gs[((int64_t)j * B + b) * HHp + c];",
+                         "float acc = 0.0f;\n      for (int j = 0; j < R; j++)\n        for (int b = 0; b < B; b++)\n          if (etc[j * B + b] == e) acc = acc + Gs[((int64_t)j * B + b) * HHp + c];\n      acc = acc + Gh[(int64_t)e * HHp + c];"),
+    "fold_reversed_duplicates": ("        for (int k2 = k + 1; k2 < K; k2++)\n          if (d[k2] < 0 && decode_row(d[k2]) / NvS == j)\n            acc = acc",
+                                 "        for (int k2 = K - 1; k2 > k; k2--)\n          if (d[k2] < 0 && decode_row(d[k2]) / NvS == j)\n            acc = acc"),
+    "primaries_combine_reversed": ("      float acc = bf16_to_f32(y[(int64_t)d[0] * H + c]);  /* route 0 is always primary */\n      for (int k = 1; k < K; k++)\n        if (d[k] >= 0)",
+                                   "      float acc = 0.0f;\n      for (int k = K - 1; k >= 0; k--)\n        if (d[k] >= 0)"),
 }
 
 CHILD = r'''
@@ -94,6 +113,12 @@ pins = [
     ("prepare_random", lambda: P.test_prepare_random_properties(o)),
     ("reduce_const", lambda: P.test_reduce_constant_fill_counts_copies(o)),
     ("reduce_int", lambda: P.test_reduce_integer_values_exact(o)),
+    ("combine_k_order", lambda: [P.test_combine_sums_in_k_order(o, v, w) for v, w in P.COMBINE_ORDER_CASES]),
+    ("combine_k_order_ranks", lambda: P.test_combine_k_order_across_ranks(o)),
+    ("fold_k_order", lambda: P.test_fold_sums_duplicates_in_k_order(o)),
+    ("fold_two_groups", lambda: P.test_fold_k_order_with_two_groups(o)),
+    ("primaries_k_order", lambda: P.test_primaries_combine_sums_in_k_order(o)),
+    ("reduce_order", lambda: [P.test_reduce_sums_in_rank_slot_order(o, *c) for c in P.REDUCE_ORDER_CASES]),
 ]
 failed = []
 for name, fn in pins:

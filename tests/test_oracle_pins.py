@@ -724,3 +724,126 @@ def test_folded_combine_error_bound(oracle_mod):
     mag = mag.reshape(sh.R * sh.S, sh.K, sh.H).sum(axis=1)
     assert np.all(np.abs(got - exact) <= 2.0 ** -7 * mag + 1e-30)
     assert np.abs(got - exact).max() > 0   # the bound is not vacuous here
+
+
+# ------------------------------------------------- summation orders
+#
+# Values chosen so that every other order of the same adds gives another
+# result: a tie at 2^20 (fp32 ulp 2^-3) or at 2^24 (ulp 2) rounds to even and
+# drops the small term only when the large one has been added first.
+
+def _f2b(v):
+    return int(np.array([v], np.float32).view(np.uint32)[0] >> 16)
+
+
+def _one_token_rows(values, ranks=None):
+    """dst and y of one token whose K routes hold `values` (bf16), route k on
+    rank ranks[k] (all on rank 0 by default), NvS = 2K rows per rank.  The
+    other ranks' tokens (S = 1) route to zero rows K..2K-1 of their rank."""
+    K = len(values)
+    ranks = ranks or [0] * K
+    R, NvS = max(ranks) + 1, 2 * K
+    dst = np.zeros((R, K), np.int32)
+    y = np.zeros((R * NvS, 1), np.uint16)
+    for r in range(1, R):
+        dst[r] = [r * NvS + K if k == 0 else -(r * NvS + K + k + 1) for k in range(K)]
+    for k, (v, j) in enumerate(zip(values, ranks)):
+        g = j * NvS + k
+        first = ranks.index(j) == k
+        dst[0, k] = g if first else -(g + 1)
+        y[g, 0] = _f2b(v)
+    return R, NvS, dst, y
+
+
+COMBINE_ORDER_CASES = [
+    # k order: (2^20 + 2^-4) ties to 2^20, then - 2^20 = 0; reversed: 2^-4
+    ([2.0 ** 20, 2.0 ** -4, -2.0 ** 20], 0.0),
+    # k order 0; pairwise (k0 + k1) + (k2 + k3) = 2^-4; reversed 2^-3 (exact)
+    ([2.0 ** 20, 2.0 ** -4, 2.0 ** -4, -2.0 ** 20], 0.0),
+    # k order: below 2^20 the fp32 ulp is 2^-4, so the six 2^-4 add exactly
+    # to -2^20 and the sum ends 0.375; reversed, each 2^-4 ties at 2^20 and
+    # is dropped (0.0); pairwise gives 0.3125
+    ([-2.0 ** 20, 2.0 ** -4, 2.0 ** -4, 2.0 ** -4, 2.0 ** -4, 2.0 ** -4, 2.0 ** -4, 2.0 ** 20],
+     0.375),
+]
+
+
+@pytest.mark.parametrize("values,want", COMBINE_ORDER_CASES)
+def test_combine_sums_in_k_order(oracle_mod, values, want):
+    """The K-sum runs in k = 0..K-1 order in fp32, starting from the k = 0
+    row, one bf16 rounding at the end [vLLM, finalize(): the unweighted sum
+    over the K routes; the k order is the method's fixed accumulation
+    order]."""
+    R, NvS, dst, y = _one_token_rows(values)
+    out, _ = oracle_mod.combine(R, 1, len(values), NvS, 1, dst, y)
+    assert oracle_mod.bf16_to_f32(out)[0, 0] == np.float32(want)
+
+
+def test_combine_k_order_across_ranks(oracle_mod):
+    """The order is the route index k, not the receiving rank: routes 0 and 2
+    on rank 1, route 1 on rank 0, rows 2^20, 2^-4, -2^20 still give 0."""
+    R, NvS, dst, y = _one_token_rows([2.0 ** 20, 2.0 ** -4, -2.0 ** 20], ranks=[1, 0, 1])
+    out, _ = oracle_mod.combine(R, 1, 3, NvS, 1, dst, y)
+    assert oracle_mod.bf16_to_f32(out)[0, 0] == 0.0
+
+
+def test_fold_sums_duplicates_in_k_order(oracle_mod):
+    """Duplicate prologue [API, Buffer.combine]: the primary (route 0) and its
+    duplicates (routes 1, 2 on the same rank) fold in k order: 2^20 + 2^-4
+    ties to 2^20, - 2^20 gives 0 (reversed duplicates would give 2^-4)."""
+    R, NvS, dst, y = _one_token_rows([2.0 ** 20, 2.0 ** -4, -2.0 ** 20])
+    yf = y.copy()
+    oracle_mod.fold_duplicates(R, 1, 3, NvS, 1, dst, yf)
+    assert yf[0, 0] == _f2b(0.0) and np.array_equal(yf[1:], y[1:])
+    out, _ = oracle_mod.combine_primaries(R, 1, 3, NvS, 1, dst, yf)
+    assert oracle_mod.bf16_to_f32(out)[0, 0] == 0.0
+
+
+def test_fold_k_order_with_two_groups(oracle_mod):
+    """Two duplicate groups of one token (ranks 0 and 1, routes interleaved
+    0,1,0,1,0): rank 0 folds routes 0, 2, 4 = 2^20, 2^-4, -2^20 -> 0; rank 1
+    folds routes 1, 3 = 2^-4, 2^-4 -> 2^-3; the primaries' sum is 2^-3."""
+    vals = [2.0 ** 20, 2.0 ** -4, 2.0 ** -4, 2.0 ** -4, -2.0 ** 20]
+    R, NvS, dst, y = _one_token_rows(vals, ranks=[0, 1, 0, 1, 0])
+    yf = y.copy()
+    oracle_mod.fold_duplicates(R, 1, 5, NvS, 1, dst, yf)
+    assert yf[0, 0] == _f2b(0.0) and yf[NvS + 1, 0] == _f2b(2.0 ** -3)
+    out, _ = oracle_mod.combine_primaries(R, 1, 5, NvS, 1, dst, yf)
+    assert oracle_mod.bf16_to_f32(out)[0, 0] == np.float32(2.0 ** -3)
+
+
+def test_primaries_combine_sums_in_k_order(oracle_mod):
+    """The deduplicated path's main combine keeps the k order over the
+    primaries: three routes on three ranks (no duplicates), rows 2^20, 2^-4,
+    -2^20 give 0 (reversed: 2^-4)."""
+    R, NvS, dst, y = _one_token_rows([2.0 ** 20, 2.0 ** -4, -2.0 ** 20], ranks=[0, 1, 2])
+    yf = y.copy()
+    oracle_mod.fold_duplicates(R, 1, 3, NvS, 1, dst, yf)
+    assert np.array_equal(yf, y)
+    out, _ = oracle_mod.combine_primaries(R, 1, 3, NvS, 1, dst, yf)
+    assert oracle_mod.bf16_to_f32(out)[0, 0] == 0.0
+
+
+REDUCE_ORDER_CASES = [
+    # one slot on each of two ranks: (2^24 + 1) ties to 2^24, - 2^24 = 0;
+    # ranks descending would give 1
+    (2, 1, [0, 0], [1.0, -2.0 ** 24], 0.0),
+    # two slots on one rank: slots ascending gives 0, descending 1
+    (1, 2, [0, 0], [1.0, -2.0 ** 24], 0.0),
+    # rank-major, not slot-major: rank 0 slots 0, 1 then rank 1 slot 0
+    # (2^24 + 1 -> 2^24, - 2^24 -> 0, + 1 -> 1); slot-major would add rank 1's
+    # slot 0 before rank 0's slot 1 and give 0
+    (2, 2, [0, 0, 0, -1], [1.0, -2.0 ** 24, 1.0, 7.0], 1.0),
+]
+
+
+@pytest.mark.parametrize("R,B,etc,gs,want", REDUCE_ORDER_CASES)
+def test_reduce_sums_in_rank_slot_order(oracle_mod, R, B, etc, gs, want):
+    """Gradient reduce [API, Buffer.reduce_grad]: the home gradient first,
+    then every slot holding the expert in ascending (rank, slot) order, fp32."""
+    etc = np.array(etc, np.int32)
+    Gh = np.array([[2.0 ** 24], [5.0]], np.float32)
+    Gs = np.array(gs, np.float32).reshape(R * B, 1)
+    oracle_mod.reduce(R, 2, B, etc, Gh, Gs, 1)
+    assert Gh[0, 0] == np.float32(want) and Gh[1, 0] == 5.0
+    assert np.all(Gs[etc >= 0] == 0)
