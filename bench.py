@@ -1,16 +1,24 @@
 #!/usr/bin/env python
 """Benchmark of the balanced expert-parallel hot path on one GB300 per process.
 
-One step = one pass of every hot-path row over one batch of synthetic input:
-plan -> dispatch (hidden + route weights) -> weight prefetch -> combine (the
-dispatched rows stand in for the expert outputs) -> plan-reuse dispatch of an
-[R, S, H] gradient -> redundant-expert gradient reduce (one projection).
-Tokens per step = R*S.  Prints one JSON line.  Beside the timed step it
-reports, on the same routing: the maxvio sweep, the decode-path preparation,
-the packed MXFP4 prefetch and the deduplicated dispatch/combine pair
-(`dedup_path`: times, bytes and the rows that would cross between ranks).
+The headline is the metric plan+dispatch+combine tokens/s on the
+DeepSeek-V3-shaped workload (R=8 ranks, E=256 experts, top-8, S=4096 tokens
+per rank, H=7168, B=32, token_padding=128) at maxvio 1.0, the largest
+configuration with a maxvio sweep and the shape of the API page's own
+Buffer(...) example.
 
-  python bench.py [--gpus N --steps K --warmup W] [--config mixtral]
+One step = one pass of every hot-path row over one batch of synthetic input:
+plan -> dispatch (hidden + route weights) -> combine (the dispatched rows
+stand in for the expert outputs) -> weight prefetch -> plan-reuse dispatch of
+an [R, S, H] gradient -> redundant-expert gradient reduce (one projection).
+CUDA events sit between the ops of every timed step; `value` = R*S tokens per
+step / the mean plan+dispatch+combine time of the timed steps (the metric),
+`whole_step` the same over the whole step.  Beside it, on the same routing:
+the maxvio sweep, the decode-path preparation, the packed MXFP4 prefetch, the
+deduplicated dispatch/combine pair (`dedup_path`), and the other workload
+shapes (`configs`: Mixtral, Kimi-K2, Qwen3 decode).
+
+  python bench.py [--gpus N --steps K --warmup W] [--config deepseek_v3]
                   [--maxvio 1.0] [--impl ours|reference]
 
 With N > 1 (torchrun), every process runs the same workload on its own GPU
@@ -47,7 +55,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="mixtral")
+    ap.add_argument("--config", default="deepseek_v3")
+    ap.add_argument("--extra-configs", default="mixtral,kimi_k2,qwen3_decode",
+                    help="comma list of other workload shapes measured after the headline "
+                         "(chain and whole step only); empty for none")
     ap.add_argument("--maxvio", default=None, help="headline routing point")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -73,7 +84,9 @@ def parse():
     args = ap.parse_args()
     if args.step_only:
         args.no_sweep = args.no_e2e = args.no_cpu_baseline = args.no_mxfp4 = True
+        args.no_dedup = True
         args.graph = False
+        args.extra_configs = ""
     return args
 
 
@@ -207,16 +220,16 @@ class Step:
         b.dispatch(self.hidden, self.w_sk, plan=self.plan, out=self.hid_nvsh,
                    weights_out=self.w_nvs)
         rec(2)
-        b.prefetch_weight(self.plan, self.W)
-        rec(3)
         b.combine(self.plan, self.hid_nvsh, self.w_nvs, out=self.out, weights_out=self.w_back)
+        rec(3)
+        b.prefetch_weight(self.plan, self.W)
         rec(4)
         b.dispatch(self.grad, plan=self.plan, out=self.grad_nvsh)
         rec(5)
         b.reduce_grad(self.plan, [self.Gh], [self.Gs])
         rec(6)
 
-    LAUNCHES_PER_STEP = 6  # plan (one cooperative launch), dispatch, prefetch, combine, dispatch, reduce
+    LAUNCHES_PER_STEP = 6  # plan (one cooperative launch), dispatch, combine, prefetch, dispatch, reduce
 
     def algorithmic_bytes(self):
         """Bytes each op must move (reads + writes), per launch."""
@@ -240,39 +253,30 @@ class Step:
         }, {"P": P, "U": U, "D": D}
 
 
-OPS = ["plan", "dispatch", "prefetch", "combine", "grad_dispatch", "reduce"]
+OPS = ["plan", "dispatch", "combine", "prefetch", "grad_dispatch", "reduce"]
+CHAIN = ("plan", "dispatch", "combine")  # the metric's ops, the first three of a step
 
 
 def timed_steps(step, steps, torch, dist=None):
-    """Run `steps` steps with events only around the whole region (the ops of
-    a step overlap their launches as in real use), then up to 50 more with
-    events between the ops for the per-op split (those events keep the ops
-    from overlapping, so the split adds up to a little more than a step).
-    Returns (total_ms of the first pass, per-op ms lists, host times of the
-    first pass)."""
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+    """Run `steps` steps with CUDA events between the ops of every step.
+    Returns (ms from the first step's start to the last step's end, per-op ms
+    lists, per-step plan+dispatch+combine ms list, host times of the region)."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    start.record()
-    for _ in range(steps):
-        step.run()
-    end.record()
+    for i in range(steps):
+        step.run(evs[i])
     torch.cuda.synchronize()
     t1 = time.time()
     if dist is not None:
         dist.barrier()
-    total = start.elapsed_time(end)
-    n2 = min(steps, 50)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n2)]
-    for i in range(n2):
-        step.run(evs[i])
-    torch.cuda.synchronize()
-    per_op = {op: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n2)]
+    total = evs[0][0].elapsed_time(evs[-1][6])
+    per_op = {op: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)]
               for j, op in enumerate(OPS)}
-    return total, per_op, (t0, t1)
+    chain = [evs[i][0].elapsed_time(evs[i][3]) for i in range(steps)]
+    return total, per_op, chain, (t0, t1)
 
 
 def time_chain(step, n, torch, graph=False):
@@ -470,12 +474,13 @@ def run_prepare(buf, sh, steps, torch):
 
 
 def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
-    """The same step through the public API with inputs in pinned host memory:
-    every step copies its inputs host->device and reads the combined result
-    (and the gathered route weights) back.  Copies run on their own streams,
-    double-buffered, so step i's compute overlaps step i+1's inputs and step
-    i-1's result; the timed region spans the first input copy to the last
-    result copy."""
+    """The metric's plan -> dispatch -> combine through the public API with
+    the inputs in pinned host memory: every step copies its inputs (top-k ids,
+    tokens_per_expert, hidden rows, route weights) host->device and reads the
+    combined rows and the gathered route weights back.  Copies run on their
+    own streams, double-buffered, so step i's compute overlaps step i+1's
+    inputs and step i-1's result; the timed region spans the first input copy
+    to the last result copy."""
     from combine_moonep_plan_gb300 import workloads as wl
     R, S, K, E, H = sh.R, sh.S, sh.K, sh.E, sh.H
     g = torch.Generator().manual_seed(seed)
@@ -484,12 +489,14 @@ def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
         "tpe": torch.from_numpy(wl.tokens_per_expert(topk_np, E)).pin_memory(),
         "hidden": torch.randn((R, S, H), generator=g).to(torch.bfloat16).pin_memory(),
         "w_sk": torch.from_numpy(wl.route_weights(sh, seed)).pin_memory(),
-        "grad": torch.randn((R, S, H), generator=g).to(torch.bfloat16).pin_memory(),
     }
     h_out = [{"out": torch.empty((R, S, H), dtype=torch.bfloat16, pin_memory=True),
               "w_back": torch.empty((R, S, K), dtype=torch.float32, pin_memory=True)}
              for _ in range(2)]
-    st = Step(buf, sh, topk_np, seed, torch)
+    NvS = buf.NvS
+    plan = buf.new_plan()
+    hid_nvsh = torch.empty((R * NvS, H), dtype=torch.bfloat16, device="cuda")
+    w_nvs = torch.empty((R * NvS,), dtype=torch.float32, device="cuda")
     sets = []
     for _ in range(2):
         sets.append({k: torch.empty_like(v, device="cuda") for k, v in h_in.items()} |
@@ -526,10 +533,9 @@ def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
                 compute.wait_event(inputs_ready[b])
                 if used[b]:
                     compute.wait_event(read_back[b])  # step i-2's result has been read
-                st.topk, st.tpe, st.hidden, st.w_sk, st.grad = (d["topk"], d["tpe"], d["hidden"],
-                                                                 d["w_sk"], d["grad"])
-                st.out, st.w_back = d["out"], d["w_back"]
-                st.run()
+                buf.plan(d["topk"], d["tpe"], plan=plan)
+                buf.dispatch(d["hidden"], d["w_sk"], plan=plan, out=hid_nvsh, weights_out=w_nvs)
+                buf.combine(plan, hid_nvsh, w_nvs, out=d["out"], weights_out=d["w_back"])
                 compute.record_event(computed[b])
             with torch.cuda.stream(d2h):
                 d2h.wait_event(computed[b])
@@ -544,90 +550,96 @@ def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
 
     run(6, False)  # warm-up: host copies and kernels
     ms = max_over_ranks(run(steps, True), dist)
-    del st
+    del hid_nvsh, w_nvs, sets, plan
+    torch.cuda.empty_cache()
     return ms / steps, bi, bo
 
 
-def cpu_baseline(sh, topk_np, seed, cols=None, hh_cols=None, repeats=1):
-    """The oracle, single-threaded on the host, over all tokens and a column
-    sample of every row; times scaled to full rows."""
-    import oracle
-    from combine_moonep_plan_gb300 import workloads as wl
-    R, S, K, E, H, B, Hp, tp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.Hp, sh.tp
-    Hs = min(H, cols or 256)
-    HHp = H * Hp
-    HHs = min(HHp, hh_cols or (1 << 16))
-    x = wl.hidden_bf16(sh, seed, rows=R * S, cols=Hs)
-    w = wl.route_weights(sh, seed)
-    gr = wl.hidden_bf16(sh, seed + 1, rows=R * S, cols=Hs)
-    tpe = wl.tokens_per_expert(topk_np, E)
-    rng = np.random.default_rng(seed)
-    W = rng.integers(0, 65535, (E + R * B, HHs), dtype=np.uint16)
-    Gh = rng.standard_normal((E, HHs), dtype=np.float32)
-    Gs = rng.standard_normal((R * B, HHs), dtype=np.float32)
-    t = {op: 0.0 for op in OPS}
-    for _ in range(repeats):
+class OracleChain:
+    """The oracle's plan -> dispatch -> combine on the whole workload (every
+    token, every hidden column), single-threaded on the host, with its
+    output buffers allocated once and reused like a framework's."""
+
+    def __init__(self, sh, topk_np, seed):
+        from combine_moonep_plan_gb300 import workloads as wl
+        self.sh = sh
+        self.topk = topk_np
+        self.tpe = wl.tokens_per_expert(topk_np, sh.E)
+        self.x = wl.hidden_bf16(sh, seed)
+        self.w = wl.route_weights(sh, seed)
+        NvS = sh.NvS
+        self.hid = np.zeros((sh.R * NvS, sh.H), np.uint16)
+        self.wn = np.zeros(sh.R * NvS, np.float32)
+
+    def step(self):
+        """One pass; returns the seconds of plan, dispatch and combine."""
+        import oracle
+        sh = self.sh
+        R, S, K, E, H, B, tp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.tp
         a = time.perf_counter()
-        st, p = oracle.plan(R, E, K, S, B, tp, topk_np, tpe, dup_records=False)
+        st, p = oracle.plan(R, E, K, S, B, tp, self.topk, self.tpe, dup_records=False)
         b = time.perf_counter()
+        if st != 0:
+            raise RuntimeError(f"oracle plan status {st}")
         NvS = p["NvS"]
-        hid = np.zeros((R * NvS, Hs), np.uint16)
-        wn = np.zeros(R * NvS, np.float32)
-        oracle.dispatch(R, S, K, E, B, NvS, Hs, p["dst"], p["zero_fill_ranges"], x, w, hid, wn)
+        oracle.dispatch(R, S, K, E, B, NvS, H, p["dst"], p["zero_fill_ranges"], self.x, self.w,
+                        self.hid, self.wn)
         c = time.perf_counter()
-        oracle.prefetch(R, E, B, p["experts_to_copy"], W, HHs)
+        oracle.combine(R, S, K, NvS, H, p["dst"], self.hid, self.wn)
         d = time.perf_counter()
-        oracle.combine(R, S, K, NvS, Hs, p["dst"], hid, wn)
-        e = time.perf_counter()
-        gh = np.zeros((R * NvS, Hs), np.uint16)
-        oracle.dispatch(R, S, K, E, B, NvS, Hs, p["dst"], p["zero_fill_ranges"], gr, None, gh)
-        f = time.perf_counter()
-        oracle.reduce(R, E, B, p["experts_to_copy"], Gh, Gs, HHs)
-        g = time.perf_counter()
-        t["plan"] += b - a
-        t["dispatch"] += (c - b) * H / Hs
-        t["prefetch"] += (d - c) * HHp / HHs
-        t["combine"] += (e - d) * H / Hs
-        t["grad_dispatch"] += (f - e) * H / Hs
-        t["reduce"] += (g - f) * HHp / HHs
-    for op in t:
-        t[op] /= repeats
-    step_s = sum(t.values())
-    sample = (f"all {R * S} tokens and the full plan; hidden columns [0,{Hs}) of {H}; "
-              f"weight/grad columns [0,{HHs}) of {HHp}; times scaled to full rows")
-    return R * S / step_s, step_s, t, sample
+        return {"plan": b - a, "dispatch": c - b, "combine": d - c}
+
+    SAMPLE = "the whole workload: every token, every hidden column (plan, dispatch, combine)"
+
+
+def cpu_baseline(sh, topk_np, seed, budget_s=15.0):
+    """The oracle timed on the host: one untimed pass (first touch of its
+    buffers), then passes until about budget_s seconds of oracle work."""
+    t0 = time.perf_counter()
+    ch = OracleChain(sh, topk_np, seed)
+    ch.step()
+    times = []
+    a = time.perf_counter()
+    while not times or time.perf_counter() - a < budget_s:
+        times.append(ch.step())
+        if len(times) >= 50:
+            break
+    per = {op: statistics.mean(t[op] for t in times) for op in CHAIN}
+    step_s = sum(per.values())
+    return {"value": R_S(sh) / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{OracleChain.SAMPLE}; mean of {len(times)} passes after one untimed",
+            "step_s": round(step_s, 4), "op_s": {k: round(v, 4) for k, v in per.items()},
+            "wall_s": round(time.perf_counter() - t0, 2), "host": host_info()}
 
 
 def reference_arm(args, sh, point, topk_np, seed, dist):
-    """The oracle as the reference arm: each step a column sample of the workload."""
+    """The oracle as the reference arm: each step is one oracle pass of the
+    metric's plan -> dispatch -> combine over the whole workload; ms_per_step
+    is its wall time."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
     steps, warm = args.steps, args.warmup
-    # size the per-step column sample so the whole run stays near 3 minutes
-    cols, hh = 64, 1 << 16
-    a = time.perf_counter()
-    cpu_baseline(sh, topk_np, seed, cols, hh)
-    est = (time.perf_counter() - a) * (steps + warm)
-    if est > 180.0:
-        scale = max(180.0 / est, 1.0 / 8)
-        cols, hh = max(8, int(cols * scale)), max(1 << 12, int(hh * scale))
+    t0 = time.perf_counter()
+    ch = OracleChain(sh, topk_np, seed)
     for _ in range(warm):
-        cpu_baseline(sh, topk_np, seed, cols, hh)
+        ch.step()
     a = time.perf_counter()
-    tot = 0.0
+    per = {op: 0.0 for op in CHAIN}
     for _ in range(steps):
-        v, step_s, per, sample = cpu_baseline(sh, topk_np, seed, cols, hh)
-        tot += step_s
+        for op, v in ch.step().items():
+            per[op] += v
     wall = time.perf_counter() - a
-    value = R_S(sh) * steps / tot
+    value = R_S(sh) * steps / wall
     return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * tot / steps,
+            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * wall / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "impl": "reference",
             "config": workload_config(sh, point),
+            "op_ms": {op: round(1e3 * v / steps, 2) for op, v in per.items()},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": sample, "wall_s": wall, "host": host_info()},
+                             "sample": OracleChain.SAMPLE + "; every timed step one full pass",
+                             "wall_s": round(time.perf_counter() - t0, 2), "host": host_info()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -686,7 +698,8 @@ def workload_config(sh, point):
                         f"{point_label(point)}",
             "R": sh.R, "E": sh.E, "K": sh.K, "S": sh.S, "H": sh.H, "H_prime": sh.Hp, "B": sh.B,
             "token_padding": sh.tp, "maxvio_point": point_label(point), "n_proj": 1,
-            "step": "plan -> dispatch(+weights) -> prefetch -> combine(+weights) -> "
+            "metric_ops": "plan -> dispatch(+weights) -> combine(+weights)",
+            "step": "plan -> dispatch(+weights) -> combine(+weights) -> prefetch -> "
                     "plan-reuse grad dispatch -> grad reduce",
             "l2": "inputs larger than L2 (no flush): every step moves several GB",
             "dup_records": False, "global_batch": sh.R * sh.S}
@@ -757,6 +770,85 @@ def profile_ops(args, sh, point, seed):
           flush=True)
 
 
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = {}
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                peaks = json.load(f)
+        except Exception:
+            peaks = {}
+    if "hbm_gbs" in peaks:
+        return float(peaks["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def summarise(step, sh, total_ms, per_op, chain, steps, peak, world=1):
+    """Per-op times and rates, the metric's chain and the whole step."""
+    alg, counts = step.algorithmic_bytes()
+    op_ms = {op: statistics.mean(v) for op, v in per_op.items()}
+    chain_ms = statistics.mean(chain)
+    ops = {o: {"ms": round(op_ms[o], 5), "GB": round(alg[o] / 1e9, 4),
+               "GBps": round(alg[o] / (op_ms[o] / 1e3) / 1e9, 1) if op_ms[o] > 0 else None,
+               "frac_of_peak": round(alg[o] / (op_ms[o] / 1e3) / 1e9 / peak, 4)
+               if op_ms[o] > 0 else None,
+               "ms_p10_p50_p90": [round(float(np.percentile(per_op[o], q)), 5)
+                                  for q in (10, 50, 90)]} for o in OPS}
+    tokens = R_S(sh) * world
+    return {
+        "chain_ms": chain_ms, "tokens_per_s": tokens / (chain_ms / 1e3),
+        "chain_ms_p10_p50_p90": [round(float(np.percentile(chain, q)), 5) for q in (10, 50, 90)],
+        "chain_hbm_GBps": sum(alg[o] for o in CHAIN) / (chain_ms / 1e3) / 1e9,
+        "whole_step": {"ms_per_step": total_ms / steps,
+                       "tokens_per_s": tokens / (total_ms / steps / 1e3),
+                       "hbm_GBps": sum(alg.values()) / (total_ms / steps / 1e3) / 1e9},
+        "plan_frac_of_dispatch": op_ms["plan"] / op_ms["dispatch"],
+        "ops": ops, "plan_counts": counts, "op_ms": op_ms, "alg": alg,
+    }
+
+
+def roofline_entry(op, summ, peak, peak_src, config_name):
+    achieved = summ["alg"][op] / (summ["op_ms"][op] / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": op, "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
+            "bytes_per_launch": summ["alg"][op], "ms_per_launch": round(summ["op_ms"][op], 5),
+            "traffic": recorded_traffic(op, config_name)}
+
+
+def measure_config(name, args, torch, peak, seed_idx=0, steps=None):
+    """The step on another workload shape at its headline routing point:
+    the metric's chain and the whole step, nothing else."""
+    from combine_moonep_plan_gb300 import workloads as wl
+    from combine_moonep_plan_gb300.api import Buffer
+    sh = wl.SHAPES[name]
+    point = HEADLINE[name]
+    seed = wl.seed_for(name, seed_idx)
+    topk_np, info = make_routing(sh, point, seed)
+    buf = Buffer(S=sh.S, H=sh.H, K=sh.K, E=sh.E, num_ep_ranks=sh.R, B=sh.B,
+                 token_padding=sh.tp, zero_copy_views=False)
+    step = Step(buf, sh, topk_np, seed, torch)
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    n = steps or max(args.steps, 20)
+    total, per_op, chain, _ = timed_steps(step, n, torch, None)
+    summ = summarise(step, sh, total, per_op, chain, n, peak)
+    status = buf.get_status()
+    out = {"workload": workload_config(sh, point)["workload"], "maxvio": round(info["maxvio"], 4),
+           "plan_dispatch_combine_tokens_per_s": summ["tokens_per_s"],
+           "chain_ms": round(summ["chain_ms"], 5),
+           "plan_us": round(1e3 * summ["op_ms"]["plan"], 2),
+           "plan_frac_of_dispatch": round(summ["plan_frac_of_dispatch"], 4),
+           "dispatch_frac_of_peak": summ["ops"]["dispatch"]["frac_of_peak"],
+           "combine_frac_of_peak": summ["ops"]["combine"]["frac_of_peak"],
+           "whole_step": summ["whole_step"], "ops": summ["ops"], "steps": n,
+           "device_status": status}
+    del step
+    buf.destroy()
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -805,11 +897,12 @@ def main():
     status = buf.get_status()
     if status != 0:
         raise SystemExit(f"device status {status} during warm-up")
+    peak, peak_src = load_peaks()
 
     graph_ms = None
     if args.graph:
-        # plan -> dispatch -> prefetch -> combine -> grad dispatch -> reduce as
-        # one CUDA graph (the decode-sized case is launch-latency bound)
+        # the whole step as one CUDA graph (the decode-sized case is
+        # launch-latency bound)
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
@@ -832,39 +925,22 @@ def main():
 
     sampler = ClockSampler(local)
     time.sleep(0.3)
-    total_ms, per_op, (t0, t1) = timed_steps(step, args.steps, torch, dist)
+    total_ms, per_op, chain, (t0, t1) = timed_steps(step, args.steps, torch, dist)
     time.sleep(0.25)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
-    total_ms = max_over_ranks(total_ms, dist)
-    ms_per_step = total_ms / args.steps
-    alg, counts = step.algorithmic_bytes()
-    op_ms = {op: statistics.mean(v) for op, v in per_op.items()}
+    summ = summarise(step, sh, total_ms, per_op, chain, args.steps, peak, world)
+    chain_ms = max_over_ranks(summ["chain_ms"], dist)
     tokens = R_S(sh) * world
-    value = tokens / (ms_per_step / 1e3)
-    pdc_ms = op_ms["plan"] + op_ms["dispatch"] + op_ms["combine"]
-
-    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) if os.path.exists(
-            os.path.join(ROOT, "MEASURED_PEAKS.json")) else open(os.devnull) as f:
-        try:
-            peaks = json.load(f)
-        except Exception:
-            peaks = {}
-    peak = peaks.get("hbm_gbs", 6800.0)
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    dom = max((o for o in OPS if o != "plan"), key=lambda o: op_ms[o])
-    achieved = alg[dom] / (op_ms[dom] / 1e3) / 1e9
-    ops = {o: {"ms": round(op_ms[o], 5), "GB": round(alg[o] / 1e9, 4),
-               "GBps": round(alg[o] / (op_ms[o] / 1e3) / 1e9, 1) if op_ms[o] > 0 else None,
-               "frac_of_peak": round(alg[o] / (op_ms[o] / 1e3) / 1e9 / peak, 4)
-               if op_ms[o] > 0 else None,
-               "ms_p10_p50_p90": [round(float(np.percentile(per_op[o], q)), 5)
-                                  for q in (10, 50, 90)]} for o in OPS}
-    chain_ms = (time_chain(step, max(20, min(args.steps, 200)), torch)
-                if not args.step_only else None)
+    value = tokens / (chain_ms / 1e3)
+    # the dominant kernel of the metric's chain, and both graded copy ops
+    dom = max(("dispatch", "combine"), key=lambda o: summ["op_ms"][o])
+    roof = roofline_entry(dom, summ, peak, peak_src, sh.name)
+    roof_ops = {o: roofline_entry(o, summ, peak, peak_src, sh.name) for o in ("dispatch", "combine")}
+    back_to_back_ms = (time_chain(step, max(20, min(args.steps, 200)), torch)
+                       if not args.step_only else None)
     chain_graph_ms = (time_chain(step, max(20, min(args.steps, 200)), torch, graph=True)
                       if args.graph else None)
-    step_bytes = sum(alg.values())
 
     sweep = []
     if not args.no_sweep:
@@ -873,78 +949,77 @@ def main():
             s2 = Step(buf, sh, tk, seed, torch)
             for _ in range(3):
                 s2.run()
-            tot2, po2, _ = timed_steps(s2, args.sweep_steps, torch, None)
-            a2, c2 = s2.algorithmic_bytes()
-            m2 = {o: statistics.mean(v) for o, v in po2.items()}
-            pdc2 = m2["plan"] + m2["dispatch"] + m2["combine"]
+            tot2, po2, ch2, _ = timed_steps(s2, args.sweep_steps, torch, None)
+            m = summarise(s2, sh, tot2, po2, ch2, args.sweep_steps, peak)
             sweep.append({
                 "maxvio_point": point_label(p), "maxvio": round(info["maxvio"], 4),
-                "step_tokens_per_s": R_S(sh) / (tot2 / args.sweep_steps / 1e3),
-                "plan_dispatch_combine_tokens_per_s": R_S(sh) / (pdc2 / 1e3),
-                "plan_us": round(1e3 * m2["plan"], 2),
-                "dispatch_GBps": round(a2["dispatch"] / (m2["dispatch"] / 1e3) / 1e9, 1),
-                "combine_GBps": round(a2["combine"] / (m2["combine"] / 1e3) / 1e9, 1),
-                "plan_frac_of_dispatch": round(m2["plan"] / m2["dispatch"], 4),
-                "padding_rows": c2["P"], "slots_used": c2["U"]})
+                "plan_dispatch_combine_tokens_per_s": m["tokens_per_s"],
+                "chain_hbm_GBps": round(m["chain_hbm_GBps"], 1),
+                "chain_frac_of_peak": round(m["chain_hbm_GBps"] / peak, 4),
+                "step_tokens_per_s": m["whole_step"]["tokens_per_s"],
+                "plan_us": round(1e3 * m["op_ms"]["plan"], 2),
+                "dispatch_GBps": m["ops"]["dispatch"]["GBps"],
+                "combine_GBps": m["ops"]["combine"]["GBps"],
+                "dispatch_frac_of_peak": m["ops"]["dispatch"]["frac_of_peak"],
+                "combine_frac_of_peak": m["ops"]["combine"]["frac_of_peak"],
+                "plan_frac_of_dispatch": round(m["plan_frac_of_dispatch"], 4),
+                "padding_rows": m["plan_counts"]["P"], "slots_used": m["plan_counts"]["U"]})
             del s2
         torch.cuda.synchronize()
 
     prep = run_prepare(buf, sh, 20, torch) if not args.step_only else None
     dedup = (run_dedup(sh, step, max(10, min(args.steps, 50)), torch, peak)
-             if not args.step_only and not args.no_dedup else None)
-
+             if not args.no_dedup else None)
     mxfp4 = None
     if not args.no_mxfp4:
         mxfp4 = run_mxfp4_prefetch(buf, step, sh, max(10, min(args.steps, 50)), torch, peak)
+
+    # free the headline step before the end-to-end and the other shapes
+    step_counts = summ["plan_counts"]
+    del step
+    torch.cuda.empty_cache()
 
     e2e = None
     if not args.no_e2e:
         ms_e2e, bi, bo = run_e2e(buf, sh, topk_np, seed, args.e2e_steps, torch, dist)
         e2e = {"value": tokens / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": args.e2e_steps}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": args.e2e_steps,
+               "ops": "plan -> dispatch -> combine through api.Buffer, inputs copied in and "
+                      "the combined rows and route weights read back every step"}
+    status = buf.get_status()
+    buf.destroy()
+    torch.cuda.empty_cache()
+
+    configs = {}
+    for name in [c for c in args.extra_configs.split(",") if c and c != args.config]:
+        configs[name] = measure_config(name, args, torch, peak)
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0:
-        # the cost of one repeat (input generation excluded: one call with 3
-        # repeats minus one with 1), then as many repeats as fit in about 15 s
-        # of oracle work
-        a0 = time.perf_counter()
-        cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20)
-        t1 = time.perf_counter() - a0
-        a0 = time.perf_counter()
-        cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20, repeats=3)
-        t3 = time.perf_counter() - a0
-        per_rep = max((t3 - t1) / 2, 1e-3)
-        reps = int(min(400, max(1, 15.0 / per_rep)))
-        a0 = time.perf_counter()
-        v, step_s, per, sample = cpu_baseline(sh, topk_np, seed, cols=512, hh_cols=1 << 20,
-                                              repeats=reps)
-        wall = time.perf_counter() - a0
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{sample}; mean of {reps} repeats", "step_s": step_s,
-               "wall_s": round(t1 + t3 + wall, 2), "host": host_info()}
+        cpu = cpu_baseline(sh, topk_np, seed)
 
-    status = buf.get_status()
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": chain_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": workload_config(sh, point),
         "routing": {k: v for k, v in rinfo.items() if k != "hot"},
-        "plan_dispatch_combine_tokens_per_s": R_S(sh) * world / (pdc_ms / 1e3),
-        "plan_dispatch_combine_chain": {
-            "ms": round(chain_ms, 5), "tokens_per_s": R_S(sh) * world / (chain_ms / 1e3),
-            "graph_ms": round(chain_graph_ms, 5) if chain_graph_ms else None} if chain_ms else None,
-        "plan_frac_of_dispatch": op_ms["plan"] / op_ms["dispatch"],
-        "step_hbm_GBps": step_bytes / (ms_per_step / 1e3) / 1e9,
-        "ops": ops, "plan_counts": counts,
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": peak_src, "traffic": recorded_traffic(dom, sh.name)},
+        "plan_frac_of_dispatch": summ["plan_frac_of_dispatch"],
+        "chain_hbm_GBps": summ["chain_hbm_GBps"],
+        "chain_frac_of_peak": summ["chain_hbm_GBps"] / peak,
+        "chain_ms_p10_p50_p90": summ["chain_ms_p10_p50_p90"],
+        "whole_step": summ["whole_step"],
+        "back_to_back_chain": {
+            "ms": round(back_to_back_ms, 5), "tokens_per_s": tokens / (back_to_back_ms / 1e3),
+            "graph_ms": round(chain_graph_ms, 5) if chain_graph_ms else None,
+            "note": "plan -> dispatch -> combine issued back to back with no event between "
+                    "the ops"} if back_to_back_ms else None,
+        "ops": summ["ops"], "plan_counts": step_counts,
+        "roofline": roof, "roofline_ops": roof_ops,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
-        "clocks": clocks, "sweep": sweep, "mxfp4_prefetch": mxfp4, "decode_prepare": prep,
-        "dedup_path": dedup,
+        "clocks": clocks, "sweep": sweep, "configs": configs, "mxfp4_prefetch": mxfp4,
+        "decode_prepare": prep, "dedup_path": dedup,
         "device_status": status,
     }
     if graph_ms is not None:

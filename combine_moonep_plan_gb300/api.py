@@ -358,42 +358,55 @@ class Buffer:
 
 
 class BufferPool:
-    """Buffers at power-of-two token capacities, created on first use
-    [vLLM MoonEPBufferPool].  A Buffer fixes its capacity S, so one
-    full-capacity buffer would pad every step to max_tokens_per_rank; the
-    pool serves the smallest power of two that holds the step's token count
-    (at least min_tokens, at most max_tokens_per_rank).  Every caller that
-    must agree on the buffer (all ranks of a step) passes the same count."""
+    """Decode-step Buffers at a few token capacities, made on first use.
+
+    A Buffer's token capacity S is fixed at creation and every step pads its
+    batch up to it, so a single buffer sized for the largest batch makes a
+    small decode step pay for the largest one.  The pool maps a step's token
+    count to a capacity by the vLLM integration's rule (MoonEPBufferPool: the
+    smallest power of two that holds the tokens, kept within [min_tokens,
+    max_tokens_per_rank]) and keeps one Buffer per capacity it has served, so
+    the number of distinct buffers grows with log2(max / min) at most.  Every
+    rank of a step must ask with the same token count, so that they agree on
+    the capacity.  A count above max_tokens_per_rank is refused by get(): no
+    buffer could hold that batch."""
 
     def __init__(self, max_tokens_per_rank: int, min_tokens: int = 1, **buffer_kwargs):
-        if max_tokens_per_rank < 1 or min_tokens < 1:
-            raise ValueError("max_tokens_per_rank and min_tokens must be >= 1")
-        buffer_kwargs.pop("S", None)
+        if not 1 <= min_tokens <= max_tokens_per_rank:
+            raise ValueError("need 1 <= min_tokens <= max_tokens_per_rank")
+        if "S" in buffer_kwargs:
+            raise ValueError("the pool chooses S; pass the other Buffer arguments only")
         self.max_tokens_per_rank = max_tokens_per_rank
         self.min_tokens = min_tokens
-        self._kwargs = buffer_kwargs
-        self._buffers: dict[int, Buffer] = {}
+        self._buffer_kwargs = dict(buffer_kwargs)
+        self._by_capacity: dict[int, Buffer] = {}
 
     def capacity_for(self, num_tokens: int) -> int:
-        if num_tokens >= self.max_tokens_per_rank:
-            return self.max_tokens_per_rank
-        cap = 1 << max(num_tokens - 1, 0).bit_length()
-        return min(max(cap, self.min_tokens), self.max_tokens_per_rank)
+        """The rule alone: smallest power of two >= num_tokens, clamped to
+        [min_tokens, max_tokens_per_rank]."""
+        p = 1
+        while p < num_tokens:
+            p <<= 1
+        return min(max(p, self.min_tokens), self.max_tokens_per_rank)
 
     def get(self, num_tokens: int) -> tuple[int, Buffer]:
-        """(capacity, buffer) for a step of num_tokens tokens per rank."""
+        """(capacity, Buffer of that capacity) for a step of num_tokens tokens
+        per rank; the Buffer is created the first time its capacity is used."""
+        if num_tokens < 0 or num_tokens > self.max_tokens_per_rank:
+            raise ValueError(f"{num_tokens} tokens per rank: outside [0, "
+                             f"{self.max_tokens_per_rank}]")
         cap = self.capacity_for(num_tokens)
-        buf = self._buffers.get(cap)
-        if buf is None:
-            buf = Buffer(S=cap, **self._kwargs)
-            self._buffers[cap] = buf
-        return cap, buf
+        if cap not in self._by_capacity:
+            self._by_capacity[cap] = Buffer(S=cap, **self._buffer_kwargs)
+        return cap, self._by_capacity[cap]
 
     @property
     def capacities(self) -> list[int]:
-        return sorted(self._buffers)
+        """Capacities that have a Buffer, ascending."""
+        return sorted(self._by_capacity)
 
     def destroy(self) -> None:
-        for buf in self._buffers.values():
+        """Destroy every Buffer the pool made; the pool can be used again."""
+        while self._by_capacity:
+            _, buf = self._by_capacity.popitem()
             buf.destroy()
-        self._buffers.clear()

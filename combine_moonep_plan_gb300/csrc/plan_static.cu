@@ -25,13 +25,16 @@ __device__ __align__(256) int32_t g_plan_scratch[kNoAllocScratchWords];
 constexpr int kMaxDevices = 256;
 std::mutex g_setup_mu;
 int32_t *g_scratch_addr[kMaxDevices];  // device address of g_plan_scratch, per device
-int g_scratch_E[kMaxDevices];          // largest E the kernels were configured for
 
 int64_t round_words(int64_t w) { return (w + 63) / 64 * 64; }
 
 // Once per device, with that device current: the device address of the
 // scratch array (the host-side symbol is only a stand-in, not a device
-// address) and the planner kernels' shared-memory limits.
+// address).  On every call: the planner kernels' shared-memory limits for
+// this (R, E, B).  Their tables grow with E*R and with B, not with E alone,
+// so a limit set for an earlier shape may be too low for this one;
+// plan_configure only raises a limit (never lowers it, other shapes share the
+// kernels) and returns at once when it is already high enough.
 int setup(int device, int R, int E, int B, int32_t **scratch) {
   if (device < 0 || device >= kMaxDevices) return MOONEP_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_setup_mu);
@@ -44,12 +47,9 @@ int setup(int device, int R, int E, int B, int32_t **scratch) {
     }
     g_scratch_addr[device] = static_cast<int32_t *>(ptr);
   }
-  if (E > g_scratch_E[device]) {
-    if (plan_configure(R, E, B) != cudaSuccess) {
-      cudaGetLastError();
-      return MOONEP_ERR_CUDA;
-    }
-    g_scratch_E[device] = E;
+  if (plan_configure(R, E, B) != cudaSuccess) {
+    cudaGetLastError();
+    return MOONEP_ERR_CUDA;
   }
   *scratch = g_scratch_addr[device];
   return MOONEP_OK;

@@ -192,8 +192,9 @@ int moonep_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
  * the process exits; configurations whose tables do not fit (roughly
  * E*R*ceil(S*K/2048) + R*S*K + a few tables of E+B words) are rejected with
  * MOONEP_ERR_INVALID_ARG.  The first call on a device looks up that array's
- * device address and sets kernel attributes, so make it before any stream
- * capture.  All calls share the array and a call overwrites what the last
+ * device address, and the first call for each new (R, E, B) raises the
+ * planner kernels' shared-memory limits, so make those calls before any
+ * stream capture.  All calls share the array and a call overwrites what the last
  * one left there: calls that overlap on the GPU (on different streams, or
  * from several host threads without ordering) race and give wrong plans.
  * The plan it produces feeds no other entry point (they take a

@@ -303,3 +303,52 @@ def test_full_size_other_top_k(R, E, K, S, B, H):
     assert torch.equal(out.view(torch.int16), (x.float() * K).to(torch.bfloat16).view(torch.int16))
     buf.destroy()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,point", [("deepseek_v3", 1.0), ("kimi_k2", "hot30")])
+def test_full_size_plan_reuse_dispatch(name, point):
+    """Combine-backward dispatch at full size, launched as bench.py launches
+    it: a bf16 [R, S, H] gradient dispatched with a clone of the forward plan
+    and no weights [API, Buffer.dispatch with a saved plan].  Every row of
+    every rank is compared with the oracle's dispatch on two column windows
+    (the first and last 64 columns: dispatch moves columns independently);
+    tail rows keep their poison in full; the forward's route weights are
+    left as they were."""
+    from combine_moonep_plan_gb300.api import Buffer
+    sh = wl.SHAPES[name]
+    R, S, K, E, H, B, tp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.tp
+    seed = wl.seed_for(name, 11)
+    topk = _routing(sh, point, seed)
+    st, op = oracle.plan(R, E, K, S, B, tp, topk, None, dup_records=False)
+    assert st == 0
+    NvS = op["NvS"]
+    buf = Buffer(S=S, H=H, K=K, E=E, num_ep_ranks=R, B=B, token_padding=tp,
+                 zero_copy_views=False)
+    dev = "cuda"
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    x = torch.randn((R, S, H), generator=gen, device=dev).to(torch.bfloat16)
+    w = torch.from_numpy(wl.route_weights(sh, seed)).to(dev)
+    hid, wn, _, plan = buf.dispatch(x, w, torch.from_numpy(topk).to(dev))
+    saved = plan.clone()
+    del hid
+    torch.cuda.synchronize()
+    wn0 = wn.clone()
+    grad = torch.randn((R, S, H), generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.full((R * NvS, H), float("nan"), dtype=torch.bfloat16, device=dev)
+    nan_bits = int(out[0, 0].view(torch.int16).item())
+    buf.dispatch(grad, plan=saved, out=out)
+    assert buf.get_status() == 0
+    assert torch.equal(wn.view(torch.int32), wn0.view(torch.int32))
+    ends = op["cu_seqlens"][:, -1]
+    for c0 in (0, H - 64):
+        gcols = _bits(grad.reshape(R * S, H)[:, c0:c0 + 64].contiguous())
+        want = oracle.dispatch(R, S, K, E, B, NvS, 64, op["dst"], op["zero_fill_ranges"], gcols)
+        got = _bits(out[:, c0:c0 + 64].contiguous())
+        for j in range(R):
+            lo = j * NvS
+            assert np.array_equal(got[lo:lo + ends[j]], want[lo:lo + ends[j]]), (c0, j)
+    for j in range(R):
+        tail = out[j * NvS + int(ends[j]):(j + 1) * NvS].view(torch.int16)
+        assert torch.all(tail == nan_bits), f"rank {j} tail written"
+    del out, grad, x, wn, wn0

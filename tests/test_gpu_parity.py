@@ -383,6 +383,49 @@ def test_plan_reuse_dispatch_equals_fresh():
         assert torch.equal(a[lo:lo + end].view(torch.int16), b[lo:lo + end].view(torch.int16))
 
 
+@pytest.mark.parametrize("name,kind,S", [("kimi_k2", "hot", 300), ("deepseek_v3", "zipf", 257),
+                                         ("tiny", "zipf", 64)])
+def test_plan_reuse_dispatch_matches_oracle(name, kind, S):
+    """Combine-backward dispatch [API, Buffer.dispatch with a saved plan;
+    Buffer.combine backward]: an independent [R, S, H] gradient dispatched
+    with a clone of the forward plan and no weights equals the oracle's
+    dispatch of that gradient (weights absent) on every valid and padding
+    row; tail rows keep their poison, and the forward's zero-copy rows and
+    route weights stay as the forward left them."""
+    sh = _small(name, S) if name != "tiny" else wl.SHAPES["tiny"]
+    topk = _routing(sh, kind, 31)
+    cfg = _cfg_of(sh)
+    buf = _buffer(cfg, H=sh.H, dup=False, views=True)
+    tk = torch.from_numpy(topk).cuda()
+    x = torch.randn(sh.R, sh.S, sh.H, device="cuda").bfloat16()
+    w = torch.rand(sh.R, sh.S, sh.K, device="cuda")
+    hid, wn, _, plan = buf.dispatch(x, w, tk, zero_copy=True, router_weights_zero_copy=True)
+    saved = plan.clone()
+    torch.cuda.synchronize()
+    hid0, wn0 = hid.clone(), wn.clone()
+    g = torch.randn(sh.R, sh.S, sh.H, device="cuda").bfloat16()
+    poison = torch.full((sh.R * buf.NvS, sh.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out, wout, cu, _ = buf.dispatch(g, plan=saved, out=poison)
+    assert out.data_ptr() == poison.data_ptr() and wout is None and cu is None
+    assert buf.get_status() == 0
+    st, op = _oracle_plan(cfg, topk)
+    assert st == 0
+    NvS = op["NvS"]
+    gb = g.view(torch.int16).cpu().numpy().view(np.uint16).reshape(sh.R * sh.S, sh.H)
+    want = np.full((sh.R * NvS, sh.H), 0x7fc0, np.uint16)
+    oracle.dispatch(sh.R, sh.S, sh.K, sh.E, sh.B, NvS, sh.H, op["dst"], op["zero_fill_ranges"],
+                    gb, None, want)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    nan_bits = int(torch.tensor(float("nan"), dtype=torch.bfloat16).view(torch.int16).item()) & 0xFFFF
+    for j in range(sh.R):
+        end = int(op["cu_seqlens"][j, -1])
+        lo = j * NvS
+        assert np.array_equal(got[lo:lo + end], want[lo:lo + end]), f"rank {j} rows differ"
+        assert np.all(got[lo + end:lo + NvS] == nan_bits), f"rank {j} tail written"
+    assert torch.equal(hid.view(torch.int16), hid0.view(torch.int16))
+    assert torch.equal(wn.view(torch.int32), wn0.view(torch.int32))
+
+
 def test_zero_copy_views():
     sh = wl.SHAPES["tiny"]
     topk = _routing(sh, "zipf", 2)

@@ -95,6 +95,31 @@ def test_buffer_pool_capacities():
     pool.destroy()
 
 
+@pytest.mark.parametrize("mn,mx", [(1, 100), (16, 4096), (10, 1000), (7, 7), (3, 64)])
+def test_buffer_pool_rule_as_stated(mn, mx):
+    """Every token count against the rule's words: a power of two that holds
+    the tokens, the smallest such, then kept within [min, max].  So the
+    capacity is min, max or a power of two; it holds the batch whenever the
+    batch fits at all; and no smaller power of two inside the bounds holds it."""
+    from combine_moonep_plan_gb300.api import BufferPool
+    pool = BufferPool(max_tokens_per_rank=mx, min_tokens=mn, H=64, K=2, E=8, num_ep_ranks=2)
+    pow2 = [1 << i for i in range(24)]
+    for n in range(0, mx + 20):
+        cap = pool.capacity_for(n)
+        assert mn <= cap <= mx
+        assert cap in (mn, mx) or cap in pow2
+        if n <= mx:
+            assert cap >= n
+        smaller = [p for p in pow2 if max(n, 1) <= p < cap and mn <= p]
+        assert not smaller, (n, cap, smaller)
+        if cap not in (mn, mx):
+            assert cap // 2 < n          # the smallest power of two holding n
+    with pytest.raises(ValueError):
+        pool.get(mx + 1)
+    with pytest.raises(ValueError):
+        BufferPool(max_tokens_per_rank=8, min_tokens=9)
+
+
 def test_strerror_texts(lib):
     for code in range(-8, 1):
         assert lib.moonep_strerror(code)

@@ -6,7 +6,9 @@ context or a plan object.  This entry point takes caller-allocated outputs and
 keeps its intermediate tables in a fixed file-scope device array.  Its plan
 must equal the one moonep_plan writes for the same inputs, bit for bit (the
 plan is integer data, the tolerance every plan test uses), on two calls in a
-row, since the second call reuses the scratch the first left behind.
+row, since the second call reuses the scratch the first left behind, and
+equal the oracle's plan; one case runs in a fresh process where this entry
+point is the only planner ever called.
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test.
@@ -78,7 +80,9 @@ def _shape(name, S):
 
 def test_noalloc_plan_matches_moonep_plan_twice(lib):
     """Two calls in a row with different routings and sizes: each equals the
-    context-based planner's output."""
+    context-based planner's output and the oracle's plan.  The calls come
+    before any context of that shape exists."""
+    import oracle
     cases = [(_shape("deepseek_v3", 4096), "zipf", 21),
              (_shape("kimi_k2", 600), "hot", 22),
              (wl.SHAPES["tiny"], "zipf", 23)]
@@ -88,12 +92,74 @@ def test_noalloc_plan_matches_moonep_plan_twice(lib):
         else:
             topk, _ = wl.routing(sh, "zipf", zipf_s=1.5, seed=seed)
         tpe = wl.tokens_per_expert(topk, sh.E)
-        ref = _reference(sh, topk, tpe)
+        outs = []
         for call in range(2):
             rc, out, status = _noalloc(lib, sh, topk, tpe)
             assert rc == 0 and status == 0, (rc, status)
+            outs.append(out)
+        ref = _reference(sh, topk, tpe)
+        st, want = oracle.plan(sh.R, sh.E, sh.K, sh.S, sh.B, sh.tp, topk, tpe, dup_records=False)
+        assert st == 0
+        for call, out in enumerate(outs):
             for f in FIELDS:
                 assert torch.equal(out[f], ref[f]), f"{sh.name} call {call}: {f} differs"
+                assert np.array_equal(out[f].cpu().numpy(), want[f]), \
+                    f"{sh.name} call {call}: {f} differs from the oracle"
+
+
+FRESH_CHILD = r"""
+import ctypes, sys
+import numpy as np
+import torch
+sys.path.insert(0, {root!r})
+from combine_moonep_plan_gb300 import _lib, workloads as wl
+lib = _lib.load()
+res = {{}}
+for i, (R, E, K, S, B, tp) in enumerate({shapes!r}):
+    sh = wl.Shape("s%d" % i, R=R, E=E, K=K, S=S, H=8, Hp=8, B=B, tp=tp, weights="softmax")
+    topk, _ = wl.routing(sh, "zipf", zipf_s=1.4, seed=40 + i)
+    cfg = _lib.MoonepConfig(R=R, E=E, K=K, S=S, H=8, B=B, token_padding=tp, num_sms=0)
+    out = [torch.full(n, -7, dtype=torch.int32, device="cuda")
+           for n in ((R, S * K), (R, B), (R, E + B), (R, E + B, 2), (R, 2), (R, 2))]
+    status = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    tk = torch.from_numpy(topk).cuda()
+    rc = lib.moonep_plan_noalloc(ctypes.byref(cfg), tk.data_ptr(), None,
+                                 *[o.data_ptr() for o in out], status.data_ptr(),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    res["rc%d" % i] = np.array([rc, int(status.item())])
+    res["topk%d" % i] = topk
+    for n, o in zip({fields!r}, out):
+        res["%s%d" % (n, i)] = o.cpu().numpy()
+np.savez({path!r}, **res)
+"""
+
+
+def test_noalloc_first_planner_of_a_fresh_process(lib, tmp_path):
+    """A process whose only planner is this entry point: shapes whose
+    planner tables grow with R (same E) and with B, each compared with the
+    oracle's plan.  No context exists in that process, so nothing else has
+    set the planner kernels' shared-memory limits for these shapes."""
+    import os
+    import subprocess
+    import sys
+    import oracle
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    shapes = [(8, 384, 8, 64, 48, 16), (16, 384, 8, 64, 24, 16), (32, 384, 8, 32, 12, 16),
+              (8, 384, 8, 64, 96, 16), (4, 64, 4, 96, 16, 8)]
+    path = str(tmp_path / "fresh.npz")
+    code = FRESH_CHILD.format(root=root, shapes=shapes, fields=FIELDS, path=path)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                         timeout=600)
+    assert res.returncode == 0, res.stderr[-3000:]
+    got = np.load(path)
+    for i, (R, E, K, S, B, tp) in enumerate(shapes):
+        rc, status = got[f"rc{i}"]
+        assert rc == 0 and status == 0, (i, rc, status)
+        st, want = oracle.plan(R, E, K, S, B, tp, got[f"topk{i}"], None, dup_records=False)
+        assert st == 0
+        for f in FIELDS:
+            assert np.array_equal(got[f"{f}{i}"], want[f]), f"shape {i}: {f} differs from the oracle"
 
 
 def test_noalloc_reports_errors_and_limits(lib):
