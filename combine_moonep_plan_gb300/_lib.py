@@ -32,7 +32,8 @@ EXPORTS = (
     "moonep_dispatch_dedup", "moonep_combine_dedup",
     "moonep_prefetch_weight", "moonep_prefetch_rows", "moonep_reduce_redundant_grad", "moonep_hidden_view",
     "moonep_weight_view", "moonep_get_status", "moonep_strerror", "moonep_num_sms",
-    "moonep_plan_noalloc", "moonep_prepare",
+    "moonep_plan_noalloc", "moonep_prepare", "moonep_plan_rank", "moonep_dispatch_rank",
+    "moonep_combine_rank",
 )
 
 
@@ -103,6 +104,11 @@ def load(path: str = LIB_PATH):
         "moonep_get_status": (ci, [vp, ctypes.POINTER(ci), vp]),
         "moonep_strerror": (ctypes.c_char_p, [ci]),
         "moonep_plan_noalloc": (ci, [cfgp] + [vp] * 10),
+        "moonep_plan_rank": (ci, [vp, ci, vp, vp, planp, vp]),
+        "moonep_dispatch_rank": (ci, [vp, planp, ci, vp, vp, ctypes.POINTER(vp),
+                                      ctypes.POINTER(vp), vp]),
+        "moonep_combine_rank": (ci, [vp, planp, ci, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                     vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -347,6 +347,69 @@ class Buffer:
             self._ctx, plan.struct, len(gp), _lib.ptr_array(gp), _lib.ptr_array(sp), HHp,
             _stream()), "moonep_reduce_redundant_grad")
 
+    # ------------------------------------------------- rank-local forms
+    # The per-rank shape of the path when each EP rank is its own GPU: one
+    # exchange (the all-gather of every rank's [E] tokens_per_expert, see
+    # gather_tokens_per_expert), then each rank plans its own routes and
+    # moves its own tokens, with the other ranks' rows behind window pointers.
+    def plan_rank(self, rank: int, topk_sk: torch.Tensor, hist_all: torch.Tensor,
+                  plan: CommPlan | None = None) -> CommPlan:
+        """Rank `rank`'s share of the plan [Buffer.dispatch planning, per
+        rank]: topk_sk [S, K] int32 of that rank, hist_all [R, E] int32 the
+        gathered per-rank histograms.  Writes the rank's dst row, the tables
+        shared by every rank, and the rank's share of dup_counts."""
+        tk = _check_tensor(topk_sk, "topk_sk", torch.int32, (self.S, self.K))
+        hp = _check_tensor(hist_all, "hist_all", torch.int32, (self.R, self.E))
+        plan = self.new_plan() if plan is None else plan
+        check(_lib.load().moonep_plan_rank(self._ctx, int(rank), tk, hp, plan.struct, _stream()),
+              "moonep_plan_rank")
+        return plan
+
+    def _windows(self, rows, weights, name):
+        R, NvS, H = self.R, self.NvS, self.H
+        if len(rows) != R:
+            raise ValueError(f"{name}: expected {R} rank windows")
+        rp = [_check_tensor(t, f"{name}[{j}]", torch.bfloat16, (NvS, H)) for j, t in enumerate(rows)]
+        wp = None
+        if weights is not None:
+            if len(weights) != R:
+                raise ValueError(f"{name}: expected {R} weight windows")
+            wp = _lib.ptr_array([_check_tensor(t, f"{name} weights[{j}]", torch.float32, (NvS,))
+                                 for j, t in enumerate(weights)])
+        return _lib.ptr_array(rp), wp
+
+    def dispatch_rank(self, plan: CommPlan, rank: int, hidden_sh: torch.Tensor,
+                      route_weights_sk: torch.Tensor | None, windows, weight_windows=None):
+        """Rank `rank`'s tokens into the R rank windows (each [NvS, H] bf16,
+        its own tensor) and zero padding of the rank's own window
+        [Buffer.dispatch, per rank]."""
+        hp = _check_tensor(hidden_sh, "hidden_sh", torch.bfloat16, (self.S, self.H))
+        wp = None
+        if route_weights_sk is not None:
+            wp = _check_tensor(route_weights_sk, "route_weights_sk", torch.float32,
+                               (self.S, self.K))
+        rows, wins = self._windows(windows, weight_windows, "windows")
+        check(_lib.load().moonep_dispatch_rank(self._ctx, plan.struct, int(rank), hp, wp, rows,
+                                               wins, _stream()), "moonep_dispatch_rank")
+
+    def combine_rank(self, plan: CommPlan, rank: int, windows, weight_windows=None,
+                     out: torch.Tensor | None = None):
+        """Rank `rank`'s tokens gathered from the R rank windows and K-summed
+        [Buffer.combine, per rank].  Returns (hidden_sh [S, H] bf16,
+        route_weights_sk [S, K] fp32 or None)."""
+        rows, wins = self._windows(windows, weight_windows, "windows")
+        if out is None:
+            out = torch.empty((self.S, self.H), dtype=torch.bfloat16, device="cuda")
+        op = _check_tensor(out, "hidden_sh", torch.bfloat16, (self.S, self.H))
+        w_out = None
+        wop = None
+        if weight_windows is not None:
+            w_out = torch.empty((self.S, self.K), dtype=torch.float32, device="cuda")
+            wop = w_out.data_ptr()
+        check(_lib.load().moonep_combine_rank(self._ctx, plan.struct, int(rank), rows, wins, op,
+                                              wop, _stream()), "moonep_combine_rank")
+        return out, w_out
+
     # ------------------------------------------------------------ status
     def get_status(self) -> int:
         """Synchronise the current stream and return (and clear) the first
@@ -355,6 +418,22 @@ class Buffer:
         check(_lib.load().moonep_get_status(self._ctx, ctypes.byref(v), _stream()),
               "moonep_get_status")
         return v.value
+
+
+def gather_tokens_per_expert(tokens_per_expert: torch.Tensor, group=None) -> torch.Tensor:
+    """The rank-local planner's one exchange step: every rank's [E] int32
+    tokens_per_expert, all-gathered into [R, E] in rank order over
+    torch.distributed (the group's ranks are the EP ranks).  Every rank then
+    holds the same histogram, from which Buffer.plan_rank derives the same
+    balance tables on every rank."""
+    import torch.distributed as dist
+    t = tokens_per_expert.to(torch.int32).contiguous()
+    if t.dim() != 1:
+        raise ValueError("tokens_per_expert: expected [E]")
+    world = dist.get_world_size(group)
+    parts = [torch.empty_like(t) for _ in range(world)]
+    dist.all_gather(parts, t, group=group)
+    return torch.stack(parts)
 
 
 class BufferPool:

@@ -52,7 +52,10 @@ static size_t scratch_bytes_of(const moonep_config &c) {
   const int64_t C = (int64_t)c.S * c.K;
   // planner tiles of either path: at most R * ceil(S*K / 1024)
   const int64_t tiles = (int64_t)c.R * ((C + 1023) / 1024 > 0 ? (C + 1023) / 1024 : 1);
-  return (size_t)(c.E * (tiles + 2 * c.R) + c.R * C) * sizeof(int32_t) + 512;
+  // planner tiles of every launch form, two [R, E] and two [E] totals sets
+  const int64_t local = (C + 543) / 544 > 0 ? (C + 543) / 544 : 1;
+  const int64_t t = tiles > local ? tiles : local;
+  return (size_t)(c.E * (t + 2 * c.R + 2) + c.R * C) * sizeof(int32_t) + 1024;
 }
 
 }  // namespace moonep
@@ -258,6 +261,65 @@ int moonep_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe, moonep
   if ((st = check_plan(ctx, plan))) return st;
   if (ctx->C > 0 && !topk) return MOONEP_ERR_INVALID_ARG;
   return launch_plan(ctx, topk, tpe, plan, (cudaStream_t)stream);
+}
+
+int moonep_plan_rank(moonep_ctx *ctx, int rank, const int32_t *topk_r, const int32_t *hist_all,
+                     moonep_comm_plan *plan, void *stream) {
+  int st = check_ctx(ctx);
+  if (st) return st;
+  if ((st = check_plan(ctx, plan))) return st;
+  if (rank < 0 || rank >= ctx->cfg.R || !hist_all || (ctx->C > 0 && !topk_r))
+    return MOONEP_ERR_INVALID_ARG;
+  if ((plan->flags & MOONEP_PLAN_DUP_RECORDS) || !plan_rank_supported(ctx))
+    return MOONEP_ERR_INVALID_ARG;
+  return launch_plan_rank(ctx, rank, topk_r, hist_all, plan, (cudaStream_t)stream);
+}
+
+// The R window pointers of a rank-local call: all given and 16-byte aligned
+// (weights: all given or the array NULL, 4-byte aligned).
+static int check_windows(const moonep_ctx *ctx, const void *const *rows, const void *const *w,
+                         bool need_w) {
+  const int R = ctx->cfg.R;
+  if (!rows) return MOONEP_ERR_INVALID_ARG;
+  for (int j = 0; j < R; j++)
+    if (!rows[j] || !aligned16(rows[j])) return MOONEP_ERR_INVALID_ARG;
+  if (need_w != (w != nullptr)) return MOONEP_ERR_INVALID_ARG;
+  if (w)
+    for (int j = 0; j < R; j++)
+      if (!w[j] || ((uintptr_t)w[j] & 3)) return MOONEP_ERR_INVALID_ARG;
+  return MOONEP_OK;
+}
+
+int moonep_dispatch_rank(moonep_ctx *ctx, const moonep_comm_plan *plan, int rank,
+                         const uint16_t *hidden_r, const float *w_r, uint16_t *const *windows,
+                         float *const *w_windows, void *stream) {
+  int st = check_ctx(ctx);
+  if (st) return st;
+  if ((st = check_plan(ctx, plan))) return st;
+  if (rank < 0 || rank >= ctx->cfg.R) return MOONEP_ERR_INVALID_ARG;
+  if (ctx->cfg.S > 0 && !hidden_r) return MOONEP_ERR_INVALID_ARG;
+  if (!aligned16(hidden_r) || ((uintptr_t)w_r & 3)) return MOONEP_ERR_INVALID_ARG;
+  if ((st = check_windows(ctx, (const void *const *)windows, (const void *const *)w_windows,
+                          w_r != nullptr)))
+    return st;
+  return launch_dispatch_rank(ctx, plan, rank, hidden_r, w_r, windows, w_windows,
+                              (cudaStream_t)stream);
+}
+
+int moonep_combine_rank(moonep_ctx *ctx, const moonep_comm_plan *plan, int rank,
+                        const uint16_t *const *y_windows, const float *const *w_windows,
+                        uint16_t *out_r, float *w_out_r, void *stream) {
+  int st = check_ctx(ctx);
+  if (st) return st;
+  if ((st = check_plan(ctx, plan))) return st;
+  if (rank < 0 || rank >= ctx->cfg.R) return MOONEP_ERR_INVALID_ARG;
+  if (ctx->cfg.S > 0 && !out_r) return MOONEP_ERR_INVALID_ARG;
+  if (!aligned16(out_r) || ((uintptr_t)w_out_r & 3)) return MOONEP_ERR_INVALID_ARG;
+  if ((st = check_windows(ctx, (const void *const *)y_windows, (const void *const *)w_windows,
+                          w_out_r != nullptr)))
+    return st;
+  return launch_combine_rank(ctx, plan, rank, y_windows, w_windows, out_r, w_out_r,
+                             (cudaStream_t)stream);
 }
 
 int moonep_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *hidden,

@@ -17,6 +17,11 @@
 // two batches of four rows, 128-thread blocks) reaches the copy bandwidth.
 // HBM bytes per call: read N*H*2 + N*4 (dst) [+ N*4 weights]; write
 // R*S*H*2 [+ N*4].
+//
+// The rank-local form (one source rank's tokens, its K rows read from R
+// separately allocated rank windows) is the same kernel with another row
+// addressing: the per-GPU shape of the combine when each rank is a GPU and
+// the owner pulls its rows from its peers.
 #include "copy_common.cuh"
 #include "moonep_internal.cuh"
 
@@ -25,15 +30,37 @@ namespace {
 
 
 struct Args {
-  const uint4 *y;
-  const float *w_nvs;
   const int32_t *dst;
   uint4 *out;
   float *w_out;
   int32_t *status;
   int64_t ntok;
   int64_t total_rows;
-  int K, H8, nchunk;
+  int K, H8, nchunk, NvS;
+};
+
+// Source addressing of global row g = j*NvS + w: one [R*NvS, H] buffer, or
+// rank j's [NvS, H] rows at row[j] (its [NvS] weights at w[j]).
+struct FlatRows {
+  static constexpr bool kPrimaries = true;  // also instantiated for the deduplicated combine
+  const uint4 *y;
+  const float *w_nvs;
+  __device__ __forceinline__ const uint4 *row(int64_t g, int H8, int) const { return y + g * H8; }
+  __device__ __forceinline__ const float *weight(int64_t g, int) const { return w_nvs + g; }
+};
+
+struct WindowRows {
+  static constexpr bool kPrimaries = false;
+  const uint4 *y[kMaxRanks];
+  const float *w_nvs[kMaxRanks];
+  __device__ __forceinline__ const uint4 *row(int64_t g, int H8, int NvS) const {
+    const int j = (int)(g / NvS);
+    return y[j] + (g - (int64_t)j * NvS) * H8;
+  }
+  __device__ __forceinline__ const float *weight(int64_t g, int NvS) const {
+    const int j = (int)(g / NvS);
+    return w_nvs[j] + (g - (int64_t)j * NvS);
+  }
 };
 
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v) {
@@ -77,8 +104,8 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 // runtime-K kernel, four rows per batch.  PRIM: sum the primary
 // routes only (dst >= 0; the duplicates were folded into them), a separate
 // instantiation so that the direct kernel carries none of its code.
-template <int KT, int U, int BT, int KB, bool PRIM>
-__global__ void __launch_bounds__(BT) combine_kernel(Args a) {
+template <int KT, int U, int BT, int KB, bool PRIM, class Rows>
+__global__ void __launch_bounds__(BT) combine_kernel(Args a, Rows rows) {
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
@@ -105,7 +132,7 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
         set_status(a.status, MOONEP_ERR_PLAN);
         g = 0;
       }
-      if (c == 0 && a.w_out) a.w_out[t * K + lane] = __ldg(a.w_nvs + g);
+      if (c == 0 && a.w_out) a.w_out[t * K + lane] = __ldg(rows.weight(g, a.NvS));
     }
     const int v0 = c * 32 * U + lane;
     float acc[U][8];
@@ -116,7 +143,7 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
         uint4 x[KB][U];
 #pragma unroll
         for (int kk = 0; kk < KB; kk++) {
-          const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k0 + kk) * a.H8;
+          const uint4 *row = rows.row(__shfl_sync(0xffffffffu, g, k0 + kk), a.H8, a.NvS);
           const bool skip = (dupm >> (k0 + kk)) & 1u;
 #pragma unroll
           for (int i = 0; i < U; i++) {
@@ -141,7 +168,7 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
 #pragma unroll
         for (int kk = 0; kk < KB; kk++) {
           const int k = k0 + kk;
-          const uint4 *row = a.y + __shfl_sync(0xffffffffu, g, k & 31) * a.H8;
+          const uint4 *row = rows.row(__shfl_sync(0xffffffffu, g, k & 31), a.H8, a.NvS);
           const bool use = k < K && !((dupm >> (k & 31)) & 1u);
 #pragma unroll
           for (int i = 0; i < U; i++) {
@@ -170,24 +197,64 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a) {
   }
 }
 
-template <int KT, int U, int BT, int KB>
-cudaError_t launch(const Args &a, bool prim, int grid, cudaStream_t st) {
-  return prim ? launch_pdl(combine_kernel<KT, U, BT, KB, true>, grid, BT, 0, st, false, a)
-              : launch_pdl(combine_kernel<KT, U, BT, KB, false>, grid, BT, 0, st, false, a);
+template <int KT, int U, int BT, int KB, class Rows>
+cudaError_t launch(const Args &a, const Rows &rows, bool prim, int grid, cudaStream_t st) {
+  if constexpr (Rows::kPrimaries) {
+    if (prim)
+      return launch_pdl(combine_kernel<KT, U, BT, KB, true, Rows>, grid, BT, 0, st, false, a,
+                        rows);
+  }
+  return launch_pdl(combine_kernel<KT, U, BT, KB, false, Rows>, grid, BT, 0, st, false, a, rows);
+}
+
+// Batch shape per K (vectors per lane, threads per block, rows per batch),
+// the instantiations occupancy_combine measures.
+template <class Rows>
+cudaError_t launch_k(const Args &a, const Rows &rows, bool prim, int grid, cudaStream_t st) {
+  switch (a.K) {
+    case 1: return launch<1, 4, 256, 1>(a, rows, prim, grid, st);
+    case 2: return launch<2, 8, 128, 2>(a, rows, prim, grid, st);
+    case 3: return launch<3, 8, 128, 1>(a, rows, prim, grid, st);
+    case 4: return launch<4, 4, 128, 2>(a, rows, prim, grid, st);
+    case 6: return launch<6, 4, 128, 3>(a, rows, prim, grid, st);
+    case 8: return launch<8, 4, 128, 4>(a, rows, prim, grid, st);
+    case 10: return launch<10, 8, 128, 1>(a, rows, prim, grid, st);
+    default: return launch<0, 4, 128, 4>(a, rows, prim, grid, st);
+  }
+}
+
+int unit_vectors(int K) { return (K == 2 || K == 3 || K == 10) ? 8 : 4; }
+
+Args make_args(const moonep_ctx *ctx, const moonep_comm_plan *plan, int64_t ntok, int r0,
+               uint16_t *out, float *w_out) {
+  const moonep_config &c = ctx->cfg;
+  Args a;
+  a.dst = plan->dst + (int64_t)r0 * ctx->C;
+  a.out = reinterpret_cast<uint4 *>(out);
+  a.w_out = w_out;
+  a.status = ctx->d_status;
+  a.ntok = ntok;
+  a.total_rows = (int64_t)c.R * ctx->NvS;
+  a.K = c.K;
+  a.H8 = c.H / 8;
+  const int U = unit_vectors(c.K);
+  a.nchunk = (a.H8 + 32 * U - 1) / (32 * U);
+  a.NvS = ctx->NvS;
+  return a;
 }
 
 }  // namespace
 
 int occupancy_combine(int K) {
   int n = 0;
-  void *f = K == 1 ? (void *)combine_kernel<1, 4, 256, 1, false>
-          : K == 2 ? (void *)combine_kernel<2, 8, 128, 2, false>
-          : K == 3 ? (void *)combine_kernel<3, 8, 128, 1, false>
-          : K == 4 ? (void *)combine_kernel<4, 4, 128, 2, false>
-          : K == 6 ? (void *)combine_kernel<6, 4, 128, 3, false>
-          : K == 8 ? (void *)combine_kernel<8, 4, 128, 4, false>
-          : K == 10 ? (void *)combine_kernel<10, 8, 128, 1, false>
-                    : (void *)combine_kernel<0, 4, 128, 4, false>;
+  void *f = K == 1 ? (void *)combine_kernel<1, 4, 256, 1, false, FlatRows>
+          : K == 2 ? (void *)combine_kernel<2, 8, 128, 2, false, FlatRows>
+          : K == 3 ? (void *)combine_kernel<3, 8, 128, 1, false, FlatRows>
+          : K == 4 ? (void *)combine_kernel<4, 4, 128, 2, false, FlatRows>
+          : K == 6 ? (void *)combine_kernel<6, 4, 128, 3, false, FlatRows>
+          : K == 8 ? (void *)combine_kernel<8, 4, 128, 4, false, FlatRows>
+          : K == 10 ? (void *)combine_kernel<10, 8, 128, 1, false, FlatRows>
+                    : (void *)combine_kernel<0, 4, 128, 4, false, FlatRows>;
   const int bt = K == 1 ? 256 : 128;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, bt, 0) != cudaSuccess) n = 1;
   return n > 0 ? n : 1;
@@ -197,33 +264,24 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
                    const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st,
                    bool primaries_only) {
   const moonep_config &c = ctx->cfg;
-  Args a;
-  a.y = reinterpret_cast<const uint4 *>(y);
-  a.w_nvs = w_nvs;
-  a.dst = plan->dst;
-  a.out = reinterpret_cast<uint4 *>(out);
-  a.w_out = w_out;
-  a.status = ctx->d_status;
-  a.ntok = (int64_t)c.R * c.S;
-  a.total_rows = (int64_t)c.R * ctx->NvS;
-  a.K = c.K;
-  a.H8 = c.H / 8;
-  const int U = (c.K == 2 || c.K == 3 || c.K == 10) ? 8 : 4;
-  a.nchunk = (a.H8 + 32 * U - 1) / (32 * U);
+  Args a = make_args(ctx, plan, (int64_t)c.R * c.S, 0, out, w_out);
   if (a.ntok == 0 || a.H8 == 0) return MOONEP_OK;
-  const int grid = ctx->sms * ctx->blocks_combine;
-  cudaError_t e;
-  switch (c.K) {
-    case 1: e = launch<1, 4, 256, 1>(a, primaries_only, grid, st); break;
-    case 2: e = launch<2, 8, 128, 2>(a, primaries_only, grid, st); break;
-    case 3: e = launch<3, 8, 128, 1>(a, primaries_only, grid, st); break;
-    case 4: e = launch<4, 4, 128, 2>(a, primaries_only, grid, st); break;
-    case 6: e = launch<6, 4, 128, 3>(a, primaries_only, grid, st); break;
-    case 8: e = launch<8, 4, 128, 4>(a, primaries_only, grid, st); break;
-    case 10: e = launch<10, 8, 128, 1>(a, primaries_only, grid, st); break;
-    default: e = launch<0, 4, 128, 4>(a, primaries_only, grid, st); break;
+  FlatRows rows{reinterpret_cast<const uint4 *>(y), w_nvs};
+  return cuda_status(launch_k(a, rows, primaries_only, ctx->sms * ctx->blocks_combine, st));
+}
+
+int launch_combine_rank(moonep_ctx *ctx, const moonep_comm_plan *plan, int rank,
+                        const uint16_t *const *y_windows, const float *const *w_windows,
+                        uint16_t *out_r, float *w_out_r, cudaStream_t st) {
+  const moonep_config &c = ctx->cfg;
+  Args a = make_args(ctx, plan, c.S, rank, out_r, w_out_r);
+  if (a.ntok == 0 || a.H8 == 0) return MOONEP_OK;
+  WindowRows rows;
+  for (int j = 0; j < kMaxRanks; j++) {
+    rows.y[j] = j < c.R ? reinterpret_cast<const uint4 *>(y_windows[j]) : nullptr;
+    rows.w_nvs[j] = (w_windows && j < c.R) ? w_windows[j] : nullptr;
   }
-  return cuda_status(e);
+  return cuda_status(launch_k(a, rows, false, ctx->sms * ctx->blocks_combine, st));
 }
 
 }  // namespace moonep

@@ -11,6 +11,10 @@
 
 namespace moonep {
 
+// Ranks a configuration may have (the balance step keeps per-rank state in
+// shared memory; the rank-local copy kernels take one window per rank).
+constexpr int kMaxRanks = 64;
+
 // Routes handled by one planner tile: 8 warps x 32 lanes x 8 routes.
 constexpr int kPlanThreads = 256;
 constexpr int kPlanItems = 8;
@@ -97,7 +101,7 @@ struct moonep_ctx {
   int32_t *d_ord;      // [R*C] ordinal of a route among its tile's routes to the same expert
   uint16_t *d_hidden_view;  // optional [R*NvS, H] bf16
   float *d_weight_view;     // optional [R*NvS] fp32
-  unsigned long long *d_sync;  // [2] planner counters: arrivals, tile blocks done
+  unsigned long long *d_sync;  // [2] planner arrival counters: every-rank calls, rank-local calls
   int test_planner_timeout;    // test hook: the planner's arrival wait never completes
   int blocks_dispatch, blocks_combine, blocks_copy, blocks_reduce, blocks_expand,
       blocks_fold;  // resident blocks per SM
@@ -113,12 +117,26 @@ int cuda_status(cudaError_t e);
 // Launchers (one per translation unit).
 int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
                 moonep_comm_plan *plan, cudaStream_t st);
+// The rank-local planner (one source rank's routes, gathered [R, E]
+// histograms), and whether the configuration allows it (the single-launch
+// planner's tables fit in shared memory and one rank's tiles fit on the SMs).
+int launch_plan_rank(moonep_ctx *ctx, int rank, const int32_t *topk_r, const int32_t *hist_all,
+                     moonep_comm_plan *plan, cudaStream_t st);
+int plan_rank_supported(const moonep_ctx *ctx);
 int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *hidden,
                     const float *w_sk, uint16_t *out, float *w_out, cudaStream_t st,
                     bool primaries_only = false);
 int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t *y,
                    const float *w_nvs, uint16_t *out, float *w_out, cudaStream_t st,
                    bool primaries_only = false);
+// Rank-local forms: source rank `rank`'s tokens, rows in R rank windows
+// (windows[j] = rank j's [NvS, H] rows, w_windows[j] its [NvS] weights).
+int launch_dispatch_rank(moonep_ctx *ctx, const moonep_comm_plan *plan, int rank,
+                         const uint16_t *hidden_r, const float *w_r, uint16_t *const *windows,
+                         float *const *w_windows, cudaStream_t st);
+int launch_combine_rank(moonep_ctx *ctx, const moonep_comm_plan *plan, int rank,
+                        const uint16_t *const *y_windows, const float *const *w_windows,
+                        uint16_t *out_r, float *w_out_r, cudaStream_t st);
 // The deduplicated data flow's local steps: copy every primary row to its
 // duplicates (dispatch epilogue), or fold every rank's duplicate rows of a
 // token into its primary row (combine prologue).
@@ -140,6 +158,8 @@ int plan_hist_tiles(int R, int C, int K, int sms);
 // [R, E] totals (at plan_totals_offset) and two error words, used by
 // alternate calls, zero before a call uses them.
 int64_t plan_totals_offset(int R, int E, int C, int K, int sms);
+// After those: the rank-local planner's two [E] totals sets and error words.
+int64_t plan_rank_totals_offset(int R, int E, int C, int K, int sms);
 int64_t plan_scratch_words(int R, int E, int C, int K, int sms);
 int occupancy_dispatch(int K);
 int occupancy_combine(int K);

@@ -160,7 +160,7 @@ plan_hist_kernel(const int32_t *__restrict__ topk, PlanDims d, int32_t *__restri
 // ------------------------------------------------------------------ K2
 
 constexpr int kBalThreads = 1024;
-constexpr int kMaxR = 64;
+constexpr int kMaxR = kMaxRanks;
 
 // Per-rank and per-piece state of the balance step (shared memory).
 struct BalSmall {
@@ -805,7 +805,15 @@ struct FusedArgs {
   // [0] arrivals: grows by G + 2 per call
   unsigned long long *sync;
   int32_t *dupflag;
-  int tpr, G;         // tiles per rank, tile blocks (R * tpr)
+  int tpr, G;         // tiles per rank, tile blocks (R * tpr; tpr for one rank)
+  // Rank-local planning (src_rank >= 0): the launch holds only that source
+  // rank's routes (topk points at its [S, K]) and takes the per-rank totals
+  // from hist_all, the [R, E] histograms every rank contributed (an
+  // all-gather across GPUs); its own recount only checks hist_all[src_rank].
+  // Every rank derives the same tables from the same totals and assigns
+  // only its own routes.  totals/errw then point at a set of one row.
+  int src_rank;
+  const int32_t *hist_all;
   int unreachable;    // test hook: the arrival wait can never be satisfied
   long long wait_ns;  // limit of each wait
 };
@@ -852,14 +860,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   const int g = blockIdx.x;
   const int nblk = a.G + 2;  // tile blocks, then the table block and the list block
   const bool tile = g < a.G, table_block = g == a.G, list_block = g == a.G + 1;
-  const int r = tile ? g / a.tpr : 0, t = tile ? g % a.tpr : 0;
+  const bool local = a.src_rank >= 0;
+  const int r = local ? a.src_rank : (tile ? g / a.tpr : 0), t = tile ? g % a.tpr : 0;
+  const int trows = local ? 1 : R;     // rows of a totals set
+  const int trow = local ? 0 : r;      // this block's row in it
+  const int gbase = local ? 0 : r * a.tpr;  // this rank's first tile in the launch
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int32_t *h = sm;                     // [warps][E]
   int32_t *sCnt = h + kFusedWarps * E;  // [R*E]
   int32_t *sSrc = sCnt + E * R;         // [E]
   const BalTables tb = bal_tables(sSrc + E, d);
 
-  const int32_t *src = a.topk + (int64_t)r * C;
+  const int32_t *src = a.topk + (local ? 0 : (int64_t)r * C);
   const unsigned lt = lanemask_lt();
   const int nbits = key_bits(E);
   constexpr int items = IT;
@@ -922,7 +934,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
         run += v;
       }
       a.hist[(int64_t)g * E + e] = run;
-      if (run) atomicAdd(a.totals + ((int64_t)s_par * R + r) * E + e, run);
+      if (run) atomicAdd(a.totals + ((int64_t)s_par * trows + trow) * E + e, run);
     }
     __threadfence();  // this thread's histogram entries and totals, before the arrival
   }
@@ -941,8 +953,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   __syncthreads();
   const bool ok = s_ok;
   if (ok) {
-    const int32_t *tot_in = a.totals + (int64_t)s_par * R * E;
-    for (int i = tid; i < R * E; i += kFusedThreads) sCnt[i] = __ldcg(tot_in + i);
+    const int32_t *tot_in = a.totals + (int64_t)s_par * trows * E;
+    if (local) {
+      // the gathered histograms are the totals; this rank's recount checks
+      // its own row, a slice per block (a mismatch latches its error; the
+      // tables stay those of the gathered counts, which every rank shares)
+      for (int i = tid; i < R * E; i += kFusedThreads) sCnt[i] = __ldg(a.hist_all + i);
+      for (int e = g * kFusedThreads + tid; e < E; e += nblk * kFusedThreads)
+        if (__ldcg(tot_in + e) != __ldg(a.hist_all + (int64_t)r * E + e))
+          set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
+    } else {
+      for (int i = tid; i < R * E; i += kFusedThreads) sCnt[i] = __ldcg(tot_in + i);
+    }
     __syncthreads();
     for (int e = tid; e < E; e += kFusedThreads) {
       int tot = 0, before = 0;
@@ -956,7 +978,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     }
     // tokens_per_expert against the recount, a slice per block: a mismatch
     // latches its error but the plan stands (it is built from the recount)
-    if (a.tpe != nullptr)
+    if (a.tpe != nullptr && !local)
       for (int i = g * kFusedThreads + tid; i < R * E; i += nblk * kFusedThreads)
         if (sCnt[i] != __ldg(a.tpe + i)) set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
     __syncthreads();
@@ -967,7 +989,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     // once; balance_route's barriers order the adds before their use)
     for (int i = tid; i < E * t; i += kFusedThreads) {
       const int e = i % E, tt = i / E;
-      atomicAdd(&sSrc[e], __ldcg(a.hist + (int64_t)(r * a.tpr + tt) * E + e));
+      atomicAdd(&sSrc[e], __ldcg(a.hist + (int64_t)(gbase + tt) * E + e));
     }
     balance_route(d, tb, bs, s_err);
   }
@@ -980,8 +1002,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     balance_tables(d, tb, bs, a.o, a.in, a.lay, a.status, ok);
     // the other set of totals and error bits, used by the next call, back to
     // zero (the previous call, its last user, has completed)
-    int32_t *other = a.totals + (int64_t)(1 - s_par) * R * E;
-    for (int i = tid; i < R * E; i += kFusedThreads) other[i] = 0;
+    int32_t *other = a.totals + (int64_t)(1 - s_par) * trows * E;
+    for (int i = tid; i < trows * E; i += kFusedThreads) other[i] = 0;
     if (tid == 0) a.errw[1 - s_par] = 0;
     return;
   }
@@ -1183,20 +1205,29 @@ int plan_fused_items(int R, int C, int K, int sms) {
   return 0;
 }
 
-// Tiles of either planner path (the histogram area holds E words per tile).
+// Tiles of any planner launch (the histogram area holds E words per tile):
+// the tile path, the single-launch planner over every rank, or over one rank.
 int plan_hist_tiles(int R, int C, int K, int sms) {
   const int tile_path = R * ((C + kTile - 1) / kTile);
   const int items = plan_fused_items(R, C, K, sms);
   const int fused = items ? R * plan_fused_tiles(C, K, items) : 0;
-  return tile_path > fused ? tile_path : fused;
+  const int items1 = plan_fused_items(1, C, K, sms);
+  const int local = items1 ? plan_fused_tiles(C, K, items1) : 0;
+  const int m = tile_path > fused ? tile_path : fused;
+  return m > local ? m : local;
 }
 
 int64_t plan_totals_offset(int R, int E, int C, int K, int sms) {
   return (int64_t)E * plan_hist_tiles(R, C, K, sms);
 }
 
-int64_t plan_scratch_words(int R, int E, int C, int K, int sms) {
+// After the totals: the rank-local planner's two [E] sets and error words.
+int64_t plan_rank_totals_offset(int R, int E, int C, int K, int sms) {
   return plan_totals_offset(R, E, C, K, sms) + 2 * (int64_t)R * E + 8;
+}
+
+int64_t plan_scratch_words(int R, int E, int C, int K, int sms) {
+  return plan_rank_totals_offset(R, E, C, K, sms) + 2 * (int64_t)E + 8;
 }
 
 // Shared memory the planner kernels may use.
@@ -1251,8 +1282,7 @@ cudaError_t plan_configure(int R, int E, int B) {
   return e;
 }
 
-int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
-                moonep_comm_plan *plan, cudaStream_t st) {
+static PlanDims plan_dims(const moonep_ctx *ctx) {
   const moonep_config &c = ctx->cfg;
   PlanDims d;
   d.R = c.R;
@@ -1268,6 +1298,61 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
   d.TPR = ctx->TPR;
   d.G = ctx->G;
   d.Bm = usable_slots(d.R, d.E, d.B);
+  return d;
+}
+
+static PlanOut plan_out(const moonep_comm_plan *plan) {
+  return PlanOut{plan->dst, plan->experts_to_copy, plan->cu_seqlens, plan->zero_fill_ranges,
+                 plan->remote_stats, plan->dup_counts, plan->dup_groups, plan->dup_loffs};
+}
+
+static cudaError_t launch_fused(const FusedArgs &fa, int items, cudaStream_t st) {
+  const size_t smem = fused_smem_words(fa.d.R, fa.d.E, fa.d.B) * sizeof(int32_t);
+  const dim3 grid(fa.G + 2), block(kFusedThreads);
+  return items == 1   ? launch_pdl(plan_fused_kernel<1>, grid, block, smem, st, true, fa)
+         : items == 2 ? launch_pdl(plan_fused_kernel<2>, grid, block, smem, st, true, fa)
+         : items == 4 ? launch_pdl(plan_fused_kernel<4>, grid, block, smem, st, true, fa)
+                      : launch_pdl(plan_fused_kernel<8>, grid, block, smem, st, true, fa);
+}
+
+int plan_rank_supported(const moonep_ctx *ctx) {
+  const moonep_config &c = ctx->cfg;
+  if (c.K < 1 || c.K > kMaxK || c.R > kMaxR) return 0;
+  if (fused_smem_words(c.R, c.E, c.B) * sizeof(int32_t) > kPlanSmemLimit) return 0;
+  return plan_fused_items(1, ctx->C, c.K, ctx->sms_device) > 0;
+}
+
+int launch_plan_rank(moonep_ctx *ctx, int rank, const int32_t *topk_r, const int32_t *hist_all,
+                     moonep_comm_plan *plan, cudaStream_t st) {
+  const PlanDims d = plan_dims(ctx);
+  FusedArgs fa;
+  fa.d = d;
+  fa.src_rank = rank;
+  fa.hist_all = hist_all;
+  fa.topk = topk_r;
+  fa.tpe = nullptr;
+  fa.hist = ctx->d_hist;
+  const int items = plan_fused_items(1, d.C, d.K, ctx->sms_device);
+  fa.tpr = plan_fused_tiles(d.C, d.K, items);
+  fa.G = fa.tpr;
+  fa.totals = ctx->d_hist + plan_rank_totals_offset(d.R, d.E, d.C, d.K, ctx->sms_device);
+  fa.errw = fa.totals + 2 * (int64_t)d.E;
+  fa.o = plan_out(plan);
+  fa.in = plan->internal;
+  fa.lay = PlanLayout::make(d.R, d.E, d.B, d.NvS, false);
+  fa.status = ctx->d_status;
+  fa.sync = ctx->d_sync + 1;  // the rank-local calls' own arrival counter
+  fa.dupflag = nullptr;
+  fa.unreachable = ctx->test_planner_timeout;
+  fa.wait_ns = ctx->test_planner_timeout ? 200000000LL : 1000000000LL;
+  cudaError_t e = launch_fused(fa, items, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
+                moonep_comm_plan *plan, cudaStream_t st) {
+  const PlanDims d = plan_dims(ctx);
   const bool dup = (plan->flags & MOONEP_PLAN_DUP_RECORDS) != 0;
   PlanLayout lay = PlanLayout::make(d.R, d.E, d.B, d.NvS, dup);
   int32_t *in = plan->internal;
@@ -1277,11 +1362,12 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     e = cudaMemsetAsync(dupflag, 0, (size_t)d.R * d.NvS * sizeof(int32_t), st);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  PlanOut o{plan->dst, plan->experts_to_copy, plan->cu_seqlens, plan->zero_fill_ranges,
-            plan->remote_stats, plan->dup_counts, plan->dup_groups, plan->dup_loffs};
+  const PlanOut o = plan_out(plan);
   const int fused_k = plan_fused_choice(d.R, d.E, d.K, d.B, d.C, ctx->sms_device);
   if (fused_k > 0 && ctx->d_sync != nullptr) {
     FusedArgs fa;
+    fa.src_rank = -1;
+    fa.hist_all = nullptr;
     fa.d = d;
     fa.topk = topk;
     fa.tpe = tpe;
@@ -1299,12 +1385,7 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     fa.dupflag = dupflag;
     fa.unreachable = ctx->test_planner_timeout;
     fa.wait_ns = ctx->test_planner_timeout ? 200000000LL : 1000000000LL;
-    const size_t smem = fused_smem_words(d.R, d.E, d.B) * sizeof(int32_t);
-    const dim3 grid(fa.G + 2), block(kFusedThreads);
-    e = items == 1   ? launch_pdl(plan_fused_kernel<1>, grid, block, smem, st, true, fa)
-        : items == 2 ? launch_pdl(plan_fused_kernel<2>, grid, block, smem, st, true, fa)
-        : items == 4 ? launch_pdl(plan_fused_kernel<4>, grid, block, smem, st, true, fa)
-                     : launch_pdl(plan_fused_kernel<8>, grid, block, smem, st, true, fa);
+    e = launch_fused(fa, items, st);
     if (e != cudaSuccess) return cuda_status(e);
   } else {
     e = cudaMemsetAsync(in, 0, kMetaWords * sizeof(int32_t), st);

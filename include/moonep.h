@@ -174,6 +174,61 @@ int moonep_plan_clone(const moonep_comm_plan *src, moonep_comm_plan *dst, void *
 int moonep_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
                 moonep_comm_plan *plan, void *stream);
 
+/* Rank-local planner: the per-rank form of moonep_plan when each of the R
+ * ranks is its own GPU [API, Buffer.dispatch(...): planning is collective,
+ * every rank plans from the cross-rank statistics (MoonEPCommPlan
+ * remote_stats); README, "How to set B"].  The one exchange step is an
+ * all-gather of every rank's [E] tokens_per_expert into hist_all; each rank
+ * then derives the same balance tables from hist_all and assigns only its own
+ * routes, so no other routing data crosses between ranks.
+ *   rank      source rank r of this call, 0 <= r < R
+ *   topk_r    [S, K] int32 expert ids of rank r only
+ *   hist_all  [R, E] int32 gathered per-rank histograms; row r is checked
+ *             against a recount of topk_r (a mismatch latches
+ *             MOONEP_ERR_HIST_MISMATCH; the tables stay those of hist_all,
+ *             which every rank shares, and rank r's rows are unspecified)
+ * Writes rank r's row of dst ([S*K] at plan->dst + r*S*K; other rows are not
+ * touched), and experts_to_copy, cu_seqlens, zero_fill_ranges, remote_stats
+ * and the plan's internal tables for every rank, equal to moonep_plan's.
+ * dup_counts[j] is written with rank r's share: {duplicate routes of rank
+ * r's tokens landing on rank j, their groups}; summed over the R calls (an
+ * all-reduce across GPUs) it equals moonep_plan's.  The R calls together
+ * give moonep_plan's plan, bit for bit.  Plans with MOONEP_PLAN_DUP_RECORDS,
+ * and configurations whose planner tables do not fit in shared memory, are
+ * refused (MOONEP_ERR_INVALID_ARG).  Rank-local calls of one context must
+ * not overlap on the GPU (they share its scratch, as moonep_plan calls do). */
+int moonep_plan_rank(moonep_ctx *ctx, int rank, const int32_t *topk_r,
+                     const int32_t *hist_all, moonep_comm_plan *plan, void *stream);
+
+/* Rank-local dispatch [API, Buffer.dispatch(...): tokens written straight
+ * into the receiving ranks' buffers; README item 3]: rank r's tokens go to
+ * their K destination rows in R rank windows, each its own allocation (on R
+ * GPUs, peer pointers), and rank r zero-fills the padding rows of its own
+ * window.  The R calls together give moonep_dispatch's rows.
+ *   hidden_r   [S, H] bf16 rows of rank r
+ *   w_r        [S, K] fp32 route weights of rank r, or NULL
+ *   windows    HOST array of R device pointers: windows[j] = rank j's
+ *              [NvS, H] bf16 rows (16-byte aligned)
+ *   w_windows  HOST array of R device pointers to [NvS] fp32, or NULL
+ *              (given exactly when w_r is)
+ * Uses the plan's dst row r and its tables (moonep_plan or moonep_plan_rank). */
+int moonep_dispatch_rank(moonep_ctx *ctx, const moonep_comm_plan *plan, int rank,
+                         const uint16_t *hidden_r, const float *w_r,
+                         uint16_t *const *windows, float *const *w_windows, void *stream);
+
+/* Rank-local combine [API, Buffer.combine(...): the owner gathers its
+ * tokens' K rows and reduces them; vLLM finalize(): an unweighted K-sum]:
+ * out_r[s,:] = bf16_rne(fp32 sum over k = 0..K-1, in k order, of the row
+ * |dst(r,s,k)| read from the rank window that holds it).
+ *   y_windows  HOST array of R device pointers: rank j's [NvS, H] bf16 rows
+ *   w_windows  HOST array of R device pointers to [NvS] fp32, or NULL
+ *   out_r      [S, H] bf16 out
+ *   w_out_r    [S, K] fp32 out (bit copies of the routes' weights), given
+ *              exactly when w_windows is */
+int moonep_combine_rank(moonep_ctx *ctx, const moonep_comm_plan *plan, int rank,
+                        const uint16_t *const *y_windows, const float *const *w_windows,
+                        uint16_t *out_r, float *w_out_r, void *stream);
+
 /* Planner for callers that cannot allocate device memory.  The pages have no
  * counterpart: it exists for callers that must not call cudaMalloc, such as a
  * framework whose caching allocator owns (and accounts for) all device memory,

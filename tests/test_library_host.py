@@ -78,6 +78,9 @@ def test_null_arguments_rejected(lib):
     assert lib.moonep_plan_destroy(None) == 0
     assert lib.moonep_prepare(None, None, None, None, None, None, None) == ERR_INVALID_ARG
     assert lib.moonep_prefetch_rows(None, None, 1, None, None, None) == ERR_INVALID_ARG
+    assert lib.moonep_plan_rank(None, 0, None, None, None, None) == ERR_INVALID_ARG
+    assert lib.moonep_dispatch_rank(None, None, 0, None, None, None, None, None) == ERR_INVALID_ARG
+    assert lib.moonep_combine_rank(None, None, 0, None, None, None, None, None) == ERR_INVALID_ARG
 
 
 def test_buffer_pool_capacities():

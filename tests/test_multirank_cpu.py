@@ -1,10 +1,12 @@
-"""The benchmark's multi-process path on CPU (gloo, world size 2).
+"""Multi-process host logic on CPU (gloo, world size 2).
 
 Each process of `bench.py --gpus N` runs the whole R-rank problem on its own
 GPU, so the only cross-process traffic is the barrier and the max of the step
 times.  These tests run that host-side logic with two CPU processes: the
 reference arm under torchrun (rank 0 prints the one JSON line, the other rank
-exits cleanly) and the max-over-ranks reduction.
+exits cleanly) and the max-over-ranks reduction.  They also run the
+rank-local path's one exchange step, the all-gather of every rank's [E]
+tokens_per_expert that feeds moonep_plan_rank, with one process per EP rank.
 """
 import json
 import os
@@ -64,3 +66,39 @@ def test_max_over_ranks_with_gloo():
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert got == [(0, 15.0), (1, 15.0)]
+
+
+def _gather_worker(rank, world, port, q):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    sys.path.insert(0, ROOT)
+    from combine_moonep_plan_gb300 import workloads as wl
+    from combine_moonep_plan_gb300.api import gather_tokens_per_expert
+    sh = wl.Shape("x", R=world, E=12, K=3, S=40, H=8, Hp=8, B=6, tp=4, weights="softmax")
+    # every process draws the same seeded routing and keeps its own rank's rows
+    topk, _ = wl.routing(sh, "zipf", zipf_s=1.5, seed=77)
+    mine = torch.from_numpy(topk[rank].reshape(-1).astype(np.int64))
+    tpe = torch.bincount(mine, minlength=sh.E).to(torch.int32)
+    hist = gather_tokens_per_expert(tpe)
+    q.put((rank, hist.numpy().tolist(), wl.tokens_per_expert(topk, sh.E).tolist()))
+    dist.destroy_process_group()
+
+
+def test_histogram_all_gather_feeds_every_rank_the_same_counts():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gather_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=300)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    (r0, h0, want0), (r1, h1, want1) = got
+    assert (r0, r1) == (0, 1)
+    assert h0 == h1 == want0 == want1     # [R, E], rows in rank order, on every rank
