@@ -211,14 +211,18 @@ class Step:
         self.Gs = torch.randn((R, B, H, Hp), generator=g, device=dev)
         self.plan = buf.new_plan()
 
-    def run(self, events=None):
+    def plan_dispatch(self, rec=lambda i: None):
         b = self.buf
-        rec = (lambda i: events[i].record()) if events else (lambda i: None)
-        rec(0)
         b.plan(self.topk, self.tpe, plan=self.plan)
         rec(1)
         b.dispatch(self.hidden, self.w_sk, plan=self.plan, out=self.hid_nvsh,
                    weights_out=self.w_nvs)
+
+    def run(self, events=None):
+        b = self.buf
+        rec = (lambda i: events[i].record()) if events else (lambda i: None)
+        rec(0)
+        self.plan_dispatch(rec)
         rec(2)
         b.combine(self.plan, self.hid_nvsh, self.w_nvs, out=self.out, weights_out=self.w_back)
         rec(3)
@@ -229,7 +233,7 @@ class Step:
         b.reduce_grad(self.plan, [self.Gh], [self.Gs])
         rec(6)
 
-    LAUNCHES_PER_STEP = 6  # plan (one cooperative launch), dispatch, combine, prefetch, dispatch, reduce
+    LAUNCHES_PER_STEP = 6  # plan (one launch), dispatch, combine, prefetch, dispatch, reduce
 
     def algorithmic_bytes(self):
         """Bytes each op must move (reads + writes), per launch."""
@@ -286,9 +290,7 @@ def time_chain(step, n, torch, graph=False):
     b = step.buf
 
     def chain():
-        b.plan(step.topk, step.tpe, plan=step.plan)
-        b.dispatch(step.hidden, step.w_sk, plan=step.plan, out=step.hid_nvsh,
-                   weights_out=step.w_nvs)
+        step.plan_dispatch()
         b.combine(step.plan, step.hid_nvsh, step.w_nvs, out=step.out, weights_out=step.w_back)
     run = chain
     if graph:
@@ -533,8 +535,8 @@ def run_e2e(buf, sh, topk_np, seed, steps, torch, dist):
                 compute.wait_event(inputs_ready[b])
                 if used[b]:
                     compute.wait_event(read_back[b])  # step i-2's result has been read
-                buf.plan(d["topk"], d["tpe"], plan=plan)
-                buf.dispatch(d["hidden"], d["w_sk"], plan=plan, out=hid_nvsh, weights_out=w_nvs)
+                buf.dispatch(d["hidden"], d["w_sk"], d["topk"], d["tpe"], out=hid_nvsh,
+                             weights_out=w_nvs, plan_out=plan)
                 buf.combine(plan, hid_nvsh, w_nvs, out=d["out"], weights_out=d["w_back"])
                 compute.record_event(computed[b])
             with torch.cuda.stream(d2h):

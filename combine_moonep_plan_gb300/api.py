@@ -196,20 +196,28 @@ class Buffer:
                  tokens_per_expert: torch.Tensor | None = None, plan: CommPlan | None = None,
                  zero_copy: bool = False, router_weights_zero_copy: bool = False,
                  out: torch.Tensor | None = None, weights_out: torch.Tensor | None = None,
-                 dedup: bool = False):
-        """Fresh dispatch (plan is None) or plan-reuse dispatch [Buffer.dispatch].
-        dedup=True copies only the primary rows and expands the duplicates in
-        an epilogue (same result; needs a Buffer made with dup_records=True).
+                 dedup: bool = False, plan_out: CommPlan | None = None):
+        """Fresh dispatch (plan is None: plan then dispatch, into plan_out or
+        a new plan) or plan-reuse dispatch [Buffer.dispatch].  dedup=True
+        copies only the primary rows and expands the duplicates in an
+        epilogue (same result; needs a Buffer made with dup_records=True).
 
         Returns (hidden_nvsh [R*NvS, H] bf16, route_weights_nvs [R*NvS] fp32 or
         None, cu_seqlens [R, E+B] int32 (None on plan reuse), plan)."""
         R, S, H, K, NvS = self.R, self.S, self.H, self.K, self.NvS
         hp = _check_tensor(hidden_sh, "hidden_sh", torch.bfloat16, (R, S, H))
         fresh = plan is None
+        tk = tp = None
         if fresh:
             if topk_experts_sk is None:
                 raise ValueError("a fresh dispatch needs topk_experts_sk")
-            plan = self.plan(topk_experts_sk, tokens_per_expert)
+            tk = _check_tensor(topk_experts_sk, "topk_experts_sk", torch.int32, (R, S, K))
+            if tokens_per_expert is not None:
+                tp = _check_tensor(tokens_per_expert, "tokens_per_expert", torch.int32,
+                                   (R, self.E))
+            plan = self.new_plan() if plan_out is None else plan_out
+            check(_lib.load().moonep_plan(self._ctx, tk, tp, plan.struct, _stream()),
+                  "moonep_plan")
         if out is None:
             out = self.hidden_nvsh_buffer_view() if zero_copy else torch.empty(
                 (R * NvS, H), dtype=torch.bfloat16, device=hidden_sh.device)

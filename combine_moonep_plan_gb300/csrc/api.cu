@@ -117,8 +117,8 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
   const size_t ord = (size_t)c.R * ctx->C * sizeof(int32_t);
   e = cudaMalloc(&ctx->d_status, 256);
   if (e == cudaSuccess) e = cudaMemset(ctx->d_status, 0, 256);
-  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_sync, 2 * sizeof(unsigned long long));
-  if (e == cudaSuccess) e = cudaMemset(ctx->d_sync, 0, 2 * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_sync, kSyncWords * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_sync, 0, kSyncWords * sizeof(unsigned long long));
   if (e == cudaSuccess && hist) e = cudaMalloc(&ctx->d_hist, hist);
   if (e == cudaSuccess && hist) e = cudaMemset(ctx->d_hist, 0, hist);
   if (e == cudaSuccess && ord) e = cudaMalloc(&ctx->d_ord, ord);
@@ -132,6 +132,7 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
     const char *t = getenv("MOONEP_TEST_PLANNER_TIMEOUT");
     ctx->test_planner_timeout = (t && t[0] == '1') ? 1 : 0;
   }
+  if (e == cudaSuccess) ctx->plan_cluster = plan_cluster_blocks(ctx);
   if (e != cudaSuccess) {
     cudaFree(ctx->d_status);
     cudaFree(ctx->d_sync);
@@ -465,7 +466,7 @@ int moonep_get_status(moonep_ctx *ctx, int *device_status, void *stream) {
     const moonep_config &c = ctx->cfg;
     const int64_t off = plan_totals_offset(c.R, c.E, ctx->C, c.K, ctx->sms_device);
     const int64_t words = plan_scratch_words(c.R, c.E, ctx->C, c.K, ctx->sms_device) - off;
-    e = cudaMemset(ctx->d_sync, 0, 2 * sizeof(unsigned long long));
+    e = cudaMemset(ctx->d_sync, 0, kSyncWords * sizeof(unsigned long long));
     if (e == cudaSuccess) e = cudaMemset(ctx->d_hist + off, 0, (size_t)words * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
   }

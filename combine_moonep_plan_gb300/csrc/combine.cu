@@ -37,6 +37,7 @@ struct Args {
   int64_t ntok;
   int64_t total_rows;
   int K, H8, nchunk, NvS;
+  int interleave;  // number warps across blocks first (small batches)
 };
 
 // Source addressing of global row g = j*NvS + w: one [R*NvS, H] buffer, or
@@ -109,7 +110,10 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a, Rows rows) {
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
-  const int64_t wid = ((int64_t)blockIdx.x * BT + threadIdx.x) >> 5;
+  // small batches (a few units per warp): warps numbered across blocks
+  // first, so the units of the last round spread over every SM
+  const int64_t wid = a.interleave ? (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x
+                                   : ((int64_t)blockIdx.x * BT + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * BT) >> 5;
   const int K = KT > 0 ? KT : a.K;
   const int64_t units = a.ntok * a.nchunk;
@@ -240,6 +244,8 @@ Args make_args(const moonep_ctx *ctx, const moonep_comm_plan *plan, int64_t ntok
   const int U = unit_vectors(c.K);
   a.nchunk = (a.H8 + 32 * U - 1) / (32 * U);
   a.NvS = ctx->NvS;
+  const int bt = c.K == 1 ? 256 : 128;
+  a.interleave = ntok * a.nchunk <= 4 * (int64_t)ctx->sms * ctx->blocks_combine * (bt / 32);
   return a;
 }
 

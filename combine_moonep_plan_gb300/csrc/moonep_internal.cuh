@@ -15,6 +15,11 @@ namespace moonep {
 // shared memory; the rank-local copy kernels take one window per rank).
 constexpr int kMaxRanks = 64;
 
+// The planner's arrival counters (ctx->d_sync), each on its own 128-byte
+// line: whole-problem calls at word 0, rank-local calls at kSyncRankLocal.
+constexpr int kSyncWords = 32;  // 64-bit words
+constexpr int kSyncRankLocal = 16;
+
 // Routes handled by one planner tile: 8 warps x 32 lanes x 8 routes.
 constexpr int kPlanThreads = 256;
 constexpr int kPlanItems = 8;
@@ -101,8 +106,10 @@ struct moonep_ctx {
   int32_t *d_ord;      // [R*C] ordinal of a route among its tile's routes to the same expert
   uint16_t *d_hidden_view;  // optional [R*NvS, H] bf16
   float *d_weight_view;     // optional [R*NvS] fp32
-  unsigned long long *d_sync;  // [2] planner arrival counters: every-rank calls, rank-local calls
+  unsigned long long *d_sync;  // [kSyncWords] the planner's counters (kSync*)
   int test_planner_timeout;    // test hook: the planner's arrival wait never completes
+  int plan_cluster;            // blocks of the whole-problem planner launched as one
+                               // cluster (0: a cooperative launch)
   int blocks_dispatch, blocks_combine, blocks_copy, blocks_reduce, blocks_expand,
       blocks_fold;  // resident blocks per SM
 };
@@ -150,6 +157,9 @@ int launch_reduce(moonep_ctx *ctx, const moonep_comm_plan *plan, int n_proj, flo
                   float *const *Gs, int64_t HHp, cudaStream_t st);
 // Opt the planner kernels into the dynamic shared memory E experts need.
 cudaError_t plan_configure(int R, int E, int B);
+// Blocks of the single-launch planner when they can run as one thread-block
+// cluster on this device (at most 16), else 0.
+int plan_cluster_blocks(const moonep_ctx *ctx);
 // K when the single-launch planner handles this shape (0: the tile path).
 int plan_fused_choice(int R, int E, int K, int B, int C, int sms);
 // Tiles the histogram area must hold (either planner path).
@@ -180,15 +190,17 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// cluster > 1: the grid is one or more thread-block clusters of that many
+// blocks (every block of a cluster is resident at once, on one GPC).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t st, bool cooperative, Args &&...args) {
+cudaError_t launch_pdl_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool cooperative, int cluster, Args &&...args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int n = 0;
   attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[n].val.programmaticStreamSerializationAllowed = 1;
@@ -198,9 +210,23 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[n].val.cooperative = 1;
     n++;
   }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    n++;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, bool cooperative, Args &&...args) {
+  return launch_pdl_ex(kernel, grid, block, smem, st, cooperative, 1,
+                       std::forward<Args>(args)...);
 }
 
 // Latch the first error code into the status word.

@@ -816,6 +816,10 @@ struct FusedArgs {
   const int32_t *hist_all;
   int unreachable;    // test hook: the arrival wait can never be satisfied
   long long wait_ns;  // limit of each wait
+  // The launch is one thread-block cluster: its blocks meet at the cluster's
+  // hardware barrier instead of polling the arrival counter (which still
+  // counts the calls).
+  int cluster;
 };
 
 __device__ __forceinline__ long long globaltimer_ns() {
@@ -946,10 +950,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     const unsigned long long n = (unsigned long long)nblk;
     const unsigned long long old = atomicAdd(a.sync, 1ull);
     const unsigned long long target = old - old % n + n;
-    s_ok = wait_counter(a.sync, target + (a.unreachable ? 1 : 0), a.wait_ns);
+    s_ok = a.cluster ? 1 : wait_counter(a.sync, target + (a.unreachable ? 1 : 0), a.wait_ns);
     if (!s_ok) set_status(a.status, MOONEP_ERR_TIMEOUT);
-    s_err = s_ok ? __ldcg(a.errw + s_par) : 0;
   }
+  if (a.cluster) {
+    // every thread of every block of the cluster; the release/acquire pair
+    // orders the blocks' histogram, totals and error-bit writes before the
+    // reads that follow
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  }
+  if (tid == 0) s_err = s_ok ? __ldcg(a.errw + s_par) : 0;
   __syncthreads();
   const bool ok = s_ok;
   if (ok) {
@@ -1309,10 +1320,52 @@ static PlanOut plan_out(const moonep_comm_plan *plan) {
 static cudaError_t launch_fused(const FusedArgs &fa, int items, cudaStream_t st) {
   const size_t smem = fused_smem_words(fa.d.R, fa.d.E, fa.d.B) * sizeof(int32_t);
   const dim3 grid(fa.G + 2), block(kFusedThreads);
-  return items == 1   ? launch_pdl(plan_fused_kernel<1>, grid, block, smem, st, true, fa)
-         : items == 2 ? launch_pdl(plan_fused_kernel<2>, grid, block, smem, st, true, fa)
-         : items == 4 ? launch_pdl(plan_fused_kernel<4>, grid, block, smem, st, true, fa)
-                      : launch_pdl(plan_fused_kernel<8>, grid, block, smem, st, true, fa);
+  // one cluster of G + 2 blocks (co-resident by construction), else a
+  // cooperative launch
+  const bool coop = fa.cluster == 0;
+  const int cl = fa.cluster ? fa.G + 2 : 1;
+  return items == 1   ? launch_pdl_ex(plan_fused_kernel<1>, grid, block, smem, st, coop, cl, fa)
+         : items == 2 ? launch_pdl_ex(plan_fused_kernel<2>, grid, block, smem, st, coop, cl, fa)
+         : items == 4 ? launch_pdl_ex(plan_fused_kernel<4>, grid, block, smem, st, coop, cl, fa)
+                      : launch_pdl_ex(plan_fused_kernel<8>, grid, block, smem, st, coop, cl, fa);
+}
+
+// Largest cluster a launch may ask for (non-portable sizes above 8).
+constexpr int kMaxPlanCluster = 16;
+
+int plan_cluster_blocks(const moonep_ctx *ctx) {
+  const moonep_config &c = ctx->cfg;
+  if (ctx->test_planner_timeout || !ctx->d_sync) return 0;
+  if (plan_fused_choice(c.R, c.E, c.K, c.B, ctx->C, ctx->sms_device) == 0) return 0;
+  const int items = plan_fused_items(c.R, ctx->C, c.K, ctx->sms_device);
+  const int nblk = c.R * plan_fused_tiles(ctx->C, c.K, items) + 2;
+  if (nblk > kMaxPlanCluster) return 0;
+  const void *f = items == 1   ? (const void *)plan_fused_kernel<1>
+                  : items == 2 ? (const void *)plan_fused_kernel<2>
+                  : items == 4 ? (const void *)plan_fused_kernel<4>
+                               : (const void *)plan_fused_kernel<8>;
+  if (nblk > 8 &&
+      cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nblk);
+  cfg.blockDim = dim3(kFusedThreads);
+  cfg.dynamicSmemBytes = fused_smem_words(c.R, c.E, c.B) * sizeof(int32_t);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = nblk;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, f, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return clusters >= 1 ? nblk : 0;
 }
 
 int plan_rank_supported(const moonep_ctx *ctx) {
@@ -1341,10 +1394,11 @@ int launch_plan_rank(moonep_ctx *ctx, int rank, const int32_t *topk_r, const int
   fa.in = plan->internal;
   fa.lay = PlanLayout::make(d.R, d.E, d.B, d.NvS, false);
   fa.status = ctx->d_status;
-  fa.sync = ctx->d_sync + 1;  // the rank-local calls' own arrival counter
+  fa.sync = ctx->d_sync + kSyncRankLocal;  // the rank-local calls' own arrival counter
   fa.dupflag = nullptr;
   fa.unreachable = ctx->test_planner_timeout;
   fa.wait_ns = ctx->test_planner_timeout ? 200000000LL : 1000000000LL;
+  fa.cluster = 0;
   cudaError_t e = launch_fused(fa, items, st);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(cudaGetLastError());
@@ -1385,6 +1439,7 @@ int launch_plan(moonep_ctx *ctx, const int32_t *topk, const int32_t *tpe,
     fa.dupflag = dupflag;
     fa.unreachable = ctx->test_planner_timeout;
     fa.wait_ns = ctx->test_planner_timeout ? 200000000LL : 1000000000LL;
+    fa.cluster = ctx->plan_cluster == fa.G + 2 ? 1 : 0;
     e = launch_fused(fa, items, st);
     if (e != cudaSuccess) return cuda_status(e);
   } else {
