@@ -22,6 +22,8 @@
 // separately allocated rank windows) is the same kernel with another row
 // addressing: the per-GPU shape of the combine when each rank is a GPU and
 // the owner pulls its rows from its peers.
+#include <mutex>
+
 #include "copy_common.cuh"
 #include "moonep_internal.cuh"
 
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a, Rows rows) {
         uint4 x[KB][U];
 #pragma unroll
         for (int kk = 0; kk < KB; kk++) {
+          if (k0 + kk >= KK) continue;  // the last batch of a K that KB does not divide
           const uint4 *row = rows.row(__shfl_sync(0xffffffffu, g, k0 + kk), a.H8, a.NvS);
           const bool skip = (dupm >> (k0 + kk)) & 1u;
 #pragma unroll
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a, Rows rows) {
         for (int i = 0; i < U; i++) {
 #pragma unroll
           for (int kk = 0; kk < KB; kk++) {
-            if ((dupm >> (k0 + kk)) & 1u) continue;
+            if (k0 + kk >= KK || ((dupm >> (k0 + kk)) & 1u)) continue;
             if (k0 + kk == 0) set_bf16x8(acc[i], x[kk][i]);
             else add_bf16x8(acc[i], x[kk][i]);
           }
@@ -201,6 +204,151 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a, Rows rows) {
   }
 }
 
+// ------------------------------------------------ staged combine (any K)
+//
+// For a K without a register-tuned batch shape: one warp per block; every
+// unit's K row chunks (2 KB each) are copied into shared memory by the bulk
+// copy engine (cp.async.bulk, completion counted on an mbarrier), two stages
+// deep, so the next unit's K chunks are in flight while the warp sums the
+// current one from shared memory.  Bytes in flight no longer depend on
+// registers: K * 2 KB per warp and stage.  Same arithmetic as combine_kernel:
+// fp32 adds in k order from the k = 0 row, one RNE rounding.
+
+constexpr int kStageChunk = 2048;  // bytes of a row per unit
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(mbar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for a stage's copies; gives up after limit_ns (the copies of valid
+// addresses always complete, so this only bounds a broken run).
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long long limit_ns) {
+  if (mbar_try_wait(mbar, parity)) return true;
+  long long t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (!mbar_try_wait(mbar, parity)) {
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+template <class Rows>
+__global__ void __launch_bounds__(32) combine_staged_kernel(Args a, Rows rows) {
+  pdl_wait();
+  pdl_launch_dependents();
+  extern __shared__ __align__(128) uint8_t stage_mem[];
+  const int lane = threadIdx.x;
+  const int K = a.K;
+  const int stage_bytes = K * kStageChunk;
+  const uint32_t buf0 = smem_u32(stage_mem);
+  const uint32_t mbar0 = buf0 + 2 * stage_bytes;  // two mbarriers after the two stages
+  if (lane == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  const int64_t row_bytes = (int64_t)a.H8 * 16;
+  const int nchunk = a.nchunk;
+  const int64_t units = a.ntok * nchunk;
+  const int64_t nw = gridDim.x;  // one warp per block
+  const int64_t u0 = blockIdx.x;
+  const long long limit_ns = 1000000000LL;
+  unsigned pending = 0;  // bit s: stage s has copies in flight
+
+  // issue unit u's K chunk copies into stage s (d: this lane's dst entry)
+  auto issue = [&](int64_t u, int st, int32_t d) {
+    const int64_t t = u / nchunk;
+    const int c = (int)(u - t * nchunk);
+    const int64_t off = (int64_t)c * kStageChunk;
+    const int bytes = (int)min((int64_t)kStageChunk, row_bytes - off);
+    const uint32_t mbar = mbar0 + 8 * st;
+    if (lane == 0)
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar),
+                   "r"(bytes * K)
+                   : "memory");
+    __syncwarp();
+    if (lane < K) {
+      int64_t g = decode_row(d);
+      if (g >= a.total_rows) {
+        set_status(a.status, MOONEP_ERR_PLAN);
+        g = 0;
+      }
+      const uint8_t *src = reinterpret_cast<const uint8_t *>(rows.row(g, a.H8, a.NvS)) + off;
+      const uint32_t dst = buf0 + st * stage_bytes + lane * kStageChunk;
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+          ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar)
+          : "memory");
+    }
+    pending |= 1u << st;
+  };
+
+  int32_t d_cur = 0, d_nxt = 0;
+  if (u0 < units && lane < K) d_cur = __ldg(a.dst + (u0 / nchunk) * K + lane);
+  if (u0 < units) issue(u0, 0, d_cur);
+  if (u0 + nw < units && lane < K) d_nxt = __ldg(a.dst + ((u0 + nw) / nchunk) * K + lane);
+  uint32_t phase = 0;  // bit s: parity of stage s's next completion
+  int s = 0;
+  for (int64_t u = u0; u < units; u += nw) {
+    const int64_t un = u + nw;
+    if (un < units) issue(un, s ^ 1, d_nxt);
+    int32_t d_far = 0;
+    if (un + nw < units && lane < K) d_far = __ldg(a.dst + ((un + nw) / nchunk) * K + lane);
+    if (!mbar_wait(mbar0 + 8 * s, (phase >> s) & 1u, limit_ns)) {
+      set_status(a.status, MOONEP_ERR_TIMEOUT);
+      break;
+    }
+    pending &= ~(1u << s);
+    phase ^= 1u << s;
+    const int64_t t = u / nchunk;
+    const int c = (int)(u - t * nchunk);
+    if (c == 0 && a.w_out && lane < K) {
+      int64_t g = decode_row(d_cur);
+      if (g >= a.total_rows) g = 0;
+      a.w_out[t * K + lane] = __ldg(rows.weight(g, a.NvS));
+    }
+    // this lane's 16-byte vectors of the chunk: lane + 32 * i
+    const uint8_t *stage = stage_mem + s * stage_bytes;
+    const int vmax = (int)(min((int64_t)kStageChunk, row_bytes - (int64_t)c * kStageChunk) / 16);
+    uint4 *op = a.out + t * a.H8 + (int64_t)c * (kStageChunk / 16);
+#pragma unroll
+    for (int i = 0; i < kStageChunk / 512; i++) {
+      const int v = lane + 32 * i;
+      if (v >= vmax) continue;
+      float acc[8];
+      set_bf16x8(acc, *reinterpret_cast<const uint4 *>(stage + v * 16));
+      for (int k = 1; k < K; k++)
+        add_bf16x8(acc, *reinterpret_cast<const uint4 *>(stage + k * kStageChunk + v * 16));
+      st_global(op + v, pack_bf16x8(acc));
+    }
+    // the generic-proxy reads of this stage come before the copies that
+    // refill it (issued at the next iteration)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    d_cur = d_nxt;
+    d_nxt = d_far;
+    s ^= 1;
+  }
+  // a wait that gave up leaves copies in flight into this block's shared
+  // memory: wait for them (bounded) before the block exits
+  for (int st = 0; st < 2; st++)
+    if (pending & (1u << st)) mbar_wait(mbar0 + 8 * st, (phase >> st) & 1u, limit_ns);
+}
+
 template <int KT, int U, int BT, int KB, class Rows>
 cudaError_t launch(const Args &a, const Rows &rows, bool prim, int grid, cudaStream_t st) {
   if constexpr (Rows::kPrimaries) {
@@ -209,6 +357,49 @@ cudaError_t launch(const Args &a, const Rows &rows, bool prim, int grid, cudaStr
                         rows);
   }
   return launch_pdl(combine_kernel<KT, U, BT, KB, false, Rows>, grid, BT, 0, st, false, a, rows);
+}
+
+// The staged kernel's shared memory for K rows: two stages of K 2 KB chunks
+// and two mbarriers; blocks per SM (one warp each), cached per K.
+size_t staged_smem(int K) { return (size_t)2 * K * kStageChunk + 16; }
+
+template <class Rows>
+int staged_blocks_per_sm(int K) {
+  static int cache[33];  // K up to 32
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[K] == 0) {
+    const size_t smem = staged_smem(K);
+    int n = 0;
+    // the limit is set once for the largest K (a per-K setting would lower
+    // it below what an earlier K needs)
+    if (cudaFuncSetAttribute(combine_staged_kernel<Rows>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)staged_smem(32)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, combine_staged_kernel<Rows>, 32,
+                                                      smem) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cache[K] = n > 0 ? n : -1;
+  }
+  return cache[K];
+}
+
+// K with a register-tuned batch shape (combine_kernel); every other K up to
+// 32 takes the staged kernel (direct combine only).
+bool staged_k(int K) {
+  return !(K == 1 || K == 2 || K == 3 || K == 4 || K == 6 || K == 8 || K == 10);
+}
+
+template <class Rows>
+cudaError_t launch_staged(const Args &a, const Rows &rows, int sms, cudaStream_t st) {
+  const int per_sm = staged_blocks_per_sm<Rows>(a.K);
+  if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+  Args b = a;
+  b.nchunk = (int)((int64_t)a.H8 * 16 + kStageChunk - 1) / kStageChunk;
+  return launch_pdl(combine_staged_kernel<Rows>, sms * per_sm, 32, staged_smem(a.K), st, false,
+                    b, rows);
 }
 
 // Batch shape per K (vectors per lane, threads per block, rows per batch),
@@ -273,6 +464,7 @@ int launch_combine(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_t
   Args a = make_args(ctx, plan, (int64_t)c.R * c.S, 0, out, w_out);
   if (a.ntok == 0 || a.H8 == 0) return MOONEP_OK;
   FlatRows rows{reinterpret_cast<const uint4 *>(y), w_nvs};
+  if (!primaries_only && staged_k(c.K)) return cuda_status(launch_staged(a, rows, ctx->sms, st));
   return cuda_status(launch_k(a, rows, primaries_only, ctx->sms * ctx->blocks_combine, st));
 }
 
@@ -287,6 +479,7 @@ int launch_combine_rank(moonep_ctx *ctx, const moonep_comm_plan *plan, int rank,
     rows.y[j] = j < c.R ? reinterpret_cast<const uint4 *>(y_windows[j]) : nullptr;
     rows.w_nvs[j] = (w_windows && j < c.R) ? w_windows[j] : nullptr;
   }
+  if (staged_k(c.K)) return cuda_status(launch_staged(a, rows, ctx->sms, st));
   return cuda_status(launch_k(a, rows, false, ctx->sms * ctx->blocks_combine, st));
 }
 
