@@ -39,6 +39,7 @@ struct Args {
   int64_t ntok;
   int64_t total_rows;
   int K, H8, nchunk, NvS;
+  int64_t nw;      // staged kernel: blocks (one warp each) that take units
   int interleave;  // number warps across blocks first (small batches)
 };
 
@@ -103,8 +104,9 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 // (0.98 of the copy bandwidth on the Mixtral shape, 0.95 with 2 KB); K = 3
 // reads 4 KB of one row at a time, K = 4 2 KB of two rows, K = 6 2 KB of three
 // rows (1.00-1.04 of the copy bandwidth each, where a runtime-K kernel gave
-// 0.66-0.78), K = 10 4 KB of one row at a time (0.85); any other K takes the
-// runtime-K kernel, four rows per batch.  PRIM: sum the primary
+// 0.66-0.78).  The direct combine of any other K takes the staged kernel
+// below; the primaries-only sum takes K = 10 as 4 KB of one row at a time and
+// the rest through the runtime-K kernel, four rows per batch.  PRIM: sum the primary
 // routes only (dst >= 0; the duplicates were folded into them), a separate
 // instantiation so that the direct kernel carries none of its code.
 template <int KT, int U, int BT, int KB, bool PRIM, class Rows>
@@ -207,14 +209,12 @@ __global__ void __launch_bounds__(BT) combine_kernel(Args a, Rows rows) {
 // ------------------------------------------------ staged combine (any K)
 //
 // For a K without a register-tuned batch shape: one warp per block; every
-// unit's K row chunks (2 KB each) are copied into shared memory by the bulk
-// copy engine (cp.async.bulk, completion counted on an mbarrier), two stages
-// deep, so the next unit's K chunks are in flight while the warp sums the
-// current one from shared memory.  Bytes in flight no longer depend on
-// registers: K * 2 KB per warp and stage.  Same arithmetic as combine_kernel:
-// fp32 adds in k order from the k = 0 row, one RNE rounding.
-
-constexpr int kStageChunk = 2048;  // bytes of a row per unit
+// unit's K row chunks (kChunk bytes each) are copied into shared memory by
+// the bulk copy engine (cp.async.bulk, completion counted on an mbarrier),
+// kStages deep, so the next units' K chunks are in flight while the warp sums
+// the current one from shared memory.  Bytes in flight no longer depend on
+// registers: (kStages - 1) * K * kChunk per warp.  Same arithmetic as
+// combine_kernel: fp32 adds in k order from the k = 0 row, one RNE rounding.
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -245,37 +245,43 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long l
   return true;
 }
 
-template <class Rows>
+template <int kChunk, int kStages, class Rows>
 __global__ void __launch_bounds__(32) combine_staged_kernel(Args a, Rows rows) {
+  static_assert(kChunk % 512 == 0 && kStages >= 2 && kStages <= 8, "stage shape");
   pdl_wait();
   pdl_launch_dependents();
+  if (blockIdx.x >= a.nw) return;
   extern __shared__ __align__(128) uint8_t stage_mem[];
   const int lane = threadIdx.x;
   const int K = a.K;
-  const int stage_bytes = K * kStageChunk;
+  const int stage_bytes = K * kChunk;
   const uint32_t buf0 = smem_u32(stage_mem);
-  const uint32_t mbar0 = buf0 + 2 * stage_bytes;  // two mbarriers after the two stages
+  const uint32_t mbar0 = buf0 + kStages * stage_bytes;  // one mbarrier per stage after them
   if (lane == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8) : "memory");
+    for (int q = 0; q < kStages; q++)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8 * q) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
   const int64_t row_bytes = (int64_t)a.H8 * 16;
   const int nchunk = a.nchunk;
   const int64_t units = a.ntok * nchunk;
-  const int64_t nw = gridDim.x;  // one warp per block
+  const int64_t nw = a.nw;  // one warp per block
   const int64_t u0 = blockIdx.x;
   const long long limit_ns = 1000000000LL;
-  unsigned pending = 0;  // bit s: stage s has copies in flight
+  unsigned pending = 0;  // bit q: stage q has copies in flight
 
-  // issue unit u's K chunk copies into stage s (d: this lane's dst entry)
-  auto issue = [&](int64_t u, int st, int32_t d) {
+  // this lane's dst entry of unit u (route k = lane)
+  auto dst_of = [&](int64_t u) -> int32_t {
+    return (u < units && lane < K) ? __ldg(a.dst + (u / nchunk) * K + lane) : 0;
+  };
+  // issue unit u's K chunk copies into stage q (d: this lane's dst entry)
+  auto issue = [&](int64_t u, int q, int32_t d) {
     const int64_t t = u / nchunk;
     const int c = (int)(u - t * nchunk);
-    const int64_t off = (int64_t)c * kStageChunk;
-    const int bytes = (int)min((int64_t)kStageChunk, row_bytes - off);
-    const uint32_t mbar = mbar0 + 8 * st;
+    const int64_t off = (int64_t)c * kChunk;
+    const int bytes = (int)min((int64_t)kChunk, row_bytes - off);
+    const uint32_t mbar = mbar0 + 8 * q;
     if (lane == 0)
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar),
                    "r"(bytes * K)
@@ -288,65 +294,63 @@ __global__ void __launch_bounds__(32) combine_staged_kernel(Args a, Rows rows) {
         g = 0;
       }
       const uint8_t *src = reinterpret_cast<const uint8_t *>(rows.row(g, a.H8, a.NvS)) + off;
-      const uint32_t dst = buf0 + st * stage_bytes + lane * kStageChunk;
+      const uint32_t dst = buf0 + q * stage_bytes + lane * kChunk;
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
           ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar)
           : "memory");
     }
-    pending |= 1u << st;
+    pending |= 1u << q;
   };
 
-  int32_t d_cur = 0, d_nxt = 0;
-  if (u0 < units && lane < K) d_cur = __ldg(a.dst + (u0 / nchunk) * K + lane);
-  if (u0 < units) issue(u0, 0, d_cur);
-  if (u0 + nw < units && lane < K) d_nxt = __ldg(a.dst + ((u0 + nw) / nchunk) * K + lane);
-  uint32_t phase = 0;  // bit s: parity of stage s's next completion
-  int s = 0;
+  // kStages - 1 units in flight ahead of the one being summed; the dst
+  // entries of the next unit to issue are loaded one iteration ahead
+  for (int p = 0; p < kStages - 1; p++)
+    if (u0 + p * nw < units) issue(u0 + p * nw, p, dst_of(u0 + p * nw));
+  int32_t d_pre = dst_of(u0 + (int64_t)(kStages - 1) * nw);
+  uint32_t phase = 0;  // bit q: parity of stage q's next completion
+  int q = 0;
   for (int64_t u = u0; u < units; u += nw) {
-    const int64_t un = u + nw;
-    if (un < units) issue(un, s ^ 1, d_nxt);
-    int32_t d_far = 0;
-    if (un + nw < units && lane < K) d_far = __ldg(a.dst + ((un + nw) / nchunk) * K + lane);
-    if (!mbar_wait(mbar0 + 8 * s, (phase >> s) & 1u, limit_ns)) {
+    const int64_t ua = u + (int64_t)(kStages - 1) * nw;
+    if (ua < units) issue(ua, q == 0 ? kStages - 1 : q - 1, d_pre);
+    d_pre = dst_of(ua + nw);
+    if (!mbar_wait(mbar0 + 8 * q, (phase >> q) & 1u, limit_ns)) {
       set_status(a.status, MOONEP_ERR_TIMEOUT);
       break;
     }
-    pending &= ~(1u << s);
-    phase ^= 1u << s;
+    pending &= ~(1u << q);
+    phase ^= 1u << q;
     const int64_t t = u / nchunk;
     const int c = (int)(u - t * nchunk);
     if (c == 0 && a.w_out && lane < K) {
-      int64_t g = decode_row(d_cur);
+      int64_t g = decode_row(__ldg(a.dst + t * K + lane));
       if (g >= a.total_rows) g = 0;
       a.w_out[t * K + lane] = __ldg(rows.weight(g, a.NvS));
     }
     // this lane's 16-byte vectors of the chunk: lane + 32 * i
-    const uint8_t *stage = stage_mem + s * stage_bytes;
-    const int vmax = (int)(min((int64_t)kStageChunk, row_bytes - (int64_t)c * kStageChunk) / 16);
-    uint4 *op = a.out + t * a.H8 + (int64_t)c * (kStageChunk / 16);
+    const uint8_t *stage = stage_mem + q * stage_bytes;
+    const int vmax = (int)(min((int64_t)kChunk, row_bytes - (int64_t)c * kChunk) / 16);
+    uint4 *op = a.out + t * a.H8 + (int64_t)c * (kChunk / 16);
 #pragma unroll
-    for (int i = 0; i < kStageChunk / 512; i++) {
+    for (int i = 0; i < kChunk / 512; i++) {
       const int v = lane + 32 * i;
       if (v >= vmax) continue;
       float acc[8];
       set_bf16x8(acc, *reinterpret_cast<const uint4 *>(stage + v * 16));
       for (int k = 1; k < K; k++)
-        add_bf16x8(acc, *reinterpret_cast<const uint4 *>(stage + k * kStageChunk + v * 16));
+        add_bf16x8(acc, *reinterpret_cast<const uint4 *>(stage + k * kChunk + v * 16));
       st_global(op + v, pack_bf16x8(acc));
     }
     // the generic-proxy reads of this stage come before the copies that
     // refill it (issued at the next iteration)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
-    d_cur = d_nxt;
-    d_nxt = d_far;
-    s ^= 1;
+    q = q + 1 == kStages ? 0 : q + 1;
   }
   // a wait that gave up leaves copies in flight into this block's shared
   // memory: wait for them (bounded) before the block exits
-  for (int st = 0; st < 2; st++)
-    if (pending & (1u << st)) mbar_wait(mbar0 + 8 * st, (phase >> st) & 1u, limit_ns);
+  for (int p = 0; p < kStages; p++)
+    if (pending & (1u << p)) mbar_wait(mbar0 + 8 * p, (phase >> p) & 1u, limit_ns);
 }
 
 template <int KT, int U, int BT, int KB, class Rows>
@@ -359,47 +363,65 @@ cudaError_t launch(const Args &a, const Rows &rows, bool prim, int grid, cudaStr
   return launch_pdl(combine_kernel<KT, U, BT, KB, false, Rows>, grid, BT, 0, st, false, a, rows);
 }
 
-// The staged kernel's shared memory for K rows: two stages of K 2 KB chunks
-// and two mbarriers; blocks per SM (one warp each), cached per K.
-size_t staged_smem(int K) { return (size_t)2 * K * kStageChunk + 16; }
+// Stage shape of the staged kernel per K (chunk bytes, stages).
+struct StageShape {
+  int chunk, stages;
+};
 
-template <class Rows>
-int staged_blocks_per_sm(int K) {
-  static int cache[33];  // K up to 32
+// Measured at H = 7168 over K = 5..32 and chunks of 1-2 KB with 2-4 stages:
+// two stages of 2 KB chunks reach 0.99-1.04 of the copy bandwidth up to
+// K = 13; from K = 14 on, 2 KB chunks leave three blocks or fewer per SM
+// (0.67-0.90), and 1 KB chunks, twice the blocks, reach 0.96-1.01 (0.85 at
+// K = 32).  More stages gained nothing (0.85-0.98).
+StageShape stage_shape(int K) { return K <= 13 ? StageShape{2048, 2} : StageShape{1024, 2}; }
+
+size_t staged_smem(int K, StageShape sh) { return (size_t)sh.stages * K * sh.chunk + 8 * sh.stages; }
+
+template <int kChunk, int kStages, class Rows>
+cudaError_t launch_staged_shape(const Args &a, const Rows &rows, int sms, cudaStream_t st) {
+  auto f = combine_staged_kernel<kChunk, kStages, Rows>;
+  const size_t smem = staged_smem(a.K, {kChunk, kStages});
+  // blocks per SM (one warp each), cached per K; the limit is set once for
+  // the largest K (a per-K setting would lower it below what an earlier K
+  // needs)
+  static int cache[33];
   static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cache[K] == 0) {
-    const size_t smem = staged_smem(K);
-    int n = 0;
-    // the limit is set once for the largest K (a per-K setting would lower
-    // it below what an earlier K needs)
-    if (cudaFuncSetAttribute(combine_staged_kernel<Rows>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)staged_smem(32)) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, combine_staged_kernel<Rows>, 32,
-                                                      smem) != cudaSuccess) {
-      cudaGetLastError();
-      n = 0;
+  int per_sm;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[a.K] == 0) {
+      int n = 0;
+      if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)staged_smem(32, {kChunk, kStages})) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, 32, smem) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      cache[a.K] = n > 0 ? n : -1;
     }
-    cache[K] = n > 0 ? n : -1;
+    per_sm = cache[a.K];
   }
-  return cache[K];
+  if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+  Args b = a;
+  b.nchunk = (int)(((int64_t)a.H8 * 16 + kChunk - 1) / kChunk);
+  // Units are strided over the blocks; when their count is a multiple of the
+  // chunks per row, each block would take the same chunk of every row it
+  // visits, which measured 0.69-0.77 of the copy bandwidth against 0.96-1.05
+  // otherwise (top-5, 7, 10, 14 and 15 at H = 7168): one block then sits out.
+  b.nw = (int64_t)sms * per_sm;
+  if (b.nchunk > 1 && b.nw % b.nchunk == 0) b.nw -= 1;
+  return launch_pdl(f, sms * per_sm, 32, smem, st, false, b, rows);
 }
 
 // K with a register-tuned batch shape (combine_kernel); every other K up to
 // 32 takes the staged kernel (direct combine only).
-bool staged_k(int K) {
-  return !(K == 1 || K == 2 || K == 3 || K == 4 || K == 6 || K == 8 || K == 10);
-}
+bool staged_k(int K) { return !(K == 1 || K == 2 || K == 3 || K == 4 || K == 6 || K == 8); }
 
 template <class Rows>
 cudaError_t launch_staged(const Args &a, const Rows &rows, int sms, cudaStream_t st) {
-  const int per_sm = staged_blocks_per_sm<Rows>(a.K);
-  if (per_sm <= 0) return cudaErrorInvalidConfiguration;
-  Args b = a;
-  b.nchunk = (int)((int64_t)a.H8 * 16 + kStageChunk - 1) / kStageChunk;
-  return launch_pdl(combine_staged_kernel<Rows>, sms * per_sm, 32, staged_smem(a.K), st, false,
-                    b, rows);
+  const StageShape sh = stage_shape(a.K);
+  if (sh.chunk == 1024) return launch_staged_shape<1024, 2>(a, rows, sms, st);
+  return launch_staged_shape<2048, 2>(a, rows, sms, st);
 }
 
 // Batch shape per K (vectors per lane, threads per block, rows per batch),
@@ -437,6 +459,7 @@ Args make_args(const moonep_ctx *ctx, const moonep_comm_plan *plan, int64_t ntok
   a.NvS = ctx->NvS;
   const int bt = c.K == 1 ? 256 : 128;
   a.interleave = ntok * a.nchunk <= 4 * (int64_t)ctx->sms * ctx->blocks_combine * (bt / 32);
+  a.nw = 0;
   return a;
 }
 

@@ -7,7 +7,8 @@ same kind of values go through the kernels:
   or 2^20 (k = K-1), scaled per column by a power of two.  In k order the
   small terms land exactly below 2^20 and survive ((K-2)*2^-4); any order
   that adds 2^20 before them drops them at the tie.  Every K the library
-  specialises (2, 3, 4, 6, 8, 10) and the runtime-K kernel (5, 12) [vLLM,
+  specialises (2, 3, 4, 6, 8) and the shared-memory staged kernel in both of
+  its chunk sizes (5, 10, 12 with 2 KB, 14, 16, 24 with 1 KB) [vLLM,
   finalize(): the unweighted K-sum, accumulated in k order in fp32].
 * the deduplicated combine's fold and primaries sum, on the same values
   [API, Buffer.combine: duplicates accumulated into primaries in fp32].
@@ -55,7 +56,7 @@ def _tie_rows(dst, K, NvS_total, H):
     return y
 
 
-@pytest.mark.parametrize("K", [2, 3, 4, 5, 6, 8, 10, 12])
+@pytest.mark.parametrize("K", [2, 3, 4, 5, 6, 8, 10, 12, 14, 16, 24])
 @pytest.mark.parametrize("dedup", [False, True])
 def test_combine_order_sensitive_values(K, dedup):
     from combine_moonep_plan_gb300.api import Buffer

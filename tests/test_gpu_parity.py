@@ -208,6 +208,21 @@ def test_wide_and_odd_top_k(K):
     _full_pipeline(sh, topk, K)
 
 
+@pytest.mark.parametrize("K", [5, 7, 10, 14, 20])
+def test_staged_combine_full_width_rows(K):
+    """Top-K without a register-tuned combine: 14 KB rows (H = 7168) in 2 KB
+    (K <= 13) or 1 KB chunks staged through shared memory, with enough
+    tokens that every block takes several units (on 152 SMs the top-7 and
+    top-14 grids are a multiple of the chunks per row, the case where one
+    block sits out)."""
+    sh = wl.Shape("staged", R=4, E=32, K=K, S=48, H=7168, Hp=16, B=8, tp=16, weights="softmax")
+    rng = np.random.default_rng(300 + K)
+    p = rng.random(sh.E) ** 2
+    topk = np.stack([np.stack([rng.choice(sh.E, K, replace=False, p=p / p.sum())
+                               for _ in range(sh.S)]) for _ in range(sh.R)]).astype(np.int32)
+    _full_pipeline(sh, topk, 40 + K)
+
+
 @pytest.mark.parametrize("block", range(4))
 def test_random_wide_configs(block):
     """100 random shapes (up to 16 ranks, top-1..16, 1..12 experts per rank,
