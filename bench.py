@@ -76,6 +76,7 @@ def parse():
                     help="capture one step in a CUDA graph and replay it in the timed region")
     ap.add_argument("--hp", type=int, default=None, help="override H' (profiling case)")
     ap.add_argument("--s", type=int, default=None, help="override S (profiling case)")
+    ap.add_argument("--k", type=int, default=None, help="override K (profiling case)")
     ap.add_argument("--profile-op", default=None,
                     help="comma list of ops (plan,dispatch,combine,prefetch,reduce,"
                          "dispatch_dedup,combine_dedup): "
@@ -672,7 +673,9 @@ def host_info():
 
 def recorded_traffic(op, config):
     """DRAM bytes per launch of `op` on `config` from profiles/traffic.md, if
-    the kernel's source is unchanged since the capture (else None)."""
+    the kernel's source files are unchanged since the capture (else None).
+    The table's source column lists the files joined by '+', the sha1 column
+    the SHA-1 of their concatenated contents."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
@@ -681,10 +684,14 @@ def recorded_traffic(op, config):
         cells = [c.strip() for c in line.strip().strip("|").split("|")]
         if len(cells) < 5 or cells[0] != op or cells[1] != config:
             continue
-        src = os.path.join(ROOT, cells[3])
-        if not os.path.exists(src):
-            return None
-        if hashlib.sha1(open(src, "rb").read()).hexdigest() != cells[4]:
+        h = hashlib.sha1()
+        for rel in cells[3].split("+"):
+            src = os.path.join(ROOT, rel.strip())
+            if not os.path.exists(src):
+                return None
+            with open(src, "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != cells[4]:
             return None
         return int(cells[2])
     return None
@@ -719,6 +726,8 @@ def profile_ops(args, sh, point, seed):
         sh = dataclasses.replace(sh, Hp=args.hp)
     if args.s:
         sh = dataclasses.replace(sh, S=args.s)
+    if args.k:
+        sh = dataclasses.replace(sh, K=args.k)
     ops = args.profile_op.split(",")
     R, S, K, E, H, B, Hp = sh.R, sh.S, sh.K, sh.E, sh.H, sh.B, sh.Hp
     topk_np, info = make_routing(sh, point, seed)
@@ -835,6 +844,9 @@ def measure_config(name, args, torch, peak, seed_idx=0, steps=None):
     n = steps or max(args.steps, 20)
     total, per_op, chain, _ = timed_steps(step, n, torch, None)
     summ = summarise(step, sh, total, per_op, chain, n, peak)
+    nb = max(20, min(n, 200))
+    b2b = time_chain(step, nb, torch)
+    b2b_graph = time_chain(step, nb, torch, graph=True) if sh.S * sh.R <= 4096 else None
     status = buf.get_status()
     out = {"workload": workload_config(sh, point)["workload"], "maxvio": round(info["maxvio"], 4),
            "plan_dispatch_combine_tokens_per_s": summ["tokens_per_s"],
@@ -844,6 +856,9 @@ def measure_config(name, args, torch, peak, seed_idx=0, steps=None):
            "dispatch_frac_of_peak": summ["ops"]["dispatch"]["frac_of_peak"],
            "combine_frac_of_peak": summ["ops"]["combine"]["frac_of_peak"],
            "whole_step": summ["whole_step"], "ops": summ["ops"], "steps": n,
+           "back_to_back_chain": {
+               "ms": round(b2b, 5), "tokens_per_s": R_S(sh) / (b2b / 1e3),
+               "graph_ms": round(b2b_graph, 5) if b2b_graph else None},
            "device_status": status}
     del step
     buf.destroy()
