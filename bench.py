@@ -79,7 +79,7 @@ def parse():
     ap.add_argument("--k", type=int, default=None, help="override K (profiling case)")
     ap.add_argument("--profile-op", default=None,
                     help="comma list of ops (plan,dispatch,combine,prefetch,reduce,"
-                         "dispatch_dedup,combine_dedup): "
+                         "dispatch_dedup,combine_dedup,prefetch_mxfp4): "
                          "allocate only what they need and run each --steps times "
                          "(a small, self-contained case for profilers; prints timings)")
     args = ap.parse_args()
@@ -748,6 +748,12 @@ def profile_ops(args, sh, point, seed):
         t["wb"] = torch.empty((R, S, K), dtype=torch.float32, device=dev)
     if "prefetch" in ops:
         t["W"] = torch.randn((E + R * B, H, Hp), device=dev).to(torch.bfloat16)
+    if "prefetch_mxfp4" in ops:
+        rows = E + R * B
+        t["mx"] = [torch.randint(0, 256, (rows, H, Hp // 2), dtype=torch.uint8, device=dev)
+                   for _ in range(3)]
+        t["mx"] += [torch.randint(0, 256, (rows, H, Hp // 32), dtype=torch.uint8, device=dev)
+                    for _ in range(3)]
     if "reduce" in ops:
         t["Gh"] = torch.randn((E, H, Hp), device=dev)
         t["Gs"] = torch.randn((R, B, H, Hp), device=dev)
@@ -761,6 +767,8 @@ def profile_ops(args, sh, point, seed):
            "combine_dedup": lambda: buf.combine(plan, t["y"], t["wn"], out=t["out"],
                                                 weights_out=t["wb"], dedup=True),
            "prefetch": lambda: buf.prefetch_weight(plan, t["W"]),
+           "prefetch_mxfp4": lambda: buf.prefetch_weight(plan, *t["mx"][:3],
+                                                         scales=t["mx"][3:]),
            "reduce": lambda: buf.reduce_grad(plan, [t["Gh"]], [t["Gs"]])}
     res = {}
     for op in ops:
@@ -777,7 +785,9 @@ def profile_ops(args, sh, point, seed):
         res[op] = ev0.elapsed_time(ev1) / args.steps
     etc = plan.experts_to_copy.cpu().numpy()
     print(json.dumps({"profile_case": sh.name, "Hp": Hp, "maxvio": info["maxvio"], "ms": res,
-                      "slots_used": int((etc >= 0).sum()), "status": buf.get_status()}),
+                      "slots_used": int((etc >= 0).sum()),
+                      "experts_with_copies": len(np.unique(etc[etc >= 0])),
+                      "status": buf.get_status()}),
           flush=True)
 
 
