@@ -52,6 +52,12 @@ CASES = [
                         weights="softmax"), "zipf", 1.3),
     ("r4_k3_small_b", wl.Shape("r4", R=4, E=16, K=3, S=77, H=136, Hp=8, B=4, tp=4,
                                weights="softmax"), "zipf", 2.5),
+    # top-K that the combine stages through shared memory (2 KB and 1 KB
+    # chunks), rows of several chunks
+    ("r4_k5_staged", wl.Shape("r4k5", R=4, E=32, K=5, S=120, H=2048, Hp=8, B=8, tp=8,
+                              weights="softmax"), "zipf", 1.2),
+    ("r8_k14_staged", wl.Shape("r8k14", R=8, E=64, K=14, S=64, H=1024, Hp=8, B=8, tp=16,
+                               weights="softmax"), "zipf", 1.0),
 ]
 
 
