@@ -43,14 +43,14 @@ enum {
 // Word offsets of the tables inside plan->internal (see PlanLayout::make).
 // Usable prefetch slots per rank: a rank receives at most one piece, from one
 // home group, so it never fills more than L = E/R slots.
-inline int usable_slots(int R, int E, int B) { return B < E / R ? B : E / R; }
+__host__ __device__ inline int usable_slots(int R, int E, int B) { return B < E / R ? B : E / R; }
 
 // Words of the balance step's tables (shared memory, or the plan's internal
 // area when they do not fit): per expert T, Q, home row base, slot copies and
 // their index (+1 each), per (rank, donor-local expert) slot and row base,
 // experts_to_copy of the usable slots, and per segment (E + R*Bm) valid rows
 // plus two prefix sums.
-inline size_t bal_tables_words(int R, int E, int B) {
+__host__ __device__ inline size_t bal_tables_words(int R, int E, int B) {
   const size_t Bm = (size_t)usable_slots(R, E, B);
   const size_t nseg = (size_t)E + (size_t)R * Bm;
   return 7 * (size_t)E + 2 + (size_t)R * Bm + nseg + 2 * (nseg + 1);

@@ -846,7 +846,19 @@ __device__ bool wait_counter(const unsigned long long *p, unsigned long long tar
 }
 
 size_t fused_smem_words(int R, int E, int B) {
-  return (size_t)kFusedWarps * E + (size_t)E * R + (size_t)E + bal_tables_words(R, E, B);
+  return (size_t)kFusedWarps * E + (size_t)E * R + (size_t)E + bal_tables_words(R, E, B) +
+         (size_t)E;
+}
+
+// A word of block `rank`'s shared memory (distributed shared memory of the
+// cluster), at the address `p` has in this block.
+__device__ __forceinline__ int ld_cluster(const int32_t *p, unsigned rank) {
+  const unsigned la = static_cast<unsigned>(__cvta_generic_to_shared(p));
+  unsigned ra;
+  int v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
 }
 
 // IT routes per thread (1, 2, 4 or 8; tile = 1024 * IT routes).  A compile-time
@@ -874,6 +886,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   int32_t *sCnt = h + kFusedWarps * E;  // [R*E]
   int32_t *sSrc = sCnt + E * R;         // [E]
   const BalTables tb = bal_tables(sSrc + E, d);
+  int32_t *sTile = sSrc + E + bal_tables_words(R, E, d.B);  // [E] this tile's counts
+  // One cluster (whole-problem plans of at most 16 blocks): the blocks read
+  // each other's tile counts and error flags from shared memory after the
+  // cluster barrier, instead of through global totals.
+  const bool dsm = a.cluster && !local;
 
   const int32_t *src = a.topk + (local ? 0 : (int64_t)r * C);
   const unsigned lt = lanemask_lt();
@@ -888,7 +905,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     s_bad = 0;
     // parity of this call: the arrival counter reads between this call's
     // first and last arrival (no block of it has seen all arrive yet)
-    s_par = (int)((ld_acquire(a.sync) / (unsigned long long)nblk) & 1ull);
+    s_par = dsm ? 0 : (int)((ld_acquire(a.sync) / (unsigned long long)nblk) & 1ull);
   }
   if (table_block) {
     // the tile blocks add their duplicate counts after the meeting
@@ -926,7 +943,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     if (bad) atomicOr(&s_bad, 1);
     __syncthreads();
     if (tid == 0 && s_bad) {
-      atomicOr(a.errw + s_par, kErrBadExpert);
+      if (!dsm) atomicOr(a.errw + s_par, kErrBadExpert);
       set_status(a.status, MOONEP_ERR_BAD_EXPERT);
     }
     // 2. warp offsets per expert; the tile's histogram; the rank's totals
@@ -937,15 +954,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
         h[w * E + e] = run;
         run += v;
       }
-      a.hist[(int64_t)g * E + e] = run;
-      if (run) atomicAdd(a.totals + ((int64_t)s_par * trows + trow) * E + e, run);
+      if (dsm) {
+        sTile[e] = run;
+      } else {
+        a.hist[(int64_t)g * E + e] = run;
+        if (run) atomicAdd(a.totals + ((int64_t)s_par * trows + trow) * E + e, run);
+      }
     }
-    __threadfence();  // this thread's histogram entries and totals, before the arrival
+    if (!dsm) __threadfence();  // this thread's histogram entries and totals, before the arrival
   }
   __syncthreads();
 
+  // this block's first tokens_per_expert word to check, loaded now so that
+  // its latency overlaps the meeting
+  const int i_tpe = g * kFusedThreads + tid;
+  const int tpe0 = (a.tpe != nullptr && !local && i_tpe < R * E) ? __ldg(a.tpe + i_tpe) : 0;
+
   // 3. all blocks arrive; each waits for the rest
-  if (tid == 0) {
+  if (tid == 0 && dsm) s_ok = 1;
+  if (tid == 0 && !dsm) {
     __threadfence();
     const unsigned long long n = (unsigned long long)nblk;
     const unsigned long long old = atomicAdd(a.sync, 1ull);
@@ -960,7 +987,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   }
-  if (tid == 0) s_err = s_ok ? __ldcg(a.errw + s_par) : 0;
+  if (dsm) {
+    // error flags of the tile blocks, one lane per block
+    if (warp == 0) {
+      const int b = lane < a.G ? ld_cluster(&s_bad, lane) : 0;
+      const unsigned m = __ballot_sync(0xffffffffu, b != 0);
+      if (lane == 0) s_err = m ? kErrBadExpert : 0;
+    }
+  } else if (tid == 0) {
+    s_err = s_ok ? __ldcg(a.errw + s_par) : 0;
+  }
   __syncthreads();
   const bool ok = s_ok;
   if (ok) {
@@ -973,6 +1009,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
       for (int e = g * kFusedThreads + tid; e < E; e += nblk * kFusedThreads)
         if (__ldcg(tot_in + e) != __ldg(a.hist_all + (int64_t)r * E + e))
           set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
+    } else if (dsm) {
+      // rank j's totals: the sum of its tiles' counts (blocks j*tpr ...)
+      for (int i = tid; i < R * E; i += kFusedThreads) {
+        const int j = i / E, e = i - j * E;
+        int v = 0;
+        for (int tt = 0; tt < a.tpr; tt++) v += ld_cluster(sTile + e, j * a.tpr + tt);
+        sCnt[i] = v;
+      }
     } else {
       for (int i = tid; i < R * E; i += kFusedThreads) sCnt[i] = __ldcg(tot_in + i);
     }
@@ -990,8 +1034,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     // tokens_per_expert against the recount, a slice per block: a mismatch
     // latches its error but the plan stands (it is built from the recount)
     if (a.tpe != nullptr && !local)
-      for (int i = g * kFusedThreads + tid; i < R * E; i += nblk * kFusedThreads)
-        if (sCnt[i] != __ldg(a.tpe + i)) set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
+      for (int i = i_tpe; i < R * E; i += nblk * kFusedThreads)
+        if (sCnt[i] != (i == i_tpe ? tpe0 : __ldg(a.tpe + i)))
+          set_status(a.status, MOONEP_ERR_HIST_MISMATCH);
     __syncthreads();
   }
   if (ok) {
@@ -1000,13 +1045,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     // once; balance_route's barriers order the adds before their use)
     for (int i = tid; i < E * t; i += kFusedThreads) {
       const int e = i % E, tt = i / E;
-      atomicAdd(&sSrc[e], __ldcg(a.hist + (int64_t)(gbase + tt) * E + e));
+      atomicAdd(&sSrc[e], dsm ? ld_cluster(sTile + e, gbase + tt)
+                              : __ldcg(a.hist + (int64_t)(gbase + tt) * E + e));
     }
-    balance_route(d, tb, bs, s_err);
   }
+  // this block has read the others' shared memory (the values are in use,
+  // so the reads are done: no ordering needed); each block waits for every
+  // block's arrival before it exits, so its counts outlive the reads
+  if (dsm) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  if (ok) balance_route(d, tb, bs, s_err);
 
   if (list_block) {
     balance_lists(d, tb, bs, a.in, a.lay, ok);
+    if (dsm) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     return;
   }
   if (table_block) {
@@ -1016,6 +1067,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     int32_t *other = a.totals + (int64_t)(1 - s_par) * trows * E;
     for (int i = tid; i < trows * E; i += kFusedThreads) other[i] = 0;
     if (tid == 0) a.errw[1 - s_par] = 0;
+    if (dsm) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     return;
   }
 
@@ -1081,6 +1133,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   __syncthreads();
   for (int i = tid; i < 2 * R; i += kFusedThreads)
     if (sDup[i]) atomicAdd(a.o.dup_counts + i, sDup[i]);
+  if (dsm) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ K4
