@@ -106,7 +106,8 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
   ctx->NvS = (int)nvs_of(c);
   ctx->TPR = (ctx->C + kTile - 1) / kTile;
   ctx->G = c.R * ctx->TPR;
-  ctx->blocks_dispatch = occupancy_dispatch(c.K);
+  ctx->blocks_dispatch = occupancy_dispatch(c.K, false);
+  ctx->blocks_dispatch_small = occupancy_dispatch(c.K, true);
   ctx->blocks_combine = occupancy_combine(c.K);
   ctx->blocks_copy = occupancy_copy();
   ctx->blocks_reduce = occupancy_reduce();

@@ -43,9 +43,9 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Args a, Rows rows) {
   dispatch_units<KT, kU>(a, rows, wid, nw);
 }
 
-template <int KT>
+template <int KT, int U = 8>
 void *kernel_ptr() {
-  return (void *)dispatch_kernel<KT, 8, FlatRows>;
+  return (void *)dispatch_kernel<KT, U, FlatRows>;
 }
 
 template <int KT, class Rows>
@@ -103,10 +103,16 @@ DispatchArgs dispatch_args(const moonep_ctx *ctx, const moonep_comm_plan *plan,
   return a;
 }
 
-int occupancy_dispatch(int K) {
+// Resident blocks per SM of the 4 KB-unit kernel (small_units: the 2 KB-unit
+// kernel, which needs fewer registers, so more of its blocks fit).
+int occupancy_dispatch(int K, bool small_units) {
   int n = 0;
-  void *f = K == 1 ? kernel_ptr<1>() : K == 2 ? kernel_ptr<2>() : K == 4 ? kernel_ptr<4>()
-          : K == 8 ? kernel_ptr<8>() : kernel_ptr<0>();
+  void *f = small_units
+                ? (K == 1 ? kernel_ptr<1, 4>() : K == 2 ? kernel_ptr<2, 4>()
+                   : K == 4 ? kernel_ptr<4, 4>() : K == 8 ? kernel_ptr<8, 4>()
+                            : kernel_ptr<0, 4>())
+                : (K == 1 ? kernel_ptr<1>() : K == 2 ? kernel_ptr<2>() : K == 4 ? kernel_ptr<4>()
+                   : K == 8 ? kernel_ptr<8>() : kernel_ptr<0>());
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess) n = 1;
   return n > 0 ? n : 1;
 }
@@ -115,9 +121,9 @@ int launch_dispatch(moonep_ctx *ctx, const moonep_comm_plan *plan, const uint16_
                     const float *w_sk, uint16_t *out, float *w_out, cudaStream_t st,
                     bool primaries_only) {
   const moonep_config &c = ctx->cfg;
-  const int grid = ctx->sms * ctx->blocks_dispatch;
   const int64_t ntok = (int64_t)c.R * c.S;
-  const int u = unit_vectors(ntok, c.H / 8, grid);
+  const int u = unit_vectors(ntok, c.H / 8, ctx->sms * ctx->blocks_dispatch);
+  const int grid = ctx->sms * (u == 4 ? ctx->blocks_dispatch_small : ctx->blocks_dispatch);
   Args a = dispatch_args(ctx, plan, hidden, w_sk, ntok, 0, 0, c.R * ctx->EB, u);
   a.primaries_only = primaries_only ? 1 : 0;
   if (a.H8 == 0) return MOONEP_OK;
@@ -129,8 +135,8 @@ int launch_dispatch_rank(moonep_ctx *ctx, const moonep_comm_plan *plan, int rank
                          const uint16_t *hidden_r, const float *w_r, uint16_t *const *windows,
                          float *const *w_windows, cudaStream_t st) {
   const moonep_config &c = ctx->cfg;
-  const int grid = ctx->sms * ctx->blocks_dispatch;
-  const int u = unit_vectors(c.S, c.H / 8, grid);
+  const int u = unit_vectors(c.S, c.H / 8, ctx->sms * ctx->blocks_dispatch);
+  const int grid = ctx->sms * (u == 4 ? ctx->blocks_dispatch_small : ctx->blocks_dispatch);
   Args a = dispatch_args(ctx, plan, hidden_r, w_r, c.S, rank, rank * ctx->EB,
                          (rank + 1) * ctx->EB, u);
   if (a.H8 == 0) return MOONEP_OK;
