@@ -109,6 +109,7 @@ int moonep_ctx_create(const moonep_config *cfg, int alloc_views, moonep_ctx **ou
   ctx->blocks_dispatch = occupancy_dispatch(c.K, false);
   ctx->blocks_dispatch_small = occupancy_dispatch(c.K, true);
   ctx->blocks_combine = occupancy_combine(c.K);
+  ctx->blocks_combine_small = occupancy_combine_small(c.K);
   ctx->blocks_copy = occupancy_copy();
   ctx->blocks_reduce = occupancy_reduce();
   ctx->blocks_expand = occupancy_dedup(false);

@@ -110,7 +110,7 @@ struct moonep_ctx {
   int test_planner_timeout;    // test hook: the planner's arrival wait never completes
   int plan_cluster;            // blocks of the whole-problem planner launched as one
                                // cluster (0: a cooperative launch)
-  int blocks_dispatch, blocks_dispatch_small, blocks_combine, blocks_copy, blocks_reduce, blocks_expand,
+  int blocks_dispatch, blocks_dispatch_small, blocks_combine, blocks_combine_small, blocks_copy, blocks_reduce, blocks_expand,
       blocks_fold;  // resident blocks per SM
 };
 
@@ -173,6 +173,7 @@ int64_t plan_rank_totals_offset(int R, int E, int C, int K, int sms);
 int64_t plan_scratch_words(int R, int E, int C, int K, int sms);
 int occupancy_dispatch(int K, bool small_units);
 int occupancy_combine(int K);
+int occupancy_combine_small(int K);
 int occupancy_copy();
 int occupancy_reduce();
 int occupancy_dedup(bool fold);
