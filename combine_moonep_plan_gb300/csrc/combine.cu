@@ -443,16 +443,17 @@ cudaError_t launch_k(const Args &a, const Rows &rows, bool prim, int grid, cudaS
 int unit_vectors(int K) { return (K == 2 || K == 3 || K == 10) ? 8 : 4; }
 
 // Small batches with K = 8 (a few units per warp, the decode step): units of
-// 1 KB of each row, in batches of four rows.  The kernel then needs 92
-// registers instead of 168, so five blocks fit per SM instead of three; at the
-// decode shape the combine inside the step drops from 16.4 to 14.0 us and the
-// plan->dispatch->combine chain from 35.5 to 34.6 us.
+// 1 KB of each row, in batches of two rows.  The kernel then needs 72
+// registers instead of 168, so seven blocks fit per SM instead of three; at
+// the decode shape the combine inside the step drops from 16.4 to 12.5 us and
+// the plan->dispatch->combine chain from 35.5 to 33.7 us (1 KB units in
+// batches of four rows, five blocks per SM: 14.3 and 34.7 us).
 constexpr int kSmallU = 2;
 
 template <class Rows>
 cudaError_t launch_small_k8(Args a, const Rows &rows, bool prim, int grid, cudaStream_t st) {
   a.nchunk = (a.H8 + 32 * kSmallU - 1) / (32 * kSmallU);
-  return launch<8, kSmallU, 128, 4>(a, rows, prim, grid, st);
+  return launch<8, kSmallU, 128, 2>(a, rows, prim, grid, st);
 }
 
 Args make_args(const moonep_ctx *ctx, const moonep_comm_plan *plan, int64_t ntok, int r0,
@@ -482,7 +483,7 @@ int occupancy_combine_small(int K) {
   if (K != 8) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &n, combine_kernel<8, kSmallU, 128, 4, false, FlatRows>, 128, 0) != cudaSuccess) {
+          &n, combine_kernel<8, kSmallU, 128, 2, false, FlatRows>, 128, 0) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
