@@ -913,17 +913,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     __threadfence();
   }
   if (tile) {
+    // this tile's routes, loaded first so that their latency overlaps the
+    // zeroing of the counts
+#pragma unroll
+    for (int c = 0; c < items; c++) {
+      const int i = wbase + c * lpc + lane;
+      e_reg[c] = lane < lpc && i < C ? __ldg(src + i) : -1;
+    }
     for (int i = tid; i < kFusedWarps * E; i += kFusedThreads) h[i] = 0;
     __syncthreads();
 
     // 1. counts and in-warp ordinals
     int32_t *hw = h + warp * E;
     bool bad = false;
-#pragma unroll
-    for (int c = 0; c < items; c++) {
-      const int i = wbase + c * lpc + lane;
-      e_reg[c] = lane < lpc && i < C ? __ldg(src + i) : -1;
-    }
 #pragma unroll
     for (int c = 0; c < items; c++) {
       const int i = wbase + c * lpc + lane;
