@@ -268,15 +268,11 @@ __device__ void block_scan2(int32_t *a, int32_t *b, int cnt, int tp, bool totals
 // padded starts, and the row bases the route assignment needs.  Called by a
 // whole block of kBalThreads threads; err_in holds the error bits found so
 // far.  Writes only t and s.
-__device__ void balance_route(const PlanDims &d, const BalTables &t, BalSmall &s, int err_in) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kWarps = kBalThreads / 32;
-  const int R = d.R, E = d.E, L = d.L, B = d.B, Bm = d.Bm, LB = L + Bm, C = d.C;
-
-  if (tid == 0) {
-    s.err = err_in;
-    s.np = 0;
-  }
+// The balance step's initial table values (no input needed, so a caller may
+// run this early, before the per-expert totals are known).
+__device__ __forceinline__ void balance_init(const PlanDims &d, const BalTables &t, BalSmall &s) {
+  const int tid = threadIdx.x;
+  const int R = d.R, L = d.L, Bm = d.Bm, LB = L + Bm;
   for (int i = tid; i < R * L; i += kBalThreads) {
     t.slot_b[i] = -1;
     t.slot_rb[i] = 0;
@@ -290,6 +286,20 @@ __device__ void balance_route(const PlanDims &d, const BalTables &t, BalSmall &s
     s.recv_piece[j] = -1;
     s.nslots[j] = 0;
   }
+}
+
+// inited: balance_init already ran, and a block barrier followed it.
+__device__ void balance_route(const PlanDims &d, const BalTables &t, BalSmall &s, int err_in,
+                              bool inited = false) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kBalThreads / 32;
+  const int R = d.R, E = d.E, L = d.L, B = d.B, Bm = d.Bm, LB = L + Bm, C = d.C;
+
+  if (tid == 0) {
+    s.err = err_in;
+    s.np = 0;
+  }
+  if (!inited) balance_init(d, t, s);
   // Phase B: offset of P_e inside Q_home(e) (one warp per home group), G_j.
   for (int j = warp; j < R; j += kWarps) {
     int carry = 0;
@@ -912,6 +922,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
     for (int i = tid; i < 2 * R; i += kFusedThreads) a.o.dup_counts[i] = 0;
     __threadfence();
   }
+  // the balance step's initial tables, off its critical path (the barriers
+  // before the balance step order these writes before its reads)
+  balance_init(d, tb, bs);
   if (tile) {
     // this tile's routes, loaded first so that their latency overlaps the
     // zeroing of the counts
@@ -1055,7 +1068,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) plan_fused_kernel(FusedArgs 
   // so the reads are done: no ordering needed); each block waits for every
   // block's arrival before it exits, so its counts outlive the reads
   if (dsm) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  if (ok) balance_route(d, tb, bs, s_err);
+  if (ok) balance_route(d, tb, bs, s_err, true);
 
   if (list_block) {
     balance_lists(d, tb, bs, a.in, a.lay, ok);
